@@ -1,0 +1,178 @@
+"""fp64 CPU oracle for the Mamba selective scan and selective state update.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline leg may import this package.  It shares no code
+with the CUDA path: ``oracle.c`` is plain C built with gcc (``-O2``, no
+fast-math, OpenMP over channels) and loaded here through ctypes.
+
+Every function takes numpy arrays, upcasts them to float64 exactly, and
+returns float64 results.  Shapes follow the listings of "Deep dive into
+Mamba" section 4.4 and the MambaBlock of "State space models and Mamba":
+u, dt_raw, z: (batch, L, d_inner); B, C: (batch, L, d_state);
+A: (d_inner, d_state); D, dt_bias: (d_inner,).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile ``src`` (default oracle.c) into the shared library ``out``."""
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-fno-fast-math", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _f64(x):
+    if x is None:
+        return None
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(x):
+    if x is None:
+        return ctypes.POINTER(ctypes.c_double)()
+    return x.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _dims(u, B):
+    batch, L, d_inner = u.shape
+    d_state = B.shape[-1]
+    return batch, L, d_inner, d_state
+
+
+class Oracle:
+    """ctypes view of one build of oracle.c."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        i64 = ctypes.c_int64
+        lib.oracle_softplus.restype = ctypes.c_double
+        lib.oracle_softplus.argtypes = [ctypes.c_double]
+        lib.oracle_silu.restype = ctypes.c_double
+        lib.oracle_silu.argtypes = [ctypes.c_double]
+        lib.oracle_threads.restype = ctypes.c_int
+        lib.oracle_threads.argtypes = [ctypes.c_int]
+        lib.oracle_scan_fwd.restype = ctypes.c_int
+        lib.oracle_scan_fwd.argtypes = [dp] * 11 + [i64] * 4 + [ctypes.c_int]
+        lib.oracle_state_update.restype = ctypes.c_int
+        lib.oracle_state_update.argtypes = [dp] * 10 + [i64] * 3 + [ctypes.c_int]
+        lib.oracle_scan_fwd_segmented.restype = ctypes.c_int
+        lib.oracle_scan_fwd_segmented.argtypes = ([dp] * 10 + [i64] * 5
+                                                  + [ctypes.c_int])
+        self.lib = lib
+        self.path = lib_path
+
+    def threads(self, nthreads: int = 0) -> int:
+        """Number of OpenMP threads a call with ``nthreads`` uses (0 = all)."""
+        return int(self.lib.oracle_threads(int(nthreads)))
+
+    def softplus(self, x: float) -> float:
+        """log(1 + e^x), evaluated without overflow (scalar)."""
+        return float(self.lib.oracle_softplus(float(x)))
+
+    def silu(self, z: float) -> float:
+        """z * sigmoid(z) (scalar)."""
+        return float(self.lib.oracle_silu(float(z)))
+
+    def scan_fwd(self, u, dt_raw, A, B, C, D=None, z=None, dt_bias=None,
+                 h0=None, nthreads: int = 0):
+        """Selective scan forward in fp64.  Returns (out, last_state)."""
+        u, dt_raw, A, B, C = map(_f64, (u, dt_raw, A, B, C))
+        D, z, dt_bias, h0 = map(_f64, (D, z, dt_bias, h0))
+        batch, L, d_inner, d_state = _dims(u, B)
+        out = np.zeros((batch, L, d_inner), dtype=np.float64)
+        last = np.zeros((batch, d_inner, d_state), dtype=np.float64)
+        rc = self.lib.oracle_scan_fwd(
+            _ptr(u), _ptr(dt_raw), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+            _ptr(z), _ptr(dt_bias), _ptr(h0), _ptr(out), _ptr(last), batch,
+            L, d_inner, d_state, int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_scan_fwd rejected its sizes")
+        return out, last
+
+    def scan_fwd_segmented(self, u, dt_raw, A, B, C, D=None, z=None,
+                           dt_bias=None, seg: int = 64, nthreads: int = 0):
+        """Segmented scan with the associative merge -> (out, last_state)."""
+        u, dt_raw, A, B, C = map(_f64, (u, dt_raw, A, B, C))
+        D, z, dt_bias = map(_f64, (D, z, dt_bias))
+        batch, L, d_inner, d_state = _dims(u, B)
+        out = np.zeros((batch, L, d_inner), dtype=np.float64)
+        last = np.zeros((batch, d_inner, d_state), dtype=np.float64)
+        rc = self.lib.oracle_scan_fwd_segmented(
+            _ptr(u), _ptr(dt_raw), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+            _ptr(z), _ptr(dt_bias), _ptr(out), _ptr(last), batch, L,
+            d_inner, d_state, int(seg), int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_scan_fwd_segmented rejected its sizes")
+        return out, last
+
+    def state_update(self, state, u, dt_raw, A, B, C, D=None, z=None,
+                     dt_bias=None, nthreads: int = 0):
+        """One decode step in fp64 -> (new_state, out); inputs untouched.
+
+        state: (batch, d_inner, d_state); u, dt_raw, z: (batch, d_inner);
+        B, C: (batch, d_state).
+        """
+        st = np.array(state, dtype=np.float64, copy=True, order="C")
+        u, dt_raw, A, B, C = map(_f64, (u, dt_raw, A, B, C))
+        D, z, dt_bias = map(_f64, (D, z, dt_bias))
+        batch, d_inner, d_state = st.shape
+        out = np.zeros((batch, d_inner), dtype=np.float64)
+        rc = self.lib.oracle_state_update(
+            _ptr(st), _ptr(u), _ptr(dt_raw), _ptr(A), _ptr(B), _ptr(C),
+            _ptr(D), _ptr(z), _ptr(dt_bias), _ptr(out), batch, d_inner,
+            d_state, int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_state_update rejected its sizes")
+        return st, out
+
+
+_default = None
+
+
+def default() -> Oracle:
+    """The oracle built from oracle.c (compiled on first use)."""
+    global _default
+    if _default is None:
+        _default = Oracle(build())
+    return _default
+
+
+def threads(nthreads: int = 0) -> int:
+    return default().threads(nthreads)
+
+
+def softplus(x: float) -> float:
+    return default().softplus(x)
+
+
+def silu(z: float) -> float:
+    return default().silu(z)
+
+
+def scan_fwd(*args, **kwargs):
+    return default().scan_fwd(*args, **kwargs)
+
+
+def scan_fwd_segmented(*args, **kwargs):
+    return default().scan_fwd_segmented(*args, **kwargs)
+
+
+def state_update(*args, **kwargs):
+    return default().state_update(*args, **kwargs)

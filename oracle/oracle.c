@@ -1,0 +1,225 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for the Mamba selective scan (S6)
+ * and the single-token selective state update.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link or
+ * call this file: only tests/, __graft_entry__.smoke() and bench.py's CPU
+ * baseline leg use it.  It shares no code, header, table or constant with the
+ * CUDA path.
+ *
+ * What it computes (sources are web pages on the subject; cited by page title
+ * and section):
+ *   - "Deep dive into Mamba: architecture and implementation of selective
+ *     state-space models" (aiattnstudio.link/posts/mamba), section 4.4
+ *     (complete selective scan) and section 5.2 (the block's selective scan):
+ *     dA = exp(delta*A), dB*u = delta*B*u, sequential h = dA*h + dB*u starting
+ *     from a zero fp32 state, y = sum_n C*h, y += D*u.
+ *   - "State space models and Mamba" (metaphor-xennon.pages.dev), the
+ *     MambaBlock listing: delta = softplus(.) of the dt projection (whose
+ *     Linear carries a bias, here dt_bias), the same scan with
+ *     y = einsum('bdn,bn->bd', h, C), then the gate y * silu(z).
+ *   - Mamba paper-presentation article (hnwysp.cn/news/102080), section 3.2:
+ *     h_t = a_t*h_{t-1} + b_t is associative, so the sequence can be cut into
+ *     segments, each run serially from a zero state, keeping the segment-end
+ *     state and the segment's transfer coefficient, then merged by a prefix
+ *     scan (oracle_scan_fwd_segmented).
+ *
+ * Readings taken where the pages are silent or disagree (each is listed in
+ * the design notes):
+ *   - dB = delta*B (the form all listings use), not the zero-order-hold B.
+ *   - y_t sees u_t: h_t = dA_t*h_{t-1} + dB_t*u_t, y_t = C_t . h_t.
+ *   - softplus is applied exactly once, to dt_raw + dt_bias; it is evaluated
+ *     exactly (no large-x threshold).
+ *   - the D skip and the gate are applied in full precision, gate after skip.
+ *   - the initial state is zero unless h0 is given (h0 is an extension used
+ *     for split prefill; NULL means zero).
+ *
+ * All arrays are row-major and contiguous, fp64:
+ *   u, dt_raw, z, out : (batch, L, d_inner)
+ *   B, C              : (batch, L, d_state)
+ *   A                 : (d_inner, d_state)
+ *   D, dt_bias        : (d_inner)              nullable -> 0 / no bias
+ *   h0, last_state    : (batch, d_inner, d_state) nullable
+ *   z                 : nullable -> no gate
+ * Built with -O2, no fast-math, libm exp/log1p.  OpenMP over the independent
+ * (batch, channel) pairs; nthreads <= 0 means the OpenMP default.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* softplus(x) = log(1 + e^x), written so that neither branch overflows. */
+double oracle_softplus(double x) {
+    if (x > 0.0) return x + log1p(exp(-x));
+    return log1p(exp(x));
+}
+
+/* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
+double oracle_silu(double z) {
+    return z / (1.0 + exp(-z));
+}
+
+static int set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) return nthreads;
+    return omp_get_max_threads();
+#else
+    (void)nthreads;
+    return 1;
+#endif
+}
+
+/* Number of OpenMP threads a call with `nthreads` would use. */
+int oracle_threads(int nthreads) { return set_threads(nthreads); }
+
+/*
+ * One channel (b, d) over the time range [t0, t1), starting from state h
+ * (length d_state, updated in place).  Writes out[b, t, d] when out != NULL.
+ * This is the body shared by every oracle entry point below; it is the
+ * sequential recurrence of the listings, one time step after the other.
+ */
+static void scan_channel(const double* u, const double* dt_raw, const double* A,
+                         const double* B, const double* C, const double* D,
+                         const double* z, const double* dt_bias, double* out,
+                         double* h, int64_t b, int64_t d, int64_t t0, int64_t t1,
+                         int64_t L, int64_t d_inner, int64_t d_state) {
+    const double bias = dt_bias ? dt_bias[d] : 0.0;
+    const double skip = D ? D[d] : 0.0;
+    for (int64_t t = t0; t < t1; ++t) {
+        const int64_t i = (b * L + t) * d_inner + d;      /* (b, t, d) */
+        const int64_t r = (b * L + t) * d_state;          /* (b, t, :) */
+        const double delta = oracle_softplus(dt_raw[i] + bias);
+        const double ut = u[i];
+        double y = 0.0;
+        for (int64_t n = 0; n < d_state; ++n) {
+            const double dA = exp(delta * A[d * d_state + n]);
+            const double dBu = delta * B[r + n] * ut;
+            h[n] = dA * h[n] + dBu;
+            y += C[r + n] * h[n];
+        }
+        y += skip * ut;
+        if (z) y *= oracle_silu(z[i]);
+        if (out) out[i] = y;
+    }
+}
+
+/*
+ * Selective scan forward: every output y[b, t, d] and the final state.
+ * Returns 0, or -1 on a bad size.
+ */
+int oracle_scan_fwd(const double* u, const double* dt_raw, const double* A,
+                    const double* B, const double* C, const double* D,
+                    const double* z, const double* dt_bias, const double* h0,
+                    double* out, double* last_state, int64_t batch, int64_t L,
+                    int64_t d_inner, int64_t d_state, int nthreads) {
+    if (batch < 0 || L < 0 || d_inner < 0 || d_state < 1) return -1;
+    const int64_t nch = batch * d_inner;
+    const int nt = set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+    for (int64_t c = 0; c < nch; ++c) {
+        const int64_t b = c / d_inner, d = c % d_inner;
+        double* h = (double*)malloc((size_t)d_state * sizeof(double));
+        for (int64_t n = 0; n < d_state; ++n)
+            h[n] = h0 ? h0[c * d_state + n] : 0.0;
+        scan_channel(u, dt_raw, A, B, C, D, z, dt_bias, out, h, b, d, 0, L, L,
+                     d_inner, d_state);
+        if (last_state)
+            memcpy(last_state + c * d_state, h, (size_t)d_state * sizeof(double));
+        free(h);
+    }
+    return 0;
+}
+
+/*
+ * Single-token decode step: the same update with L = 1, the state read from
+ * and written back to `state` (batch, d_inner, d_state) in place.  Inputs u,
+ * dt_raw, z, out are (batch, d_inner); B, C are (batch, d_state).
+ */
+int oracle_state_update(double* state, const double* u, const double* dt_raw,
+                        const double* A, const double* B, const double* C,
+                        const double* D, const double* z, const double* dt_bias,
+                        double* out, int64_t batch, int64_t d_inner,
+                        int64_t d_state, int nthreads) {
+    if (batch < 0 || d_inner < 0 || d_state < 1) return -1;
+    const int64_t nch = batch * d_inner;
+    const int nt = set_threads(nthreads);
+#pragma omp parallel for schedule(static) num_threads(nt)
+    for (int64_t c = 0; c < nch; ++c) {
+        const int64_t b = c / d_inner, d = c % d_inner;
+        scan_channel(u, dt_raw, A, B, C, D, z, dt_bias, out, state + c * d_state,
+                     b, d, 0, 1, 1, d_inner, d_state);
+    }
+    return 0;
+}
+
+/*
+ * Segmented form of the same scan (presentation article, section 3.2; the
+ * chunk + recompute scheme of "Deep dive into Mamba" section 7.3):
+ *   1. cut [0, L) into segments of `seg` steps;
+ *   2. run each segment serially from a zero state, keeping its end state
+ *      b_k and its transfer coefficient a_k = prod of dA over the segment;
+ *   3. merge the segments in order with the associative combine
+ *      (a1, b1) then (a2, b2)  ->  (a2*a1, a2*b1 + b2), which gives the
+ *      state entering every segment;
+ *   4. rerun every segment from its entering state to emit the outputs.
+ * It must agree with oracle_scan_fwd up to fp64 rounding.
+ */
+int oracle_scan_fwd_segmented(const double* u, const double* dt_raw,
+                              const double* A, const double* B, const double* C,
+                              const double* D, const double* z,
+                              const double* dt_bias, double* out,
+                              double* last_state, int64_t batch, int64_t L,
+                              int64_t d_inner, int64_t d_state, int64_t seg,
+                              int nthreads) {
+    if (batch < 0 || L < 0 || d_inner < 0 || d_state < 1 || seg < 1) return -1;
+    const int64_t nseg = (L + seg - 1) / seg;
+    const int64_t nch = batch * d_inner;
+    const int nt = set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+    for (int64_t c = 0; c < nch; ++c) {
+        const int64_t b = c / d_inner, d = c % d_inner;
+        const double bias = dt_bias ? dt_bias[d] : 0.0;
+        double* a_seg = (double*)calloc((size_t)(nseg * d_state) + 1, sizeof(double));
+        double* b_seg = (double*)calloc((size_t)(nseg * d_state) + 1, sizeof(double));
+        double* h = (double*)calloc((size_t)d_state, sizeof(double));
+        /* step 2: per-segment summary from a zero state */
+        for (int64_t k = 0; k < nseg; ++k) {
+            const int64_t t0 = k * seg, t1 = (t0 + seg < L) ? t0 + seg : L;
+            for (int64_t n = 0; n < d_state; ++n) {
+                double a = 1.0, s = 0.0;
+                for (int64_t t = t0; t < t1; ++t) {
+                    const int64_t i = (b * L + t) * d_inner + d;
+                    const int64_t r = (b * L + t) * d_state;
+                    const double delta = oracle_softplus(dt_raw[i] + bias);
+                    const double dA = exp(delta * A[d * d_state + n]);
+                    s = dA * s + delta * B[r + n] * u[i];
+                    a = dA * a;
+                }
+                a_seg[k * d_state + n] = a;
+                b_seg[k * d_state + n] = s;
+            }
+        }
+        /* step 3: in-order merge; h holds the state entering segment k */
+        for (int64_t k = 0; k < nseg; ++k) {
+            const int64_t t0 = k * seg, t1 = (t0 + seg < L) ? t0 + seg : L;
+            double* hk = (double*)malloc((size_t)d_state * sizeof(double));
+            memcpy(hk, h, (size_t)d_state * sizeof(double));
+            /* step 4: rerun the segment from its entering state */
+            scan_channel(u, dt_raw, A, B, C, D, z, dt_bias, out, hk, b, d, t0,
+                         t1, L, d_inner, d_state);
+            free(hk);
+            for (int64_t n = 0; n < d_state; ++n)
+                h[n] = a_seg[k * d_state + n] * h[n] + b_seg[k * d_state + n];
+        }
+        if (last_state)
+            memcpy(last_state + c * d_state, h, (size_t)d_state * sizeof(double));
+        free(a_seg);
+        free(b_seg);
+        free(h);
+    }
+    return 0;
+}

@@ -1,0 +1,273 @@
+"""Pins that tie the fp64 oracle to facts outside itself.
+
+Each check takes an oracle object (``oracle.Oracle``) so that the same checks
+can be run against builds of the oracle with a planted mistake
+(tests/test_oracle_mutants.py): every plausible mistake must fail at least
+one of them.  None of these checks re-types the oracle's loop; each uses a
+different evaluation that the pages or plain mathematics fix:
+
+  * softplus / silu identities and values (inverse of the bias recipe,
+    softplus(x) - softplus(-x) = x, silu via tanh);
+  * the unrolled state-space/attention dual sum ("Deep dive into Mamba"
+    section 6.1 and the formula summary of section 12), evaluated with
+    cumulative sums of the step size instead of running products;
+  * the LTI special case as a causal convolution with kernel
+    K = (C.B', C.A'.B', C.A'^2.B', ...) (presentation article, section 2.1);
+  * the geometric-series closed form for a constant scalar system;
+  * segmented scan == sequential scan (presentation article, section 3.2);
+  * the dt -> 0 and dt -> infinity limits (presentation article, 4.1);
+  * decode steps == scan ("State space models and Mamba", Mamba decoding);
+  * the stability bound |h| <= sum |dt B u| when A < 0;
+  * a hand-worked example with exactly representable decays
+    (tests/golden/hand_worked_l3_n2.json).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+from selective_state_space_144_b300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def rel_l2(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = float(np.linalg.norm(ref.ravel()))
+    num = float(np.linalg.norm((got - ref).ravel()))
+    if den == 0.0:
+        return num
+    return num / den
+
+
+def _softplus_np(x):
+    # library routine: log(e^0 + e^x)
+    return np.logaddexp(0.0, np.asarray(x, dtype=np.float64))
+
+
+def _silu_np(z):
+    z = np.asarray(z, dtype=np.float64)
+    return z * 0.5 * (1.0 + np.tanh(0.5 * z))
+
+
+def _random_case(batch, L, d_inner, d_state, seed, with_z=True):
+    x = synth.scan_inputs(batch, L, d_inner, d_state, dtype="f32", seed=seed,
+                          D="normal", A_kind="random", with_z=with_z)
+    # make the bias channel-dependent and the skip non-trivial
+    return x
+
+
+# --------------------------------------------------------------------------
+def check_softplus(orc):
+    for v in (1e-3, 0.0123, 0.1, 0.5, 3.0):
+        got = orc.softplus(math.log(math.expm1(v)))
+        assert abs(got - v) <= 1e-14 * v + 1e-300, (v, got)
+    assert abs(orc.softplus(0.0) - math.log(2.0)) <= 1e-16
+    for x in (-30.0, -5.0, -0.3, 0.7, 12.0, 40.0):
+        d = orc.softplus(x) - orc.softplus(-x)
+        assert abs(d - x) <= 1e-14 * max(1.0, abs(x)), (x, d)
+    assert orc.softplus(800.0) == 800.0
+    assert 0.0 <= orc.softplus(-800.0) < 1e-300
+
+
+def check_silu(orc):
+    assert orc.silu(0.0) == 0.0
+    for zv in (-20.0, -3.0, -0.4, 0.25, 1.5, 9.0):
+        ref = float(_silu_np(zv))
+        assert abs(orc.silu(zv) - ref) <= 1e-14 * max(1.0, abs(ref)), zv
+        assert abs(orc.silu(zv) - orc.silu(-zv) - zv) <= 1e-14 * max(1, abs(zv))
+
+
+def _dual_form(x, h0=None):
+    """y via the unrolled sum over j <= t of C_t (prod_{l=j+1..t} dA_l) dB_j u_j,
+    the products taken as exp(A * (S_t - S_j)) with S the running sum of the
+    step sizes; plus the h0 term exp(A * S_t) h0; then D*u and the gate."""
+    u = x.u.astype(np.float64)
+    batch, L, d_inner = u.shape
+    N = x.B.shape[-1]
+    A = x.A.astype(np.float64)
+    Bm = x.B.astype(np.float64)
+    Cm = x.C.astype(np.float64)
+    bias = 0.0 if x.dt_bias is None else x.dt_bias.astype(np.float64)
+    delta = _softplus_np(x.dt_raw.astype(np.float64) + bias)
+    S = np.cumsum(delta, axis=1)                     # (b, t, d), inclusive
+    y = np.zeros((batch, L, d_inner))
+    last = np.zeros((batch, d_inner, N))
+    for b in range(batch):
+        for d in range(d_inner):
+            for t in range(L):
+                acc = 0.0
+                for j in range(t + 1):
+                    w = np.exp(A[d] * (S[b, t, d] - S[b, j, d]))
+                    acc += float(np.sum(Cm[b, t] * w * delta[b, j, d]
+                                        * Bm[b, j] * u[b, j, d]))
+                if h0 is not None:
+                    acc += float(np.sum(Cm[b, t] * np.exp(A[d] * S[b, t, d])
+                                        * h0[b, d]))
+                y[b, t, d] = acc
+            for j in range(L):
+                last[b, d] += (np.exp(A[d] * (S[b, L - 1, d] - S[b, j, d]))
+                               * delta[b, j, d] * Bm[b, j] * u[b, j, d])
+            if h0 is not None:
+                last[b, d] += np.exp(A[d] * S[b, L - 1, d]) * h0[b, d]
+    if x.D is not None:
+        y += x.D.astype(np.float64)[None, None, :] * u
+    if x.z is not None:
+        y *= _silu_np(x.z)
+    return y, last
+
+
+def check_dual_form(orc):
+    x = _random_case(2, 12, 3, 3, seed=11)
+    y_ref, last_ref = _dual_form(x)
+    y, last = orc.scan_fwd(x.u, x.dt_raw, x.A, x.B, x.C, x.D, x.z, x.dt_bias)
+    assert rel_l2(y, y_ref) < 1e-12, rel_l2(y, y_ref)
+    assert rel_l2(last, last_ref) < 1e-12, rel_l2(last, last_ref)
+    # with a given initial state
+    rng = np.random.default_rng(5)
+    h0 = rng.standard_normal((2, 3, 3))
+    y_ref, last_ref = _dual_form(x, h0=h0)
+    y, last = orc.scan_fwd(x.u, x.dt_raw, x.A, x.B, x.C, x.D, x.z, x.dt_bias,
+                           h0=h0)
+    assert rel_l2(y, y_ref) < 1e-12, rel_l2(y, y_ref)
+    assert rel_l2(last, last_ref) < 1e-12, rel_l2(last, last_ref)
+
+
+def check_lti_convolution(orc):
+    """Constant dt, B, C over time: y = K * u + D u with
+    K_k = sum_n C_n exp(k dt A_n) dt B_n, evaluated directly per lag k."""
+    batch, L, d_inner, N = 2, 256, 3, 4
+    rng = np.random.default_rng(7)
+    x = _random_case(batch, L, d_inner, N, seed=12, with_z=False)
+    raw = rng.normal(0.0, 0.5, size=d_inner)
+    x.dt_raw = np.broadcast_to(raw[None, None, :], (batch, L, d_inner)).copy()
+    Bc = rng.standard_normal((batch, N))
+    Cc = rng.standard_normal((batch, N))
+    x.B = np.broadcast_to(Bc[:, None, :], (batch, L, N)).copy()
+    x.C = np.broadcast_to(Cc[:, None, :], (batch, L, N)).copy()
+    y, last = orc.scan_fwd(x.u, x.dt_raw, x.A, x.B, x.C, x.D, None, x.dt_bias)
+    A = x.A.astype(np.float64)
+    dt = _softplus_np(raw + x.dt_bias.astype(np.float64))
+    k = np.arange(L, dtype=np.float64)
+    y_ref = np.zeros((batch, L, d_inner))
+    for b in range(batch):
+        for d in range(d_inner):
+            K = (Cc[b][None, :] * np.exp(k[:, None] * dt[d] * A[d][None, :])
+                 * dt[d] * Bc[b][None, :]).sum(axis=1)
+            ud = x.u[b, :, d].astype(np.float64)
+            y_ref[b, :, d] = np.convolve(K, ud)[:L] + x.D[d] * ud
+    assert rel_l2(y, y_ref) < 1e-12, rel_l2(y, y_ref)
+
+
+def check_geometric_series(orc):
+    """u = B = C = 1, N = 1, constant dt: h_t = dt (1 - a^(t+1)) / (1 - a),
+    a = exp(dt A); y_t = h_t + D."""
+    batch, L, d_inner, N = 1, 40, 2, 1
+    A = np.array([[-0.7], [-2.0]])
+    raw = np.array([0.3, -1.1])
+    Dv = np.array([0.25, -1.5])
+    u = np.ones((batch, L, d_inner))
+    dt_raw = np.broadcast_to(raw, (batch, L, d_inner)).copy()
+    ones = np.ones((batch, L, N))
+    y, last = orc.scan_fwd(u, dt_raw, A, ones, ones, Dv, None, None)
+    dt = _softplus_np(raw)
+    t = np.arange(L, dtype=np.float64)[:, None]
+    a = np.exp(dt * A[:, 0])
+    h = dt * (1.0 - a ** (t + 1)) / (1.0 - a)
+    assert rel_l2(y[0], h + Dv) < 1e-13, rel_l2(y[0], h + Dv)
+    assert rel_l2(last[0, :, 0], h[-1]) < 1e-13
+
+
+def check_segmented_equals_sequential(orc):
+    L = 150
+    x = _random_case(2, L, 3, 4, seed=13)
+    y0, last0 = orc.scan_fwd(x.u, x.dt_raw, x.A, x.B, x.C, x.D, x.z, x.dt_bias)
+    for seg in (1, 3, 64, L, 1000):
+        y, last = orc.scan_fwd_segmented(x.u, x.dt_raw, x.A, x.B, x.C, x.D,
+                                         x.z, x.dt_bias, seg=seg)
+        assert rel_l2(y, y0) < 1e-12, (seg, rel_l2(y, y0))
+        assert rel_l2(last, last0) < 1e-12, (seg, rel_l2(last, last0))
+
+
+def check_dt_limits(orc):
+    x = _random_case(2, 20, 3, 4, seed=14)
+    # dt -> 0: state stays ~0, y -> D u silu(z)
+    small = np.full_like(x.dt_raw, -40.0)
+    y, last = orc.scan_fwd(x.u, small, x.A, x.B, x.C, x.D, x.z, None)
+    assert np.max(np.abs(last)) < 1e-15
+    ref = x.D[None, None, :] * x.u.astype(np.float64) * _silu_np(x.z)
+    assert rel_l2(y, ref) < 1e-12
+    # dt -> infinity with A <= -1: the state forgets everything but the
+    # current input, h_t = dt B_t u_t, y_t = dt (C_t . B_t) u_t + D u_t
+    big = np.full_like(x.dt_raw, 40.0)
+    A = np.minimum(x.A, -1.0)
+    y, last = orc.scan_fwd(x.u, big, A, x.B, x.C, x.D, x.z, None)
+    dt = _softplus_np(40.0)
+    CB = np.sum(x.C.astype(np.float64) * x.B.astype(np.float64), axis=-1)
+    u = x.u.astype(np.float64)
+    ref = (dt * CB[:, :, None] * u + x.D[None, None, :] * u) * _silu_np(x.z)
+    assert rel_l2(y, ref) < 1e-12, rel_l2(y, ref)
+    ref_last = dt * x.B[:, -1, None, :].astype(np.float64) * u[:, -1, :, None]
+    assert rel_l2(last, ref_last) < 1e-12
+
+
+def check_decode_equals_scan(orc):
+    batch, L, d_inner, N = 3, 17, 4, 5
+    x = _random_case(batch, L, d_inner, N, seed=15)
+    y, last = orc.scan_fwd(x.u, x.dt_raw, x.A, x.B, x.C, x.D, x.z, x.dt_bias)
+    st = np.zeros((batch, d_inner, N))
+    for t in range(L):
+        st, o = orc.state_update(st, x.u[:, t], x.dt_raw[:, t], x.A,
+                                 x.B[:, t], x.C[:, t], x.D, x.z[:, t],
+                                 x.dt_bias)
+        assert np.array_equal(o, y[:, t]), t
+    assert np.array_equal(st, last)
+
+
+def check_stability_bound(orc):
+    x = _random_case(2, 300, 3, 4, seed=16)
+    _, last = orc.scan_fwd(x.u, x.dt_raw, x.A, x.B, x.C, x.D, x.z, x.dt_bias)
+    delta = _softplus_np(x.dt_raw.astype(np.float64)
+                         + x.dt_bias.astype(np.float64))
+    bound = np.einsum("btd,btn->bdn", np.abs(delta * x.u),
+                      np.abs(x.B.astype(np.float64)))
+    assert np.all(np.abs(last) <= bound * (1 + 1e-12))
+    # decays strictly inside (0, 1): the state must not simply accumulate
+    assert np.all(np.abs(last) < bound)
+
+
+def check_hand_worked(orc):
+    with open(os.path.join(GOLDEN, "hand_worked_l3_n2.json")) as f:
+        g = json.load(f)
+    inp = g["inputs"]
+    u = np.array(inp["u"], dtype=np.float64).reshape(1, -1, 1)
+    L = u.shape[1]
+    dt_raw = np.zeros((1, L, 1))
+    A = np.array(inp["A"], dtype=np.float64).reshape(1, -1)
+    B = np.array(inp["B"], dtype=np.float64).reshape(1, L, -1)
+    C = np.array(inp["C"], dtype=np.float64).reshape(1, L, -1)
+    D = np.array([inp["D"]], dtype=np.float64)
+    y, last = orc.scan_fwd(u, dt_raw, A, B, C, D, None, None)
+    ln2 = math.log(2.0)
+    y_ref = np.array([p * ln2 + q for p, q in g["expected"]["y"]])
+    last_ref = np.array([p * ln2 for p in g["expected"]["last_state_over_ln2"]])
+    assert np.allclose(y[0, :, 0], y_ref, rtol=1e-14, atol=1e-15), (y, y_ref)
+    assert np.allclose(last[0, 0], last_ref, rtol=1e-14, atol=1e-15)
+
+
+ALL_CHECKS = [
+    check_softplus,
+    check_silu,
+    check_dual_form,
+    check_lti_convolution,
+    check_geometric_series,
+    check_segmented_equals_sequential,
+    check_dt_limits,
+    check_decode_equals_scan,
+    check_stability_bound,
+    check_hand_worked,
+]

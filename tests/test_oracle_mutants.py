@@ -1,0 +1,70 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check
+that the pins catch every one.  The oracle source itself is never changed:
+each mutant is a textual edit of a temporary copy, built with the same flags.
+"""
+import os
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, text in oracle.c, replacement).  Only the first occurrence is edited.
+MUTANTS = [
+    ("dropped_decay", "h[n] = dA * h[n] + dBu;", "h[n] = h[n] + dBu;"),
+    ("decay_sign", "const double dA = exp(delta * A[d * d_state + n]);",
+     "const double dA = exp(-delta * A[d * d_state + n]);"),
+    ("C_for_B_in_output", "y += C[r + n] * h[n];", "y += B[r + n] * h[n];"),
+    ("dropped_delta_in_input", "const double dBu = delta * B[r + n] * ut;",
+     "const double dBu = B[r + n] * ut;"),
+    ("dropped_skip", "y += skip * ut;", ";"),
+    ("gate_without_sigmoid", "if (z) y *= oracle_silu(z[i]);",
+     "if (z) y *= z[i];"),
+    ("sigmoid_sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    ("softplus_as_exp", "return log1p(exp(x));", "return exp(x);"),
+    ("softplus_pos_branch", "if (x > 0.0) return x + log1p(exp(-x));",
+     "if (x > 0.0) return log1p(exp(-x));"),
+    ("A_transposed", "exp(delta * A[d * d_state + n])",
+     "exp(delta * A[n * d_inner + d])"),
+    ("BC_ignore_batch", "const int64_t r = (b * L + t) * d_state;",
+     "const int64_t r = t * d_state;"),
+    ("dropped_bias", "oracle_softplus(dt_raw[i] + bias)",
+     "oracle_softplus(dt_raw[i])"),
+    ("strictly_causal_output",
+     "h[n] = dA * h[n] + dBu;\n            y += C[r + n] * h[n];",
+     "y += C[r + n] * h[n];\n            h[n] = dA * h[n] + dBu;"),
+    ("skip_index", "const double skip = D ? D[d] : 0.0;",
+     "const double skip = D ? D[0] : 0.0;"),
+    ("ignored_h0", "h[n] = h0 ? h0[c * d_state + n] : 0.0;", "h[n] = 0.0;"),
+    ("decode_state_offset", "state + c * d_state,", "state + d * d_state,"),
+    ("segment_transfer_dropped", "a = dA * a;", "a = dA;"),
+    ("segment_merge_no_decay",
+     "h[n] = a_seg[k * d_state + n] * h[n] + b_seg[k * d_state + n];",
+     "h[n] = h[n] + b_seg[k * d_state + n];"),
+    ("segment_rerun_from_zero", "memcpy(hk, h, (size_t)d_state * sizeof(double));",
+     "memset(hk, 0, (size_t)d_state * sizeof(double));"),
+]
+
+
+def _fails_some_pin(orc):
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            check(orc)
+        except Exception:          # an assertion, a NaN comparison, a crash
+            return check.__name__
+    return None
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor missing: {old!r}"
+    mutated = src.replace(old, new, 1)
+    path = tmp_path / f"oracle_{name}.c"
+    path.write_text(mutated)
+    lib = oracle.build(force=True, src=str(path),
+                       out=str(tmp_path / f"liboracle_{name}.so"))
+    caught_by = _fails_some_pin(oracle.Oracle(lib))
+    assert caught_by is not None, f"no pin catches mutant {name}"
