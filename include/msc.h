@@ -1,0 +1,143 @@
+/*
+ * msc.h -- C ABI of the Mamba selective scan (S6) for NVIDIA B300 (sm_103a).
+ *
+ * Two operations, both defined by the web pages on the subject:
+ *
+ *   msc_selective_scan_fwd   -- the selective scan forward of "Deep dive into
+ *     Mamba: architecture and implementation of selective state-space models"
+ *     (aiattnstudio.link/posts/mamba), sections 4.4 and 5.2, with the step
+ *     size delta = softplus(dt + dt_bias) and the output gate y * silu(z) of
+ *     the MambaBlock in "State space models and Mamba"
+ *     (metaphor-xennon.pages.dev):
+ *         delta = softplus(dt[b,t,d] + dt_bias[d])
+ *         h[n]  = exp(delta * A[d,n]) * h[n] + delta * B[b,t,n] * u[b,t,d]
+ *         y     = sum_n C[b,t,n] * h[n] + D[d] * u[b,t,d]
+ *         out[b,t,d] = y * silu(z[b,t,d])             (silu(z) = z*sigmoid(z))
+ *     with h = 0 before t = 0, the state h held in fp32, and the state after
+ *     the last step written to last_state.
+ *
+ *   msc_selective_state_update -- one decode step of the same recurrence
+ *     (the "Mamba decoding" example of "State space models and Mamba":
+ *     constant memory per token), reading and writing the fp32 state in
+ *     place.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers to contiguous row-major arrays.
+ *     The caller owns every buffer; the library never frees caller memory.
+ *   - `dtype` gives the storage type of u, dt, z, B, C and out (fp32 or
+ *     bf16).  A, D, dt_bias, state and last_state are always fp32.  All
+ *     arithmetic is fp32; out is rounded once, to nearest even.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     Argument errors are returned synchronously, before anything is
+ *     launched; launch failures return MSC_ERR_CUDA.  Faults inside a
+ *     kernel surface at the caller's next synchronisation.
+ *   - out must not overlap any input.  Inputs are never written.
+ *   - Pointers must be aligned to their element size; wider alignment
+ *     (16 bytes) selects vector loads, any other alignment still runs on the
+ *     GPU with element loads.  There is no CPU fallback.
+ *   - Supported sizes: batch, L, d_inner >= 0; 1 <= d_state <= 64; every
+ *     array's element count must fit in int64 and the launch grid in 2^31-1
+ *     blocks.  Empty batches are valid and launch nothing.
+ */
+#ifndef MSC_H
+#define MSC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* msc_stream_t;
+
+typedef enum msc_dtype {
+    MSC_F32 = 0,  /* float */
+    MSC_BF16 = 1  /* bfloat16 (1 sign, 8 exponent, 7 mantissa bits) */
+} msc_dtype;
+
+typedef enum msc_status {
+    MSC_OK = 0,
+    MSC_ERR_INVALID_ARG = 1,  /* NULL required pointer, negative size, bad dtype */
+    MSC_ERR_UNSUPPORTED = 2,  /* d_state outside [1, 64], or sizes overflow */
+    MSC_ERR_ALIGNMENT = 3,    /* a pointer not aligned to its element size */
+    MSC_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    MSC_ERR_WORKSPACE = 5     /* workspace NULL or smaller than required */
+} msc_status;
+
+/*
+ * Selective scan forward.
+ *   u, dt, z, out : (batch, L, d_inner), `dtype`       z nullable: no gate
+ *   B, C          : (batch, L, d_state), `dtype`
+ *   A             : (d_inner, d_state) fp32            any real values
+ *   D, dt_bias    : (d_inner) fp32                     nullable: 0
+ *   last_state    : (batch, d_inner, d_state) fp32     nullable: not written
+ * With L == 0 last_state is set to zero.  Scratch for the inter-chunk carry,
+ * when the plan needs it, is taken stream-ordered (cudaMallocAsync /
+ * cudaFreeAsync on `stream`); use msc_selective_scan_fwd_ws to pass it in.
+ */
+msc_status msc_selective_scan_fwd(
+    const void* u, const void* dt, const float* A, const void* B,
+    const void* C, const float* D, const void* z, const float* dt_bias,
+    void* out, float* last_state, int64_t batch, int64_t L, int64_t d_inner,
+    int64_t d_state, msc_dtype dtype, msc_stream_t stream);
+
+/*
+ * Bytes of device workspace msc_selective_scan_fwd_ws needs for these sizes
+ * on the current device (0 when the plan runs in one pass).  The plan, and
+ * so the size, depends on the device's SM count and on msc_tuning_set.
+ */
+msc_status msc_selective_scan_workspace_size(
+    int64_t batch, int64_t L, int64_t d_inner, int64_t d_state,
+    msc_dtype dtype, size_t* bytes);
+
+/*
+ * As msc_selective_scan_fwd, with caller-owned device workspace of at least
+ * msc_selective_scan_workspace_size bytes, 256-byte aligned (NULL allowed
+ * when that size is 0).  Nothing is allocated.  The workspace is scratch:
+ * its contents on entry do not matter, and two calls that share one
+ * workspace must not run concurrently.
+ */
+msc_status msc_selective_scan_fwd_ws(
+    const void* u, const void* dt, const float* A, const void* B,
+    const void* C, const float* D, const void* z, const float* dt_bias,
+    void* out, float* last_state, int64_t batch, int64_t L, int64_t d_inner,
+    int64_t d_state, msc_dtype dtype, void* workspace,
+    size_t workspace_bytes, msc_stream_t stream);
+
+/*
+ * Single-token selective state update (decode).
+ *   state         : (batch, d_inner, d_state) fp32, read and written in place
+ *   u, dt, z, out : (batch, d_inner), `dtype`          z nullable: no gate
+ *   B, C          : (batch, d_state), `dtype`
+ *   A             : (d_inner, d_state) fp32
+ *   D, dt_bias    : (d_inner) fp32                     nullable: 0
+ * out must not overlap state or any input.
+ */
+msc_status msc_selective_state_update(
+    float* state, const void* u, const void* dt, const float* A,
+    const void* B, const void* C, const float* D, const void* z,
+    const float* dt_bias, void* out, int64_t batch, int64_t d_inner,
+    int64_t d_state, msc_dtype dtype, msc_stream_t stream);
+
+/*
+ * Plan overrides, for measurement and tuning.  Keys:
+ *   "scan_chunks"   number of time chunks the scan is cut into (0 = auto)
+ *   "scan_min_chunk" shortest chunk the automatic plan will make (steps)
+ * Process-wide and not thread-safe; returns MSC_ERR_INVALID_ARG for an
+ * unknown key or a negative value.
+ */
+msc_status msc_tuning_set(const char* key, int64_t value);
+
+/* Static description of a status code (never NULL). */
+const char* msc_status_string(msc_status status);
+
+/* Library version, as major*10000 + minor*100 + patch. */
+int msc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSC_H */

@@ -1,0 +1,243 @@
+"""Mamba selective scan (S6) on NVIDIA B300 -- Python binding of libmsc.so.
+
+Argument marshalling only: every step of the computation runs in the sm_103a
+kernels behind the C ABI of ``include/msc.h``.  PyTorch supplies device
+memory and streams.  There is no CPU fallback: if ``libmsc.so`` has not been
+built, every call raises ``RuntimeError``.
+
+    selective_scan_fwd(u, dt, A, B, C, D=None, z=None, dt_bias=None,
+                       out=None, last_state=None, return_last_state=True)
+    selective_state_update(state, u, dt, A, B, C, D=None, z=None,
+                           dt_bias=None, out=None)
+
+Shapes: u, dt, z: (batch, L, d_inner); B, C: (batch, L, d_state);
+A: (d_inner, d_state); D, dt_bias: (d_inner,); state / last_state:
+(batch, d_inner, d_state).  u, dt, z, B, C share one dtype (float32 or
+bfloat16); A, D, dt_bias and the state are float32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "MscError", "selective_scan_fwd", "selective_scan_fwd_ws",
+    "selective_state_update", "scan_workspace_size", "tuning_set",
+    "library_path", "load",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIBNAME = "libmsc.so"
+
+MSC_F32, MSC_BF16 = 0, 1
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported size",
+           3: "pointer not aligned to its element size",
+           4: "CUDA runtime error",
+           5: "workspace missing, too small or misaligned"}
+
+
+class MscError(RuntimeError):
+    """A non-zero msc_status returned by the library."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {_STATUS.get(status, 'unknown status')} "
+                         f"(status {status})")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, _LIBNAME)
+
+
+def load():
+    """Load libmsc.so (once).  Raises RuntimeError when it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with "
+            "`python -m selective_state_space_144_b300.build` "
+            "(there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    st = ctypes.c_int
+    lib.msc_selective_scan_fwd.restype = st
+    lib.msc_selective_scan_fwd.argtypes = [vp] * 10 + [i64] * 4 + [st, vp]
+    lib.msc_selective_scan_fwd_ws.restype = st
+    lib.msc_selective_scan_fwd_ws.argtypes = ([vp] * 10 + [i64] * 4
+                                              + [st, vp, sz, vp])
+    lib.msc_selective_scan_workspace_size.restype = st
+    lib.msc_selective_scan_workspace_size.argtypes = [i64] * 4 + [
+        st, ctypes.POINTER(sz)]
+    lib.msc_selective_state_update.restype = st
+    lib.msc_selective_state_update.argtypes = [vp] * 10 + [i64] * 3 + [st, vp]
+    lib.msc_tuning_set.restype = st
+    lib.msc_tuning_set.argtypes = [ctypes.c_char_p, i64]
+    lib.msc_status_string.restype = ctypes.c_char_p
+    lib.msc_status_string.argtypes = [st]
+    lib.msc_version.restype = ctypes.c_int
+    lib.msc_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise MscError(fn, status)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return MSC_BF16
+    if t.dtype == torch.float32:
+        return MSC_F32
+    raise TypeError(f"unsupported storage dtype {t.dtype} "
+                    "(float32 or bfloat16)")
+
+
+def _ptr(t, name, dtype=None, shape=None, device=None):
+    if t is None:
+        return None
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, "
+                         f"expected {tuple(shape)}")
+    return t.data_ptr()
+
+
+def _stream(device):
+    return _torch().cuda.current_stream(device).cuda_stream
+
+
+def _scan_args(u, dt, A, B, C, D, z, dt_bias, out, last_state,
+               return_last_state):
+    torch = _torch()
+    if u.dim() != 3 or B.dim() != 3:
+        raise ValueError("u must be (batch, L, d_inner), B (batch, L, d_state)")
+    batch, L, d_inner = u.shape
+    d_state = B.shape[-1]
+    dev = u.device
+    code = _dtype_code(u)
+    sdt = u.dtype
+    f32 = torch.float32
+    p = dict(
+        u=_ptr(u, "u", sdt, (batch, L, d_inner), dev),
+        dt=_ptr(dt, "dt", sdt, (batch, L, d_inner), dev),
+        A=_ptr(A, "A", f32, (d_inner, d_state), dev),
+        B=_ptr(B, "B", sdt, (batch, L, d_state), dev),
+        C=_ptr(C, "C", sdt, (batch, L, d_state), dev),
+        D=_ptr(D, "D", f32, (d_inner,), dev),
+        z=_ptr(z, "z", sdt, (batch, L, d_inner), dev),
+        dt_bias=_ptr(dt_bias, "dt_bias", f32, (d_inner,), dev),
+    )
+    if out is None:
+        out = torch.empty((batch, L, d_inner), dtype=sdt, device=dev)
+    p["out"] = _ptr(out, "out", sdt, (batch, L, d_inner), dev)
+    if last_state is None and return_last_state:
+        last_state = torch.empty((batch, d_inner, d_state), dtype=f32,
+                                 device=dev)
+    p["last_state"] = _ptr(last_state, "last_state", f32,
+                           (batch, d_inner, d_state), dev)
+    return p, out, last_state, (batch, L, d_inner, d_state), code, dev
+
+
+def selective_scan_fwd(u, dt, A, B, C, D=None, z=None, dt_bias=None,
+                       out=None, last_state=None, return_last_state=True):
+    """Selective scan forward on the GPU -> (out, last_state).
+
+    Enqueued on the current CUDA stream of u's device; returns at once.
+    Scratch for the inter-chunk carry (when needed) is taken stream-ordered
+    by the library.
+    """
+    lib = load()
+    p, out, last_state, dims, code, dev = _scan_args(
+        u, dt, A, B, C, D, z, dt_bias, out, last_state, return_last_state)
+    st = lib.msc_selective_scan_fwd(
+        p["u"], p["dt"], p["A"], p["B"], p["C"], p["D"], p["z"],
+        p["dt_bias"], p["out"], p["last_state"], *dims, code, _stream(dev))
+    _check("msc_selective_scan_fwd", st)
+    return out, last_state
+
+
+def scan_workspace_size(batch, L, d_inner, d_state, dtype) -> int:
+    """Bytes of workspace selective_scan_fwd_ws needs on the current device."""
+    torch = _torch()
+    code = MSC_BF16 if dtype == torch.bfloat16 else MSC_F32
+    n = ctypes.c_size_t(0)
+    _check("msc_selective_scan_workspace_size",
+           load().msc_selective_scan_workspace_size(
+               batch, L, d_inner, d_state, code, ctypes.byref(n)))
+    return int(n.value)
+
+
+def selective_scan_fwd_ws(u, dt, A, B, C, D=None, z=None, dt_bias=None,
+                          out=None, last_state=None, workspace=None,
+                          return_last_state=True):
+    """As selective_scan_fwd with a caller-owned uint8 CUDA workspace."""
+    lib = load()
+    p, out, last_state, dims, code, dev = _scan_args(
+        u, dt, A, B, C, D, z, dt_bias, out, last_state, return_last_state)
+    wp = _ptr(workspace, "workspace", None, None, dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.msc_selective_scan_fwd_ws(
+        p["u"], p["dt"], p["A"], p["B"], p["C"], p["D"], p["z"],
+        p["dt_bias"], p["out"], p["last_state"], *dims, code, wp, wbytes,
+        _stream(dev))
+    _check("msc_selective_scan_fwd_ws", st)
+    return out, last_state
+
+
+def selective_state_update(state, u, dt, A, B, C, D=None, z=None,
+                           dt_bias=None, out=None):
+    """One decode step on the GPU; updates ``state`` in place -> out."""
+    torch = _torch()
+    lib = load()
+    if state.dim() != 3:
+        raise ValueError("state must be (batch, d_inner, d_state)")
+    batch, d_inner, d_state = state.shape
+    dev = state.device
+    code = _dtype_code(u)
+    sdt = u.dtype
+    f32 = torch.float32
+    if out is None:
+        out = torch.empty((batch, d_inner), dtype=sdt, device=dev)
+    st = lib.msc_selective_state_update(
+        _ptr(state, "state", f32, (batch, d_inner, d_state), dev),
+        _ptr(u, "u", sdt, (batch, d_inner), dev),
+        _ptr(dt, "dt", sdt, (batch, d_inner), dev),
+        _ptr(A, "A", f32, (d_inner, d_state), dev),
+        _ptr(B, "B", sdt, (batch, d_state), dev),
+        _ptr(C, "C", sdt, (batch, d_state), dev),
+        _ptr(D, "D", f32, (d_inner,), dev),
+        _ptr(z, "z", sdt, (batch, d_inner), dev),
+        _ptr(dt_bias, "dt_bias", f32, (d_inner,), dev),
+        _ptr(out, "out", sdt, (batch, d_inner), dev),
+        batch, d_inner, d_state, code, _stream(dev))
+    _check("msc_selective_state_update", st)
+    return out
+
+
+def tuning_set(key: str, value: int):
+    """Process-wide plan override (see msc_tuning_set in include/msc.h)."""
+    _check("msc_tuning_set", load().msc_tuning_set(key.encode(), int(value)))

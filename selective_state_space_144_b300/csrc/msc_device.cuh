@@ -1,0 +1,103 @@
+// msc_device.cuh -- fp32 device arithmetic shared by the scan and decode
+// kernels: the step-size nonlinearity (softplus), the gate (silu), the
+// exponential, and typed loads/stores for fp32 and bf16 storage.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace msc {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x on the MUFU pipe (PTX ex2.approx, flush-to-zero: results below the
+// fp32 normal range become 0, which is the limit the decay tends to).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// log(1 + e) for e in [0, 1] as e * P(2e - 1); P interpolates log1p(e)/e at
+// the 9 Chebyshev nodes of [0, 1] (coefficients from gen_log1p_poly.py).
+// Max relative error about 1.9e-7 in fp32, i.e. accurate where 1 + e
+// rounding would lose the low bits of small e.
+__device__ __forceinline__ float log1p_unit(float e) {
+    const float s = fmaf(2.0f, e, -1.0f);
+    float p = 2.0023837e-05f;
+    p = fmaf(p, s, -6.695044e-05f);
+    p = fmaf(p, s, 0.00018186837f);
+    p = fmaf(p, s, -0.0006321981f);
+    p = fmaf(p, s, 0.0022891003f);
+    p = fmaf(p, s, -0.008463899f);
+    p = fmaf(p, s, 0.033152375f);
+    p = fmaf(p, s, -0.14426334f);
+    p = fmaf(p, s, 0.8109302f);
+    return e * p;
+}
+
+// softplus(x) = log(1 + e^x) = max(x, 0) + log(1 + e^-|x|).  The step size
+// of the selective scan (the Delta of the pages' selection mechanism).
+__device__ __forceinline__ float softplus(float x) {
+    const float e = ex2(-fabsf(x) * kLog2e);
+    return fmaxf(x, 0.0f) + log1p_unit(e);
+}
+
+// silu(z) = z * sigmoid(z) = z / (1 + e^-z).  For z -> -inf the divisor
+// overflows to inf and the fast divide returns 0, the limit of silu.
+__device__ __forceinline__ float silu(float z) {
+    return __fdividef(z, 1.0f + ex2(-z * kLog2e));
+}
+
+// ---- typed element access -------------------------------------------------
+template <typename T> struct Elem;
+
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float load(const float* p) { return __ldg(p); }
+    static __device__ __forceinline__ void store(float* p, float v) { *p = v; }
+    // 4 consecutive elements, p 16-byte aligned
+    static __device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
+        const float4 q = __ldg(reinterpret_cast<const float4*>(p));
+        v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    }
+};
+
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float bits_to_float(uint32_t b16) {
+        return __uint_as_float(b16 << 16);
+    }
+    static __device__ __forceinline__ float load(const __nv_bfloat16* p) {
+        const unsigned short b = __ldg(reinterpret_cast<const unsigned short*>(p));
+        return bits_to_float(b);
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, float v) {
+        *p = __float2bfloat16_rn(v);
+    }
+    // 4 consecutive elements, p 8-byte aligned
+    static __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
+        const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
+        v[0] = __uint_as_float(q.x << 16);
+        v[1] = __uint_as_float(q.x & 0xffff0000u);
+        v[2] = __uint_as_float(q.y << 16);
+        v[3] = __uint_as_float(q.y & 0xffff0000u);
+    }
+};
+
+// Load elements [n0, n0 + 4) of a row of `n` elements into v, zero past n.
+template <typename T, bool VEC>
+__device__ __forceinline__ void load_row4(const T* row, int n0, int n, float (&v)[4]) {
+    if (VEC) {  // n % 4 == 0 and the row 4-element aligned
+        if (n0 < n) {
+            Elem<T>::load4(row + n0, v);
+        } else {
+            v[0] = v[1] = v[2] = v[3] = 0.0f;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            v[j] = (n0 + j < n) ? Elem<T>::load(row + n0 + j) : 0.0f;
+    }
+}
+
+}  // namespace msc

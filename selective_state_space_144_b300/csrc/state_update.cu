@@ -1,0 +1,103 @@
+// state_update.cu -- single-token selective state update (decode) for sm_103a.
+//
+// One step of the scan's recurrence with the state read from and written
+// back to HBM in place (the "Mamba decoding" example of "State space models
+// and Mamba": constant memory per generated token):
+//     delta = softplus(dt + dt_bias);  h = exp(delta*A) * h + delta*B*u
+//     out = (C . h + D*u) * silu(z)
+// The step is bound by streaming the fp32 state (8 bytes per state element
+// per step); a thread owns 4 consecutive states of one channel so that the
+// state moves in 16-byte vectors and a warp touches 512 contiguous bytes.
+#include "msc_device.cuh"
+#include "msc_internal.h"
+
+namespace msc {
+
+template <typename T, int G, bool VEC>
+__global__ void __launch_bounds__(kUpdateThreads)
+state_update_kernel(UpdateArgs a) {
+    const int64_t gid = (int64_t)blockIdx.x * kUpdateThreads + threadIdx.x;
+    const int g = (int)(gid % G);
+    const int64_t nch = a.batch * a.d_inner;
+    const int64_t ch_raw = gid / G;
+    const bool valid = ch_raw < nch;
+    const int64_t ch = valid ? ch_raw : nch - 1;  // idle lanes read in bounds
+    const int64_t b = ch / a.d_inner;
+    const int64_t d = ch - b * a.d_inner;
+    const int N = (int)a.N;
+    const int n0 = g * 4;
+
+    float* srow = a.state + ch * N;
+    float h[4];
+    if (VEC) {
+        if (n0 < N) {
+            const float4 q = *reinterpret_cast<const float4*>(srow + n0);
+            h[0] = q.x; h[1] = q.y; h[2] = q.z; h[3] = q.w;
+        } else {
+            h[0] = h[1] = h[2] = h[3] = 0.0f;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) h[j] = (n0 + j < N) ? srow[n0 + j] : 0.0f;
+    }
+    float A2[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        A2[j] = (n0 + j < N) ? __ldg(a.A + d * N + n0 + j) * kLog2e : 0.0f;
+
+    const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
+    const float x = Elem<T>::load(static_cast<const T*>(a.dt) + ch) + bias;
+    const float uu = Elem<T>::load(static_cast<const T*>(a.u) + ch);
+    const float delta = softplus(x);
+    const float du = delta * uu;
+    float Bv[4], Cv[4];
+    load_row4<T, VEC>(static_cast<const T*>(a.B) + b * N, n0, N, Bv);
+    load_row4<T, VEC>(static_cast<const T*>(a.C) + b * N, n0, N, Cv);
+    float y = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float dA = ex2(delta * A2[j]);
+        h[j] = fmaf(dA, h[j], du * Bv[j]);
+        y = fmaf(Cv[j], h[j], y);
+    }
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+    if (!valid) return;
+    if (VEC) {
+        if (n0 < N)
+            *reinterpret_cast<float4*>(srow + n0) = make_float4(h[0], h[1], h[2], h[3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (n0 + j < N) srow[n0 + j] = h[j];
+    }
+    if (g == 0) {
+        y = fmaf(a.D ? __ldg(a.D + d) : 0.0f, uu, y);
+        if (a.z) y *= silu(Elem<T>::load(static_cast<const T*>(a.z) + ch));
+        Elem<T>::store(static_cast<T*>(a.out) + ch, y);
+    }
+}
+
+template <typename T, bool VEC>
+static cudaError_t launch_update_v(const UpdateArgs& a, cudaStream_t s) {
+    const int G = lanes_per_channel(a.N);
+    const int64_t threads = a.batch * a.d_inner * G;
+    const unsigned nb = (unsigned)((threads + kUpdateThreads - 1) / kUpdateThreads);
+    switch (G) {
+        case 1: state_update_kernel<T, 1, VEC><<<nb, kUpdateThreads, 0, s>>>(a); break;
+        case 2: state_update_kernel<T, 2, VEC><<<nb, kUpdateThreads, 0, s>>>(a); break;
+        case 4: state_update_kernel<T, 4, VEC><<<nb, kUpdateThreads, 0, s>>>(a); break;
+        case 8: state_update_kernel<T, 8, VEC><<<nb, kUpdateThreads, 0, s>>>(a); break;
+        default: state_update_kernel<T, 16, VEC><<<nb, kUpdateThreads, 0, s>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_state_update(const UpdateArgs& a, msc_dtype dtype, cudaStream_t s) {
+    if (dtype == MSC_BF16)
+        return a.vec ? launch_update_v<__nv_bfloat16, true>(a, s)
+                     : launch_update_v<__nv_bfloat16, false>(a, s);
+    return a.vec ? launch_update_v<float, true>(a, s) : launch_update_v<float, false>(a, s);
+}
+
+}  // namespace msc

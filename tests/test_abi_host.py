@@ -1,0 +1,159 @@
+"""The C ABI on the host: the library loads, exports every symbol that
+include/msc.h declares, and rejects bad arguments synchronously, before any
+launch (so none of these tests needs a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import selective_state_space_144_b300 as msc
+from selective_state_space_144_b300 import build as msc_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "msc.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    msc_build.build()
+    return msc.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(msc_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("msc_selective_scan_fwd", "msc_selective_state_update",
+                     "msc_selective_scan_fwd_ws",
+                     "msc_selective_scan_workspace_size", "msc_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libmsc.so does not export {name}"
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = lib.msc_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.msc_status_string(99) == b"unknown status"
+    assert lib.msc_version() >= 100
+
+
+V = ctypes.c_void_p
+FAKE = 0x10000          # never dereferenced: validation fails first
+
+
+def scan(lib, *, u=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None,
+         bias=None, out=FAKE, last=None, batch=2, L=8, d_inner=16, d_state=16,
+         dtype=1):
+    return lib.msc_selective_scan_fwd(u, dt, A, B, C, D, z, bias, out, last,
+                                      batch, L, d_inner, d_state, dtype, None)
+
+
+def test_scan_rejects_bad_sizes(lib):
+    assert scan(lib, d_state=0) == 2
+    assert scan(lib, d_state=65) == 2
+    assert scan(lib, batch=-1) == 1
+    assert scan(lib, L=-1) == 1
+    assert scan(lib, d_inner=-3) == 1
+    assert scan(lib, dtype=7) == 1
+    big = 2**62
+    assert scan(lib, batch=big, L=big) == 2        # element count overflow
+
+
+def test_scan_rejects_null_and_misaligned(lib):
+    assert scan(lib, u=None) == 1
+    assert scan(lib, out=None) == 1
+    assert scan(lib, A=None) == 1
+    assert scan(lib, u=FAKE + 1) == 3              # bf16 needs 2-byte alignment
+    assert scan(lib, u=FAKE + 2, dtype=0) == 3     # fp32 needs 4-byte alignment
+    assert scan(lib, D=FAKE + 2) == 3              # D is fp32
+    assert scan(lib, last=FAKE + 1) == 3
+
+
+def test_scan_empty_is_a_no_op(lib):
+    # nothing to compute: returns OK without touching (fake) pointers
+    assert scan(lib, batch=0) == 0
+    assert scan(lib, d_inner=0) == 0
+
+
+def test_workspace_size_query(lib):
+    n = ctypes.c_size_t(123)
+    assert lib.msc_selective_scan_workspace_size(8, 2048, 1536, 16, 1,
+                                                 ctypes.byref(n)) == 0
+    assert lib.msc_selective_scan_workspace_size(0, 2048, 1536, 16, 1,
+                                                 ctypes.byref(n)) == 0
+    assert n.value == 0
+    assert lib.msc_selective_scan_workspace_size(1, 2048, 1536, 0, 1,
+                                                 ctypes.byref(n)) == 2
+    assert lib.msc_selective_scan_workspace_size(1, 2048, 1536, 16, 1,
+                                                 None) == 1
+    # one chunk -> no carry workspace
+    assert lib.msc_tuning_set(b"scan_chunks", 1) == 0
+    try:
+        assert lib.msc_selective_scan_workspace_size(
+            1, 4096, 64, 16, 1, ctypes.byref(n)) == 0
+        assert n.value == 0
+        assert lib.msc_tuning_set(b"scan_chunks", 4) == 0
+        assert lib.msc_selective_scan_workspace_size(
+            2, 4096, 64, 16, 1, ctypes.byref(n)) == 0
+        assert n.value == 2 * 2 * 3 * 64 * 16 * 4   # (a, b) x batch x (K-1) x D x N
+    finally:
+        lib.msc_tuning_set(b"scan_chunks", 0)
+
+
+def test_workspace_variant_rejects_small_workspace(lib):
+    assert lib.msc_tuning_set(b"scan_chunks", 4) == 0
+    try:
+        st = lib.msc_selective_scan_fwd_ws(
+            FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, None,
+            2, 4096, 64, 16, 1, None, 0, None)
+        assert st == 5
+        st = lib.msc_selective_scan_fwd_ws(
+            FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, None,
+            2, 4096, 64, 16, 1, FAKE + 16, 1 << 30, None)
+        assert st == 5                              # not 256-byte aligned
+    finally:
+        lib.msc_tuning_set(b"scan_chunks", 0)
+
+
+def test_tuning_keys(lib):
+    assert lib.msc_tuning_set(b"no_such_key", 1) == 1
+    assert lib.msc_tuning_set(b"scan_chunks", -1) == 1
+    assert lib.msc_tuning_set(None, 1) == 1
+    assert lib.msc_tuning_set(b"scan_min_chunk", 512) == 0
+
+
+def upd(lib, *, state=FAKE, u=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None,
+        z=None, bias=None, out=FAKE, batch=4, d_inner=16, d_state=16, dtype=1):
+    return lib.msc_selective_state_update(state, u, dt, A, B, C, D, z, bias,
+                                          out, batch, d_inner, d_state, dtype,
+                                          None)
+
+
+def test_state_update_validation(lib):
+    assert upd(lib, d_state=0) == 2
+    assert upd(lib, d_state=100) == 2
+    assert upd(lib, batch=-1) == 1
+    assert upd(lib, state=None) == 1
+    assert upd(lib, out=None) == 1
+    assert upd(lib, state=FAKE + 2) == 3
+    assert upd(lib, z=FAKE + 1) == 3
+    assert upd(lib, dtype=5) == 1
+    assert upd(lib, batch=0) == 0
+
+
+def test_python_binding_fails_loudly_without_cuda_tensors():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 4, 8)
+    with pytest.raises(ValueError):
+        msc.selective_scan_fwd(x, x, torch.zeros(8, 4), torch.zeros(1, 4, 4),
+                               torch.zeros(1, 4, 4))
