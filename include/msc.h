@@ -63,7 +63,9 @@ typedef enum msc_status {
     MSC_ERR_UNSUPPORTED = 2,  /* d_state outside [1, 64], or sizes overflow */
     MSC_ERR_ALIGNMENT = 3,    /* a pointer not aligned to its element size */
     MSC_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
-    MSC_ERR_WORKSPACE = 5     /* workspace NULL or smaller than required */
+    MSC_ERR_WORKSPACE = 5,    /* workspace NULL, smaller than required or misaligned */
+    MSC_ERR_TIMEOUT = 6       /* a kernel gave up waiting for a data copy (see
+                                 msc_check_device_error) */
 } msc_status;
 
 /*
@@ -122,13 +124,39 @@ msc_status msc_selective_state_update(
     int64_t d_state, msc_dtype dtype, msc_stream_t stream);
 
 /*
+ * Kernels never spin without bound: every wait for an asynchronous copy
+ * gives up after a fixed number of polls, records the event in a device
+ * word, and the kernel exits early (its outputs are then incomplete).  This
+ * reads that word -- call it after synchronising the streams the library
+ * was used on -- and returns MSC_ERR_TIMEOUT when it is set, MSC_OK
+ * otherwise; a nonzero `clear` resets it.  MSC_ERR_CUDA if the read fails.
+ */
+msc_status msc_check_device_error(int clear);
+
+/*
  * Plan overrides, for measurement and tuning.  Keys:
  *   "scan_chunks"   number of time chunks the scan is cut into (0 = auto)
  *   "scan_min_chunk" shortest chunk the automatic plan will make (steps)
+ *   "scan_path"     0 = automatic, 1 = element-load kernels only (no TMA)
+ *   "scan_lanes"    lanes per channel of the TMA kernels: 0 = automatic, 2, 4
  * Process-wide and not thread-safe; returns MSC_ERR_INVALID_ARG for an
  * unknown key or a negative value.
  */
 msc_status msc_tuning_set(const char* key, int64_t value);
+
+/*
+ * Measurement hook.  While enabled, every call records a CUDA event pair
+ * on its stream around its main kernel -- kind MSC_PROF_SCAN for the scan's
+ * output kernel, MSC_PROF_UPDATE for the decode kernel -- and counts every
+ * kernel it launches.  msc_profile_read synchronises those events and
+ * returns, since the last read: the number of kernels launched, and per
+ * kind the number of timed main kernels and their summed device time in
+ * milliseconds (arrays of 2, indexed by kind; NULL outputs are skipped);
+ * then it resets.  Process-wide and not thread-safe.  Disabled by default.
+ */
+enum { MSC_PROF_SCAN = 0, MSC_PROF_UPDATE = 1 };
+msc_status msc_profile_enable(int on);
+msc_status msc_profile_read(int64_t* launches, int64_t* timed, double* total_ms);
 
 /* Static description of a status code (never NULL). */
 const char* msc_status_string(msc_status status);

@@ -23,6 +23,7 @@ import os
 __all__ = [
     "MscError", "selective_scan_fwd", "selective_scan_fwd_ws",
     "selective_state_update", "scan_workspace_size", "tuning_set",
+    "check_device_error", "profile_enable", "profile_read",
     "library_path", "load",
 ]
 
@@ -33,7 +34,8 @@ MSC_F32, MSC_BF16 = 0, 1
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported size",
            3: "pointer not aligned to its element size",
            4: "CUDA runtime error",
-           5: "workspace missing, too small or misaligned"}
+           5: "workspace missing, too small or misaligned",
+           6: "a kernel's bounded wait for a data copy gave up"}
 
 
 class MscError(RuntimeError):
@@ -82,6 +84,13 @@ def load():
     lib.msc_status_string.argtypes = [st]
     lib.msc_version.restype = ctypes.c_int
     lib.msc_version.argtypes = []
+    lib.msc_check_device_error.restype = st
+    lib.msc_check_device_error.argtypes = [ctypes.c_int]
+    lib.msc_profile_enable.restype = st
+    lib.msc_profile_enable.argtypes = [ctypes.c_int]
+    lib.msc_profile_read.restype = st
+    lib.msc_profile_read.argtypes = [ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                     ctypes.POINTER(ctypes.c_double)]
     _lib = lib
     return lib
 
@@ -236,6 +245,29 @@ def selective_state_update(state, u, dt, A, B, C, D=None, z=None,
         batch, d_inner, d_state, code, _stream(dev))
     _check("msc_selective_state_update", st)
     return out
+
+
+def check_device_error(clear: bool = True):
+    """Raise MscError(MSC_ERR_TIMEOUT) if a kernel's bounded wait gave up.
+    Synchronise the streams used first."""
+    _check("msc_check_device_error", load().msc_check_device_error(int(clear)))
+
+
+def profile_enable(on: bool = True):
+    """Start/stop recording event pairs around each call's main kernel."""
+    _check("msc_profile_enable", load().msc_profile_enable(int(on)))
+
+
+def profile_read():
+    """Since the last read: (kernels launched, {"scan": (timed, ms),
+    "update": (timed, ms)}) -- main-kernel counts and summed device time.
+    Synchronises the recorded events, then resets the counters."""
+    n = ctypes.c_int64(0)
+    timed = (ctypes.c_int64 * 2)()
+    ms = (ctypes.c_double * 2)()
+    _check("msc_profile_read", load().msc_profile_read(ctypes.byref(n), timed, ms))
+    return int(n.value), {"scan": (int(timed[0]), float(ms[0])),
+                          "update": (int(timed[1]), float(ms[1]))}
 
 
 def tuning_set(key: str, value: int):

@@ -24,7 +24,7 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}", "-Xptxas", "-v"]
 
 LIBS = {
-    "libmsc.so": ["msc_api.cu", "scan_fwd.cu", "state_update.cu"],
+    "libmsc.so": ["msc_api.cu", "scan_fwd.cu", "scan_tma.cu", "state_update.cu"],
     "libmsc_peaks.so": ["peaks.cu"],
 }
 

@@ -3,6 +3,7 @@
 // include/msc.h.
 #include <cstring>
 #include <limits>
+#include <vector>
 
 #include "msc_internal.h"
 
@@ -10,6 +11,8 @@ namespace {
 
 int64_t g_force_chunks = 0;    // "scan_chunks"
 int64_t g_min_chunk = 512;     // "scan_min_chunk"
+int64_t g_scan_path = 0;       // "scan_path": 0 auto, 1 element-load kernels only
+int64_t g_scan_lanes = 0;      // "scan_lanes": TMA kernels' lanes per channel, 0 auto
 
 bool aligned(const void* p, size_t a) {
     return (reinterpret_cast<uintptr_t>(p) % a) == 0;
@@ -91,8 +94,15 @@ ScanCheck check_scan(const void* u, const void* dt, const float* A, const void* 
             r.st = MSC_ERR_ALIGNMENT;
             return r;
         }
-    r.plan = msc::make_scan_plan(batch, L, d_inner, d_state, sm_count(), g_force_chunks,
-                                 g_min_chunk);
+    if (g_scan_path == 0 && L > 0 && msc::tma_scan_supported(d_state, d_inner, dtype, u, dt, z)) {
+        // fp32 B/C copies unless fp32 inputs already suit 16-byte TMA boxes
+        const bool need_bc = dtype == MSC_BF16 || !aligned(B, 16) || !aligned(C, 16);
+        r.plan = msc::make_tma_plan(batch, L, d_inner, d_state, sm_count(), g_force_chunks,
+                                    g_min_chunk, need_bc, g_scan_lanes);
+    } else {
+        r.plan = msc::make_scan_plan(batch, L, d_inner, d_state, sm_count(), g_force_chunks,
+                                     g_min_chunk);
+    }
     const int64_t nblocks = batch * (int64_t)r.plan.K * r.plan.ntile;
     if (nblocks > std::numeric_limits<int>::max()) {
         r.st = MSC_ERR_UNSUPPORTED;
@@ -104,7 +114,51 @@ ScanCheck check_scan(const void* u, const void* dt, const float* A, const void* 
     return r;
 }
 
+// ---- measurement hook ------------------------------------------------------
+bool g_profile = false;
+int64_t g_prof_launches = 0;
+struct ProfPair {
+    cudaEvent_t a, b;
+    int kind;
+};
+std::vector<ProfPair> g_prof_pairs;                              // recorded, unread
+std::vector<cudaEvent_t> g_prof_free;                            // reusable events
+
+cudaEvent_t prof_event() {
+    if (!g_prof_free.empty()) {
+        cudaEvent_t e = g_prof_free.back();
+        g_prof_free.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
 }  // namespace
+
+namespace msc {
+
+ProfileMark profile_begin(cudaStream_t s, int kind) {
+    ProfileMark m{nullptr, kind};
+    if (!g_profile) return m;
+    cudaEvent_t e = prof_event();
+    if (e && cudaEventRecord(e, s) == cudaSuccess) m.begin = e;
+    return m;
+}
+
+void profile_end(const ProfileMark& m, cudaStream_t s) {
+    if (!m.begin) return;
+    cudaEvent_t e = prof_event();
+    if (e && cudaEventRecord(e, s) == cudaSuccess)
+        g_prof_pairs.push_back({static_cast<cudaEvent_t>(m.begin), e, m.kind});
+}
+
+void profile_count(int launches) {
+    if (g_profile) g_prof_launches += launches;
+}
+
+}  // namespace msc
 
 static msc_status run_scan(const void* u, const void* dt, const float* A, const void* B,
                            const void* C, const float* D, const void* z,
@@ -128,12 +182,24 @@ static msc_status run_scan(const void* u, const void* dt, const float* A, const 
     msc::ScanArgs a{};
     a.u = u; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.dt_bias = dt_bias;
     a.out = out; a.last_state = last_state;
-    const size_t half = need / 2 / sizeof(float);
-    a.ws_a = need ? static_cast<float*>(w) : nullptr;
-    a.ws_b = need ? static_cast<float*>(w) + half : nullptr;
+    const size_t half = c.plan.ws_carry / 2 / sizeof(float);
+    a.ws_a = c.plan.ws_carry ? static_cast<float*>(w) : nullptr;
+    a.ws_b = c.plan.ws_carry ? static_cast<float*>(w) + half : nullptr;
     a.batch = batch; a.L = L; a.d_inner = d_inner; a.N = d_state;
     a.chunk = c.plan.chunk; a.K = c.plan.K; a.ntile = c.plan.ntile; a.vec = c.vec;
-    cudaError_t e = msc::launch_scan(a, c.plan, dtype, s);
+    cudaError_t e;
+    if (c.plan.tma) {
+        float* Bf = nullptr;
+        float* Cf = nullptr;
+        if (c.plan.ws_bc) {
+            Bf = reinterpret_cast<float*>(static_cast<char*>(w) + c.plan.ws_carry);
+            Cf = reinterpret_cast<float*>(static_cast<char*>(w) + c.plan.ws_carry +
+                                          c.plan.ws_bc / 2);
+        }
+        e = msc::launch_scan_tma(a, c.plan, dtype, Bf, Cf, s);
+    } else {
+        e = msc::launch_scan(a, c.plan, dtype, s);
+    }
     if (need > 0 && own_ws) {
         cudaError_t f = cudaFreeAsync(w, s);
         if (e == cudaSuccess) e = f;
@@ -175,9 +241,19 @@ msc_status msc_selective_scan_workspace_size(int64_t batch, int64_t L, int64_t d
         *bytes = 0;
         return MSC_OK;
     }
+    // the plan also depends on pointer alignment, unknown here: the larger of
+    // the two kernel families' needs covers either choice
+    const int sms = sm_count();
     msc::ScanPlan p =
-        msc::make_scan_plan(batch, L, d_inner, d_state, sm_count(), g_force_chunks, g_min_chunk);
-    *bytes = p.ws_bytes;
+        msc::make_scan_plan(batch, L, d_inner, d_state, sms, g_force_chunks, g_min_chunk);
+    size_t need = p.ws_bytes;
+    if (g_scan_path == 0 && msc::tma_scan_supported(d_state, d_inner, dtype, nullptr, nullptr,
+                                                    nullptr)) {
+        msc::ScanPlan q = msc::make_tma_plan(batch, L, d_inner, d_state, sms, g_force_chunks,
+                                             g_min_chunk, true, g_scan_lanes);
+        need = need > q.ws_bytes ? need : q.ws_bytes;
+    }
+    *bytes = need;
     return MSC_OK;
 }
 
@@ -210,7 +286,11 @@ msc_status msc_selective_state_update(float* state, const void* u, const void* d
     a.state = state; a.u = u; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
     a.dt_bias = dt_bias; a.out = out; a.batch = batch; a.d_inner = d_inner; a.N = d_state;
     a.vec = (d_state % 4 == 0) && aligned(state, 16) && aligned(B, 4 * es) && aligned(C, 4 * es);
-    cudaError_t e = msc::launch_state_update(a, dtype, reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    msc::ProfileMark m = msc::profile_begin(s, MSC_PROF_UPDATE);
+    cudaError_t e = msc::launch_state_update(a, dtype, s);
+    msc::profile_end(m, s);
+    msc::profile_count(1);
     return e == cudaSuccess ? MSC_OK : MSC_ERR_CUDA;
 }
 
@@ -220,11 +300,60 @@ msc_status msc_tuning_set(const char* key, int64_t value) {
         g_force_chunks = value;
         return MSC_OK;
     }
+    if (std::strcmp(key, "scan_lanes") == 0) {
+        if (value != 0 && value != 2 && value != 4) return MSC_ERR_INVALID_ARG;
+        g_scan_lanes = value;
+        return MSC_OK;
+    }
+    if (std::strcmp(key, "scan_path") == 0) {
+        if (value > 1) return MSC_ERR_INVALID_ARG;
+        g_scan_path = value;
+        return MSC_OK;
+    }
     if (std::strcmp(key, "scan_min_chunk") == 0) {
         g_min_chunk = value > 0 ? value : 1;
         return MSC_OK;
     }
     return MSC_ERR_INVALID_ARG;
+}
+
+msc_status msc_profile_enable(int on) {
+    g_profile = on != 0;
+    return MSC_OK;
+}
+
+msc_status msc_profile_read(int64_t* launches, int64_t* timed, double* total_ms) {
+    double ms[2] = {0.0, 0.0};
+    int64_t n[2] = {0, 0};
+    msc_status st = MSC_OK;
+    for (auto& pr : g_prof_pairs) {
+        float t = 0.0f;
+        if (cudaEventSynchronize(pr.b) != cudaSuccess ||
+            cudaEventElapsedTime(&t, pr.a, pr.b) != cudaSuccess)
+            st = MSC_ERR_CUDA;
+        ms[pr.kind] += t;
+        n[pr.kind] += 1;
+        g_prof_free.push_back(pr.a);
+        g_prof_free.push_back(pr.b);
+    }
+    if (launches) *launches = g_prof_launches;
+    if (timed) {
+        timed[0] = n[0];
+        timed[1] = n[1];
+    }
+    if (total_ms) {
+        total_ms[0] = ms[0];
+        total_ms[1] = ms[1];
+    }
+    g_prof_pairs.clear();
+    g_prof_launches = 0;
+    return st;
+}
+
+msc_status msc_check_device_error(int clear) {
+    unsigned int v = 0;
+    if (msc::scan_error_word(&v, clear != 0) != cudaSuccess) return MSC_ERR_CUDA;
+    return v ? MSC_ERR_TIMEOUT : MSC_OK;
 }
 
 const char* msc_status_string(msc_status s) {
@@ -235,6 +364,7 @@ const char* msc_status_string(msc_status s) {
         case MSC_ERR_ALIGNMENT: return "pointer not aligned to its element size";
         case MSC_ERR_CUDA: return "CUDA runtime error";
         case MSC_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+        case MSC_ERR_TIMEOUT: return "a kernel's bounded wait for a data copy gave up";
     }
     return "unknown status";
 }

@@ -33,11 +33,15 @@ struct ScanArgs {
 
 // How one scan call is cut up.
 struct ScanPlan {
-    int G;             // lanes per channel (each lane owns 4 states)
+    int tma;           // 1: TMA kernels (8 channels per CTA), 0: element-load kernels
+    int G;             // lanes per channel (element-load kernels: 4 states per lane;
+                       // TMA kernels: 2 or 4 lanes, N/G states per lane)
     int K;             // time chunks
     int64_t chunk;     // steps per chunk
-    int ntile;         // channel tiles
-    size_t ws_bytes;   // carry workspace
+    int ntile;         // channel tiles per (batch row, chunk)
+    size_t ws_carry;   // bytes of chunk summaries (a then b), 0 when K == 1
+    size_t ws_bc;      // bytes of fp32 copies of B then C for the TMA boxes
+    size_t ws_bytes;   // total workspace (carry, then B/C copies, 256-aligned)
 };
 
 struct UpdateArgs {
@@ -55,15 +59,37 @@ struct UpdateArgs {
     int vec;           // 1: state and B/C rows can be read 4 elements at a time
 };
 
+// Measurement hook (msc_api.cu): while enabled, launchers count kernels and
+// bracket their main kernel with an event pair on the launch stream.
+struct ProfileMark {
+    void* begin;  // cudaEvent_t or nullptr when profiling is off
+    int kind;     // MSC_PROF_SCAN or MSC_PROF_UPDATE
+};
+ProfileMark profile_begin(cudaStream_t s, int kind);
+void profile_end(const ProfileMark& m, cudaStream_t s);
+void profile_count(int launches);
+
 constexpr int kScanThreads = 128;
 constexpr int kUpdateThreads = 256;
 
 int lanes_per_channel(int64_t N);
 ScanPlan make_scan_plan(int64_t batch, int64_t L, int64_t d_inner, int64_t N,
                         int sm_count, int64_t force_chunks, int64_t min_chunk);
+ScanPlan make_tma_plan(int64_t batch, int64_t L, int64_t d_inner, int64_t N, int sm_count,
+                       int64_t force_chunks, int64_t min_chunk, bool need_bc,
+                       int64_t force_lanes);
 
 cudaError_t launch_scan(const ScanArgs& a, const ScanPlan& p, msc_dtype dtype,
                         cudaStream_t stream);
+
+// TMA path (scan_tma.cu): supported shapes, time-tile length, launch, and
+// the device word its bounded waits set when a copy never lands.
+bool tma_scan_supported(int64_t N, int64_t d_inner, msc_dtype dtype, const void* u,
+                        const void* dt, const void* z);
+int tma_scan_tile(int64_t N);
+cudaError_t launch_scan_tma(const ScanArgs& a, const ScanPlan& p, msc_dtype dtype, float* Bf,
+                            float* Cf, cudaStream_t stream);
+cudaError_t scan_error_word(unsigned int* value, bool clear);
 cudaError_t launch_state_update(const UpdateArgs& a, msc_dtype dtype,
                                 cudaStream_t stream);
 

@@ -97,6 +97,60 @@ __global__ void k_update_core(float* sink, int64_t iters) {
     if (acc == 1234.5f) sink[0] = acc;
 }
 
+// Shared-memory load throughput by access pattern: each iteration every
+// lane issues 8 independent volatile loads of W bytes (W = 4, 8 or 16) from
+// 8 precomputed addresses (so the loop is 8 loads + 8 adds).  The element
+// a lane reads within each 512-byte block is set by `pattern`:
+//   0 all lanes the same       1 lane & 3       2 lane >> 2      3 lane
+//   4 lane >> 4                5 lane >> 3      6 lane & 7
+template <int W>
+__global__ void k_lds(float* sink, int64_t iters, int pattern) {
+    __shared__ __align__(16) float sm[4096];
+    for (int i = threadIdx.x; i < 4096; i += blockDim.x) sm[i] = 0.001f * i;
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    int sel;
+    switch (pattern) {
+        case 0: sel = 0; break;
+        case 1: sel = lane & 3; break;
+        case 2: sel = lane >> 2; break;
+        case 3: sel = lane; break;
+        case 4: sel = lane >> 4; break;
+        case 5: sel = lane >> 3; break;
+        default: sel = lane & 7; break;
+    }
+    constexpr int E = W / 4;  // floats per load
+    unsigned addr[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+        addr[r] = static_cast<unsigned>(__cvta_generic_to_shared(sm + r * 128 * E / 4 * 4 + sel * E));
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int64_t it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            if (E == 4) {
+                float x, y, z, w;
+                asm volatile("ld.volatile.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(x), "=f"(y), "=f"(z), "=f"(w) : "r"(addr[r]));
+                acc[r] += x;
+            } else if (E == 2) {
+                float x, y;
+                asm volatile("ld.volatile.shared.v2.f32 {%0, %1}, [%2];"
+                             : "=f"(x), "=f"(y) : "r"(addr[r]));
+                acc[r] += x;
+            } else {
+                float x;
+                asm volatile("ld.volatile.shared.f32 %0, [%1];" : "=f"(x) : "r"(addr[r]));
+                acc[r] += x;
+            }
+        }
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) s += acc[r];
+    if (s == 1234.5f) sink[0] = s;
+}
+
 __global__ void k_copy(float4* __restrict__ dst, const float4* __restrict__ src, int64_t n) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
@@ -150,6 +204,18 @@ int msc_peak_ffma2(float* sink, int blocks, int threads, int64_t iters, cudaStre
 int msc_peak_update_core(float* sink, int blocks, int threads, int64_t iters,
                          cudaStream_t s, float* ms) {
     return timed(s, ms, [&] { k_update_core<<<blocks, threads, 0, s>>>(sink, iters); });
+}
+
+// shared loads (warp instructions) = blocks * (threads / 32) * iters * 8.
+int msc_peak_lds(float* sink, int blocks, int threads, int64_t iters, int width_bytes,
+                 int pattern, cudaStream_t s, float* ms) {
+    if (width_bytes == 16)
+        return timed(s, ms,
+                     [&] { k_lds<16><<<blocks, threads, 0, s>>>(sink, iters, pattern); });
+    if (width_bytes == 8)
+        return timed(s, ms,
+                     [&] { k_lds<8><<<blocks, threads, 0, s>>>(sink, iters, pattern); });
+    return timed(s, ms, [&] { k_lds<4><<<blocks, threads, 0, s>>>(sink, iters, pattern); });
 }
 
 // bytes moved = 2 * n16 * 16 (read + write); n16 = number of 16-byte words.

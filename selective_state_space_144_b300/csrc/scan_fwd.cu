@@ -161,9 +161,60 @@ ScanPlan make_scan_plan(int64_t batch, int64_t L, int64_t d_inner, int64_t N,
         p.chunk = 1;
     }
     p.K = (int)K;
-    p.ws_bytes = K > 1 ? 2 * (size_t)batch * (size_t)(K - 1) * (size_t)d_inner *
+    p.tma = 0;
+    p.ws_carry = K > 1 ? 2 * (size_t)batch * (size_t)(K - 1) * (size_t)d_inner *
                              (size_t)N * sizeof(float)
                        : 0;
+    p.ws_bc = 0;
+    p.ws_bytes = p.ws_carry;
+    return p;
+}
+
+static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+ScanPlan make_tma_plan(int64_t batch, int64_t L, int64_t d_inner, int64_t N, int sm_count,
+                       int64_t force_chunks, int64_t min_chunk, bool need_bc, int64_t force_lanes) {
+    ScanPlan p{};
+    p.tma = 1;
+    const int64_t target = (int64_t)sm_count * 8;  // 2 warps per SM sub-partition
+    // 2 lanes per channel (8 states each for N = 16) need half the shared-
+    // memory traffic and shuffles per update of 4 lanes; take them when the
+    // channels alone still fill the GPU, and always for N <= 32 when forced
+    int G = 4;
+    if (force_lanes == 2 && N <= 32 && d_inner % 16 == 0) {
+        G = 2;
+    } else if (force_lanes == 0 && N <= 32 && d_inner % 16 == 0 &&
+               batch * (d_inner / 16) >= target) {
+        G = 2;
+    }
+    p.G = G;
+    const int64_t cpw = 32 / G;
+    p.ntile = (int)(d_inner / cpw);
+    const int64_t TT = tma_scan_tile(N);
+    const int64_t warps1 = batch * p.ntile;  // one warp per CTA
+    int64_t K = 1;
+    if (L > 0) {
+        if (force_chunks > 0) {
+            K = force_chunks;
+        } else {
+            K = warps1 >= target ? 1 : (target + warps1 - 1) / warps1;
+            const int64_t maxK = L / (min_chunk > 0 ? min_chunk : 1);
+            K = K < maxK ? K : maxK;
+        }
+        K = K < 1 ? 1 : K;
+        int64_t chunk = (L + K - 1) / K;
+        chunk = (chunk + TT - 1) / TT * TT;  // chunk boundaries on tile boundaries
+        p.chunk = chunk;
+        K = (L + chunk - 1) / chunk;
+    } else {
+        p.chunk = TT;
+    }
+    p.K = (int)K;
+    p.ws_carry = K > 1 ? round256(2 * (size_t)batch * (size_t)(K - 1) * (size_t)d_inner *
+                                  (size_t)N * sizeof(float))
+                       : 0;
+    p.ws_bc = need_bc ? 2 * round256((size_t)batch * (size_t)L * (size_t)N * sizeof(float)) : 0;
+    p.ws_bytes = p.ws_carry + p.ws_bc;
     return p;
 }
 
@@ -176,7 +227,10 @@ static cudaError_t launch_scan_g(const ScanArgs& a, const ScanPlan& p,
             <<<(unsigned)nb, kScanThreads, 0, s>>>(a, p.K - 1);
     }
     const int64_t nb = a.batch * (int64_t)p.K * p.ntile;
+    const ProfileMark m = profile_begin(s, MSC_PROF_SCAN);
     scan_chunk_kernel<T, G, VEC, true><<<(unsigned)nb, kScanThreads, 0, s>>>(a, p.K);
+    profile_end(m, s);
+    profile_count(p.K > 1 ? 2 : 1);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,553 @@
+// scan_tma.cu -- the selective-scan forward for B300: TMA-staged tiles,
+// fp32 state in registers, packed fp32x2 arithmetic.
+//
+// Operation ("Deep dive into Mamba: architecture and implementation of
+// selective state-space models", sections 4.4 and 5.2; gate and step-size
+// bias from the MambaBlock of "State space models and Mamba"):
+//     delta = softplus(dt + dt_bias);  h = exp(delta*A) * h + delta*B*u
+//     y = C . h + D*u;  out = y * silu(z)
+// all fused: the discretised A and B, and the states, never leave the chip
+// (the kernel fusion and SRAM residency of the presentation article,
+// section 3.3 -- restated here for TMA and registers).
+//
+// Work split.  One CTA is one warp and owns CPW = 32/G consecutive channels
+// of one batch row for one time chunk.  Lane l works on channel l % CPW and
+// on the NS = N/G consecutive states g*NS ... of it, g = l / CPW, held in
+// registers as fp32 pairs.  Lanes that hold the same states are contiguous,
+// so the per-step reads of B and C from shared memory are broadcasts that
+// the shared-memory crossbar serves at full width.  Per tile of TT steps
+// one lane issues five 3-D TMA loads into a ring of S stages -- u, dt, z as
+// [TT x CPW] boxes and B, C (fp32) as [TT x N] boxes -- completing an
+// mbarrier per stage; every lane waits on it (bounded).
+//
+// Time advances in octets of 8 steps.  Per octet each lane
+//   * computes delta = softplus(dt + dt_bias) and delta*u for the 8/G steps
+//     s = g, g+G, ... of the NEXT octet of its channel (in fp32 pairs) and
+//     posts them to shared memory: the per-(step, channel) work is done
+//     once, one octet ahead so that its latency overlaps the state updates;
+//   * runs the 8 steps of the current octet on its states: dA = 2^(delta*A2)
+//     on MUFU (A2 = A*log2 e), h = dA*h + (delta*u)*B, y += C*h, with
+//     fma/mul.rn.f32x2 on state pairs; the 8 partial C.h stay in registers;
+//   * reduce-scatters the partial C.h over the G lanes of its channel with
+//     butterfly shuffles, ending with the full sums of steps g, g+G, ...,
+//     adds D*u, applies the gate and stores those outputs.
+// Steps past the end of the chunk get delta = 0, i.e. dA = 1 and no input:
+// the state passes through unchanged and nothing is stored.
+//
+// Time chunks (K > 1) follow the segmented scan of the presentation
+// article, section 3.2: the summary kernel runs chunks 0..K-2 from a zero
+// state and records (prod dA, end state); the output kernel folds the
+// summaries of the chunks before its own into its starting state with the
+// combine (a1, b1) then (a2, b2) -> (a2*a1, a2*b1 + b2).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <type_traits>
+
+#include "msc_device.cuh"
+#include "msc_internal.h"
+#include "msc_ptx.cuh"
+
+namespace msc {
+
+// Set (bit 0) by a kernel whose bounded wait for a TMA copy gave up.
+__device__ unsigned int g_scan_error;
+
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int kOct = 8;  // steps per iteration
+
+template <typename T, int G, int NS, int TT, int S>
+struct TmaLayout {
+    static constexpr int CPW = 32 / G;                  // channels per warp
+    static constexpr int N = G * NS;
+    static constexpr int kX = TT * CPW * (int)sizeof(T); // one of u / dt / z per stage
+    static constexpr int kBC = TT * N * 4;              // one of B / C (fp32) per stage
+    static constexpr int kStage = 3 * kX + 2 * kBC;
+    static constexpr int kDU = S * kStage;              // float2 [2][8 steps][CPW]
+    static constexpr int kBar = kDU + 2 * kOct * CPW * 8;
+    static constexpr int kTotal = kBar + S * 8;
+    static_assert(kX % 128 == 0 && kBC % 128 == 0, "TMA destinations must stay 128B aligned");
+    static_assert(TT % kOct == 0, "tiles hold whole octets");
+};
+
+template <typename T> __device__ __forceinline__ float lds_elem(const T* p);
+template <> __device__ __forceinline__ float lds_elem<float>(const float* p) { return *p; }
+template <> __device__ __forceinline__ float lds_elem<__nv_bfloat16>(const __nv_bfloat16* p) {
+    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p))
+                           << 16);
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// softplus of both halves of a pair: max(x, 0) + log1p(e), e = e^-|x|,
+// log1p(e) = e * P(2e - 1) (the polynomial of log1p_unit, evaluated on pairs).
+__device__ __forceinline__ u64 softplus2(u64 x2) {
+    const float x0 = lo2(x2), x1 = hi2(x2);
+    const u64 e = pk2(ex2(-fabsf(x0) * kLog2e), ex2(-fabsf(x1) * kLog2e));
+    const u64 s = fma2(e, pk2(2.0f, 2.0f), pk2(-1.0f, -1.0f));
+    u64 p = pk2(2.0023837e-05f, 2.0023837e-05f);
+    p = fma2(p, s, pk2(-6.695044e-05f, -6.695044e-05f));
+    p = fma2(p, s, pk2(0.00018186837f, 0.00018186837f));
+    p = fma2(p, s, pk2(-0.0006321981f, -0.0006321981f));
+    p = fma2(p, s, pk2(0.0022891003f, 0.0022891003f));
+    p = fma2(p, s, pk2(-0.008463899f, -0.008463899f));
+    p = fma2(p, s, pk2(0.033152375f, 0.033152375f));
+    p = fma2(p, s, pk2(-0.14426334f, -0.14426334f));
+    p = fma2(p, s, pk2(0.8109302f, 0.8109302f));
+    return add2(pk2(fmaxf(x0, 0.0f), fmaxf(x1, 0.0f)), mul2(e, p));
+}
+
+// silu of both halves of a pair: z / (1 + e^-z).
+__device__ __forceinline__ u64 silu2(u64 z2) {
+    const float z0 = lo2(z2), z1 = hi2(z2);
+    const u64 d = add2(pk2(ex2(-z0 * kLog2e), ex2(-z1 * kLog2e)), pk2(1.0f, 1.0f));
+    return mul2(z2, pk2(rcp_approx(lo2(d)), rcp_approx(hi2(d))));
+}
+
+// Reduce-scatter of the 8 per-step partial sums over the G lanes of a
+// channel (lanes ch, ch + CPW, ...): afterwards out[m] holds the full sum of
+// step g + G*m, m < 8/G.
+template <int G>
+__device__ __forceinline__ void reduce_scatter(const float (&y)[kOct], int lane,
+                                               float (&out)[kOct / G]) {
+    constexpr int CPW = 32 / G;
+    if constexpr (G == 2) {
+        const bool b0 = (lane / CPW) & 1;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {  // pair (2m, 2m+1): keep step 2m + b0
+            const float send = b0 ? y[2 * m] : y[2 * m + 1];
+            const float keep = b0 ? y[2 * m + 1] : y[2 * m];
+            out[m] = keep + __shfl_xor_sync(0xffffffffu, send, CPW);
+        }
+    } else {
+        static_assert(G == 4, "2 or 4 lanes per channel");
+        const int g = lane / CPW;
+        const bool b1 = (g >> 1) & 1, b0 = g & 1;
+        float k[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {  // steps (p, p+2), p = 0,1,4,5: keep p + 2*b1
+            const int p = (m & 1) + 4 * (m >> 1);
+            const float send = b1 ? y[p] : y[p + 2];
+            const float keep = b1 ? y[p + 2] : y[p];
+            k[m] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * CPW);
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {  // (k[2m], k[2m+1]) = steps (4m+2b1, +1): keep +b0
+            const float send = b0 ? k[2 * m] : k[2 * m + 1];
+            const float keep = b0 ? k[2 * m + 1] : k[2 * m];
+            out[m] = keep + __shfl_xor_sync(0xffffffffu, send, CPW);
+        }
+    }
+}
+
+template <typename T, int G, int NS, int TT, int S, bool OUTPUT>
+__global__ void __launch_bounds__(32)
+scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dt,
+                const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
+                const __grid_constant__ CUtensorMap tm_C, const ScanArgs a, const int kgrid) {
+    using Lay = TmaLayout<T, G, NS, TT, S>;
+    constexpr int CPW = Lay::CPW;
+    constexpr int N = Lay::N;
+    constexpr int NP = NS / 2;         // state pairs per lane
+    constexpr int OPT = TT / kOct;     // octets per tile
+    constexpr int SPL = kOct / G;      // steps per lane in the prologue / epilogue
+    constexpr int PPL = SPL / 2;       // ... as fp32 pairs
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int lane = threadIdx.x;
+    const int ch = lane % CPW;
+    const int g = lane / CPW;
+    const int n0 = g * NS;
+    int64_t bid = blockIdx.x;
+    const int tile = (int)(bid % a.ntile);
+    bid /= a.ntile;
+    const int k = (int)(bid % kgrid);
+    const int b = (int)(bid / kgrid);
+    const int d0 = tile * CPW;
+    const int64_t d = d0 + ch;
+    const int64_t tc0 = (int64_t)k * a.chunk;
+    const int nsteps = (int)min(a.chunk, a.L - tc0);
+    const int ntiles = (nsteps + TT - 1) / TT;
+    const bool has_z = OUTPUT && a.z != nullptr;
+    const uint32_t tx_bytes =
+        (uint32_t)((2 + (has_z ? 1 : 0)) * Lay::kX + (OUTPUT ? 2 : 1) * Lay::kBC);
+
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + Lay::kBar;
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(bar0 + 8 * s, 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tm_u);
+        prefetch_tensormap(&tm_dt);
+        prefetch_tensormap(&tm_B);
+        if (has_z) prefetch_tensormap(&tm_z);
+        if (OUTPUT) prefetch_tensormap(&tm_C);
+    }
+    __syncwarp();
+
+    auto issue = [&](int i) {  // lane 0: tile i of this chunk into stage i % S
+        const uint32_t st = sbase + (i % S) * Lay::kStage;
+        const uint32_t bar = bar0 + 8 * (i % S);
+        const int32_t tt = (int32_t)(tc0 + (int64_t)i * TT);
+        mbar_expect_tx(bar, tx_bytes);
+        tma_load_3d(st, &tm_u, bar, d0, tt, b);
+        tma_load_3d(st + Lay::kX, &tm_dt, bar, d0, tt, b);
+        if (has_z) tma_load_3d(st + 2 * Lay::kX, &tm_z, bar, d0, tt, b);
+        tma_load_3d(st + 3 * Lay::kX, &tm_B, bar, 0, tt, b);
+        if (OUTPUT) tma_load_3d(st + 3 * Lay::kX + Lay::kBC, &tm_C, bar, 0, tt, b);
+    };
+    int issued = min(S, ntiles);
+    if (lane == 0)
+        for (int i = 0; i < issued; ++i) issue(i);
+
+    // per-channel constants and the starting state
+    const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
+    const float Dd = (OUTPUT && a.D) ? __ldg(a.D + d) : 0.0f;
+    u64 A2[NP], hp[NP], Pp[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+        const float* Ar = a.A + d * N + n0 + 2 * i;
+        A2[i] = pk2(__ldg(Ar) * kLog2e, __ldg(Ar + 1) * kLog2e);
+        hp[i] = pk2(0.0f, 0.0f);
+        Pp[i] = pk2(1.0f, 1.0f);
+    }
+    if (OUTPUT && k > 0) {
+        for (int j2 = 0; j2 < k; ++j2) {
+            const int64_t w = ((int64_t)(b * (a.K - 1) + j2) * a.d_inner + d) * N + n0;
+#pragma unroll
+            for (int i = 0; i < NP; ++i) {
+                const float2 av = *reinterpret_cast<const float2*>(a.ws_a + w + 2 * i);
+                const float2 bv = *reinterpret_cast<const float2*>(a.ws_b + w + 2 * i);
+                hp[i] = fma2(pk2(av.x, av.y), hp[i], pk2(bv.x, bv.y));
+            }
+        }
+    }
+
+    float2* sDU = reinterpret_cast<float2*>(smem + Lay::kDU);
+    auto stage = [&](int i) -> const unsigned char* { return smem + (i % S) * Lay::kStage; };
+    const u64 bias2 = pk2(bias, bias);
+
+    // delta and delta*u of steps g + G*m (m < SPL) of the octet starting at
+    // row `row0` of tile `i` (chunk step `s_base`), posted to buffer `buf`
+    // for its core; the u of those steps is returned as pairs
+    auto prologue = [&](int i, int row0, int s_base, int buf, u64 (&uu)[PPL]) {
+        const T* sx = reinterpret_cast<const T*>(stage(i)) + (row0 + g) * CPW + ch;
+        float2* dst = sDU + buf * (kOct * CPW) + g * CPW + ch;
+#pragma unroll
+        for (int p = 0; p < PPL; ++p) {
+            const int r0 = G * (2 * p) * CPW, r1 = r0 + G * CPW;
+            uu[p] = pk2(lds_elem<T>(sx + r0), lds_elem<T>(sx + r1));
+            const u64 x = add2(pk2(lds_elem<T>(sx + TT * CPW + r0),
+                                   lds_elem<T>(sx + TT * CPW + r1)),
+                               bias2);
+            const u64 dl = softplus2(x);
+            const u64 du = mul2(dl, uu[p]);
+            const int s0 = s_base + g + G * (2 * p);
+            const bool v0 = s0 < nsteps, v1 = s0 + G < nsteps;
+            dst[(2 * p) * G * CPW] = make_float2(v0 ? lo2(dl) : 0.0f, v0 ? lo2(du) : 0.0f);
+            dst[(2 * p + 1) * G * CPW] = make_float2(v1 ? hi2(dl) : 0.0f, v1 ? hi2(du) : 0.0f);
+        }
+    };
+
+    bool ok = ntiles == 0 || __all_sync(0xffffffffu, mbar_wait(bar0, 0, kWaitLimit));
+    int waited = ntiles > 0 ? 1 : 0;  // tiles [0, waited) are known complete
+    u64 u_cur[PPL], u_nxt[PPL];
+#pragma unroll
+    for (int p = 0; p < PPL; ++p) u_cur[p] = u_nxt[p] = pk2(0.0f, 0.0f);
+    if (ok && ntiles > 0) prologue(0, 0, 0, 0, u_cur);
+    __syncwarp();
+
+    const u64 D2 = pk2(Dd, Dd);
+    T* const out_ch = static_cast<T*>(a.out) + ((int64_t)b * a.L + tc0 + g) * a.d_inner + d;
+
+    // One tile: OPT octets, unrolled so that every shared-memory offset is a
+    // constant.  FULL: the tile lies inside the chunk, no step is masked.
+    auto tile_body = [&](int i, auto full_tag) {
+        constexpr bool FULL = decltype(full_tag)::value;
+        const unsigned char* st = stage(i);
+        const float* sB0 = reinterpret_cast<const float*>(st + 3 * Lay::kX) + n0;
+        const float* sC0 = reinterpret_cast<const float*>(st + 3 * Lay::kX + Lay::kBC) + n0;
+        const T* sz0 = reinterpret_cast<const T*>(st + 2 * Lay::kX) + g * CPW + ch;
+#pragma unroll
+        for (int oo = 0; oo < OPT; ++oo) {
+            const int sb = i * TT + kOct * oo;  // chunk step of the octet's first row
+            if (!FULL && sb >= nsteps) break;   // past the end of a partial tile
+            // (1) the state updates of this octet
+            const float2* sd = sDU + (oo & 1) * (kOct * CPW) + ch;
+            const float* sB = sB0 + kOct * oo * N;
+            const float* sC = sC0 + kOct * oo * N;
+            float yv[kOct];
+#pragma unroll
+            for (int j = 0; j < kOct; ++j) {
+                const float2 v = sd[j * CPW];
+                const u64 dl2 = pk2(v.x, v.x), du2 = pk2(v.y, v.y);
+                u64 Bp[NP], Cp[NP];
+                if constexpr (NP == 1) {  // 2 states: one 8-byte read each
+                    Bp[0] = *reinterpret_cast<const u64*>(sB + j * N);
+                    if (OUTPUT) Cp[0] = *reinterpret_cast<const u64*>(sC + j * N);
+                } else {                  // 16-byte reads, two pairs each
+#pragma unroll
+                    for (int i2 = 0; i2 < NP; i2 += 2) {
+                        const ulonglong2 bq =
+                            *reinterpret_cast<const ulonglong2*>(sB + j * N + 2 * i2);
+                        Bp[i2] = bq.x;
+                        Bp[i2 + 1] = bq.y;
+                        if (OUTPUT) {
+                            const ulonglong2 cq =
+                                *reinterpret_cast<const ulonglong2*>(sC + j * N + 2 * i2);
+                            Cp[i2] = cq.x;
+                            Cp[i2 + 1] = cq.y;
+                        }
+                    }
+                }
+                u64 y2 = pk2(0.0f, 0.0f);
+#pragma unroll
+                for (int i2 = 0; i2 < NP; ++i2) {
+                    const u64 x2 = mul2(dl2, A2[i2]);
+                    const u64 dA = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
+                    hp[i2] = fma2(dA, hp[i2], mul2(du2, Bp[i2]));
+                    if (OUTPUT)
+                        y2 = fma2(Cp[i2], hp[i2], y2);
+                    else
+                        Pp[i2] = mul2(Pp[i2], dA);
+                }
+                yv[j] = lo2(y2) + hi2(y2);
+            }
+            // (2) the next octet's step sizes, after the core's reads of this
+            //     octet's (next tile: wait for it first)
+            if (oo + 1 < OPT) {
+                prologue(i, kOct * (oo + 1), sb + kOct, (oo + 1) & 1, u_nxt);
+            } else if (i + 1 < ntiles) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * ((i + 1) % S),
+                                                       ((i + 1) / S) & 1, kWaitLimit));
+                if (!ok) return;
+                waited = i + 2;
+                prologue(i + 1, 0, sb + kOct, (oo + 1) & 1, u_nxt);
+            }
+            // (3) outputs of steps g + G*m of channel ch
+            if (OUTPUT) {
+                float ys[SPL];
+                reduce_scatter<G>(yv, lane, ys);
+                T* op = out_ch + (int64_t)sb * a.d_inner;
+#pragma unroll
+                for (int p = 0; p < PPL; ++p) {
+                    u64 y2 = fma2(D2, u_cur[p], pk2(ys[2 * p], ys[2 * p + 1]));
+                    const int r0 = (kOct * oo + G * (2 * p)) * CPW, r1 = r0 + G * CPW;
+                    if (has_z)
+                        y2 = mul2(y2, silu2(pk2(lds_elem<T>(sz0 + r0), lds_elem<T>(sz0 + r1))));
+                    const int s0 = sb + g + G * (2 * p);
+                    if (FULL || s0 < nsteps)
+                        Elem<T>::store(op + (int64_t)(G * 2 * p) * a.d_inner, lo2(y2));
+                    if (FULL || s0 + G < nsteps)
+                        Elem<T>::store(op + (int64_t)(G * (2 * p + 1)) * a.d_inner, hi2(y2));
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int p = 0; p < PPL; ++p) u_cur[p] = u_nxt[p];
+        }
+        // (4) the tile is consumed: refill its stage
+        if (i + S < ntiles) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(i + S);
+            }
+            issued = i + S + 1;
+        }
+    };
+
+    for (int i = 0; ok && i < ntiles; ++i) {
+        if ((i + 1) * TT <= nsteps)
+            tile_body(i, std::integral_constant<bool, true>{});
+        else
+            tile_body(i, std::integral_constant<bool, false>{});
+    }
+
+    if (!ok) {
+        // a copy never completed: flag it, give the copies still in flight a
+        // bounded chance to land in this CTA's shared memory, then leave
+        if (lane == 0) atomicOr(&g_scan_error, 1u);
+        for (int i = waited; i < issued; ++i) mbar_wait(bar0 + 8 * (i % S), (i / S) & 1, kWaitLimit);
+        return;
+    }
+
+    if (OUTPUT) {
+        if (k == a.K - 1 && a.last_state) {
+            float* ls = a.last_state + ((int64_t)b * a.d_inner + d) * N + n0;
+#pragma unroll
+            for (int i = 0; i < NP; ++i)
+                *reinterpret_cast<float2*>(ls + 2 * i) = make_float2(lo2(hp[i]), hi2(hp[i]));
+        }
+    } else {
+        const int64_t w = ((int64_t)(b * (a.K - 1) + k) * a.d_inner + d) * N + n0;
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            *reinterpret_cast<float2*>(a.ws_a + w + 2 * i) = make_float2(lo2(Pp[i]), hi2(Pp[i]));
+            *reinterpret_cast<float2*>(a.ws_b + w + 2 * i) = make_float2(lo2(hp[i]), hi2(hp[i]));
+        }
+    }
+}
+
+// B and C as fp32 rows for the [TT x N] fp32 TMA boxes; 8 elements per
+// thread when the arrays allow 16-byte bf16 reads, element-wise otherwise.
+template <typename T>
+__global__ void bc_to_f32_kernel(const T* __restrict__ B, const T* __restrict__ C,
+                                 float* __restrict__ Bf, float* __restrict__ Cf, int64_t n,
+                                 int vec8) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (sizeof(T) == 2 && vec8) {
+        for (; i < n / 8; i += stride) {
+            const uint4 qb = __ldg(reinterpret_cast<const uint4*>(B) + i);
+            const uint4 qc = __ldg(reinterpret_cast<const uint4*>(C) + i);
+            float4* ob = reinterpret_cast<float4*>(Bf) + 2 * i;
+            float4* oc = reinterpret_cast<float4*>(Cf) + 2 * i;
+            ob[0] = make_float4(__uint_as_float(qb.x << 16), __uint_as_float(qb.x & 0xffff0000u),
+                                __uint_as_float(qb.y << 16), __uint_as_float(qb.y & 0xffff0000u));
+            ob[1] = make_float4(__uint_as_float(qb.z << 16), __uint_as_float(qb.z & 0xffff0000u),
+                                __uint_as_float(qb.w << 16), __uint_as_float(qb.w & 0xffff0000u));
+            oc[0] = make_float4(__uint_as_float(qc.x << 16), __uint_as_float(qc.x & 0xffff0000u),
+                                __uint_as_float(qc.y << 16), __uint_as_float(qc.y & 0xffff0000u));
+            oc[1] = make_float4(__uint_as_float(qc.z << 16), __uint_as_float(qc.z & 0xffff0000u),
+                                __uint_as_float(qc.w << 16), __uint_as_float(qc.w & 0xffff0000u));
+        }
+        return;
+    }
+    for (; i < n; i += stride) {
+        Bf[i] = Elem<T>::load(B + i);
+        Cf[i] = Elem<T>::load(C + i);
+    }
+}
+
+// ---- host side ----------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 3-D map over a (batch, L, cols) row-major array, box [box0 cols, box1 steps, 1].
+static bool make_map(CUtensorMap* m, CUtensorMapDataType t, int es, const void* base,
+                     int64_t cols, int64_t L, int64_t batch, int box0, int box1) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)L, (cuuint64_t)batch};
+    cuuint64_t strides[2] = {(cuuint64_t)(cols * es), (cuuint64_t)(L * cols * es)};
+    cuuint32_t box[3] = {(cuuint32_t)box0, (cuuint32_t)box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, t, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tma_scan_supported(int64_t N, int64_t d_inner, msc_dtype dtype, const void* u,
+                        const void* dt, const void* z) {
+    if (!(N == 8 || N == 16 || N == 32 || N == 64)) return false;
+    if (d_inner % 8 != 0) return false;  // whole 8-channel boxes (16 B of bf16)
+    auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    if (!al(u) || !al(dt) || (z && !al(z))) return false;
+    (void)dtype;
+    return encode_fn() != nullptr;
+}
+
+int tma_scan_tile(int64_t N) { return N <= 16 ? 32 : 16; }
+
+template <typename T, int G, int NS, int TT, int S>
+static cudaError_t launch_tma_ns(const ScanArgs& a, const ScanPlan& p, const float* Bf,
+                                 const float* Cf, cudaStream_t s) {
+    using Lay = TmaLayout<T, G, NS, TT, S>;
+    const CUtensorMapDataType tt =
+        sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const int es = (int)sizeof(T);
+    CUtensorMap mu, mdt, mz, mB, mC;
+    if (!make_map(&mu, tt, es, a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_map(&mdt, tt, es, a.dt, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_map(&mz, tt, es, a.z ? a.z : a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_map(&mB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Bf, a.N, a.L, a.batch, (int)a.N, TT) ||
+        !make_map(&mC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Cf, a.N, a.L, a.batch, (int)a.N, TT))
+        return cudaErrorInvalidValue;
+    const size_t smem = Lay::kTotal;
+    if (p.K > 1) {
+        auto kern = scan_tma_kernel<T, G, NS, TT, S, false>;
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        const int64_t nb = a.batch * (int64_t)(p.K - 1) * p.ntile;
+        kern<<<(unsigned)nb, 32, smem, s>>>(mu, mdt, mz, mB, mC, a, p.K - 1);
+    }
+    auto kern = scan_tma_kernel<T, G, NS, TT, S, true>;
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const int64_t nb = a.batch * (int64_t)p.K * p.ntile;
+    const ProfileMark m = profile_begin(s, MSC_PROF_SCAN);
+    kern<<<(unsigned)nb, 32, smem, s>>>(mu, mdt, mz, mB, mC, a, p.K);
+    profile_end(m, s);
+    profile_count(p.K > 1 ? 2 : 1);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_tma_t(const ScanArgs& a, const ScanPlan& p, const float* Bf,
+                                const float* Cf, cudaStream_t s) {
+    if (p.G == 2) {
+        switch (a.N) {
+            case 8: return launch_tma_ns<T, 2, 4, 32, 3>(a, p, Bf, Cf, s);
+            case 16: return launch_tma_ns<T, 2, 8, 32, 3>(a, p, Bf, Cf, s);
+            default: return launch_tma_ns<T, 2, 16, 16, 3>(a, p, Bf, Cf, s);  // 32
+        }
+    }
+    switch (a.N) {
+        case 8: return launch_tma_ns<T, 4, 2, 32, 3>(a, p, Bf, Cf, s);
+        case 16: return launch_tma_ns<T, 4, 4, 32, 3>(a, p, Bf, Cf, s);
+        case 32: return launch_tma_ns<T, 4, 8, 16, 3>(a, p, Bf, Cf, s);
+        default: return launch_tma_ns<T, 4, 16, 16, 2>(a, p, Bf, Cf, s);
+    }
+}
+
+cudaError_t launch_scan_tma(const ScanArgs& a, const ScanPlan& p, msc_dtype dtype, float* Bf,
+                            float* Cf, cudaStream_t s) {
+    const float* Bsrc = static_cast<const float*>(a.B);
+    const float* Csrc = static_cast<const float*>(a.C);
+    const int64_t n = a.batch * a.L * a.N;
+    if (Bf && n > 0) {  // rows converted (or realigned) to fp32 for the TMA boxes
+        const int vec8 = dtype == MSC_BF16 && (n % 8 == 0) &&
+                         (reinterpret_cast<uintptr_t>(a.B) % 16 == 0) &&
+                         (reinterpret_cast<uintptr_t>(a.C) % 16 == 0);
+        const int64_t work = vec8 ? n / 8 : n;
+        const int64_t nb = (work + 255) / 256;
+        const int blocks = (int)(nb < 4096 ? nb : 4096);
+        if (dtype == MSC_BF16)
+            bc_to_f32_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+                static_cast<const __nv_bfloat16*>(a.B), static_cast<const __nv_bfloat16*>(a.C),
+                Bf, Cf, n, vec8);
+        else
+            bc_to_f32_kernel<float><<<blocks, 256, 0, s>>>(Bsrc, Csrc, Bf, Cf, n, 0);
+        Bsrc = Bf;
+        Csrc = Cf;
+        profile_count(1);
+    }
+    if (dtype == MSC_BF16) return launch_tma_t<__nv_bfloat16>(a, p, Bsrc, Csrc, s);
+    return launch_tma_t<float>(a, p, Bsrc, Csrc, s);
+}
+
+cudaError_t scan_error_word(unsigned int* value, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(value, g_scan_error, sizeof(unsigned int));
+    if (e == cudaSuccess && clear && *value) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_scan_error, &zero, sizeof(unsigned int));
+    }
+    return e;
+}
+
+}  // namespace msc

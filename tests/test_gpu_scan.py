@@ -18,16 +18,31 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 
+def _defaults():
+    msc.tuning_set("scan_chunks", 0)
+    msc.tuning_set("scan_min_chunk", 512)
+    msc.tuning_set("scan_path", 0)
+    msc.tuning_set("scan_lanes", 0)
+
+
 @pytest.fixture(autouse=True)
 def _reset_tuning():
-    msc.tuning_set("scan_chunks", 0)
-    msc.tuning_set("scan_min_chunk", 512)
+    _defaults()
     yield
-    msc.tuning_set("scan_chunks", 0)
-    msc.tuning_set("scan_min_chunk", 512)
+    torch.cuda.synchronize()
+    msc.check_device_error()      # no bounded wait gave up during the test
+    _defaults()
 
 
-def run_gpu(x, chunks=0, with_last=True):
+# 0: automatic (the TMA kernels where the shape allows), 1: element-load kernels
+PATHS = [0, 1]
+# lanes per channel of the TMA kernels: 4 (N/4 states each) or 2 (N/2 each)
+LANES = [4, 2]
+
+
+def run_gpu(x, chunks=0, with_last=True, path=0, lanes=0):
+    msc.tuning_set("scan_path", path)
+    msc.tuning_set("scan_lanes", lanes)
     if chunks:
         msc.tuning_set("scan_chunks", chunks)
     a = scan_device_args(x)
@@ -43,8 +58,8 @@ def run_gpu(x, chunks=0, with_last=True):
     return from_device(out), (from_device(last) if with_last else None)
 
 
-def check(x, chunks=0, with_last=True):
-    y, last = run_gpu(x, chunks, with_last)
+def check(x, chunks=0, with_last=True, path=0, lanes=0):
+    y, last = run_gpu(x, chunks, with_last, path, lanes)
     y_ref, last_ref = oracle.scan_fwd(x.u, x.dt_raw, x.A, x.B, x.C, x.D, x.z,
                                       x.dt_bias)
     tol = TOL[x.dtype]
@@ -66,38 +81,76 @@ def test_tiny_f32_workload():
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("d_state", [1, 2, 3, 4, 5, 8, 12, 16, 24, 32, 33, 64])
-def test_state_sizes(dtype, d_state):
-    x = synth.scan_inputs(2, 77, 45, d_state, dtype=dtype, seed=100 + d_state,
-                          D="normal", A_kind="random")
+@pytest.mark.parametrize("d_inner", [45, 64])
+def test_state_sizes(dtype, d_state, d_inner):
+    """d_inner = 64 takes the TMA kernels for d_state in {8, 16, 32, 64};
+    45 channels (not a multiple of 8) and other d_state take the
+    element-load kernels."""
+    x = synth.scan_inputs(2, 77, d_inner, d_state, dtype=dtype,
+                          seed=100 + d_state, D="normal", A_kind="random")
     check(x)
+
+
+@pytest.mark.parametrize("lanes", LANES)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d_state", [8, 16, 32, 64])
+def test_tma_lane_splits(dtype, d_state, lanes):
+    """Both lane splits of the TMA kernels (2 lanes per channel is taken for
+    d_state <= 32 only), 3 chunks, ragged tail."""
+    x = synth.scan_inputs(2, 333, 96, d_state, dtype=dtype,
+                          seed=200 + d_state, D="normal", A_kind="random")
+    check(x, chunks=3, lanes=lanes)
+
+
+@pytest.mark.parametrize("path,lanes", [(0, 4), (0, 2), (1, 0)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("chunks", [1, 2, 3, 7, 64])
+def test_chunked_carry(dtype, chunks, path, lanes):
+    """Time cut into chunks joined by the carry pass, ragged last chunk."""
+    x = synth.scan_inputs(3, 517, 208, 16, dtype=dtype, seed=7 + chunks,
+                          D="normal")
+    check(x, chunks=chunks, path=path, lanes=lanes)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("chunks", [1, 2, 3, 7, 64])
-def test_chunked_carry(dtype, chunks):
-    """Time cut into chunks joined by the carry pass, ragged last chunk."""
-    x = synth.scan_inputs(3, 517, 200, 16, dtype=dtype, seed=7 + chunks,
-                          D="normal")
-    check(x, chunks=chunks)
+def test_tma_path_is_taken(dtype):
+    """Aligned 16-state shapes run the TMA kernels: for bf16 a B/C
+    conversion kernel plus the scan kernel, for fp32 the scan kernel alone
+    (the element-load kernels would launch one)."""
+    x = synth.scan_inputs(2, 256, 64, 16, dtype=dtype, seed=31)
+    msc.tuning_set("scan_chunks", 1)
+    msc.profile_read()
+    msc.profile_enable(True)
+    try:
+        check(x, chunks=1)
+        launches, kinds = msc.profile_read()
+    finally:
+        msc.profile_enable(False)
+    timed, ms = kinds["scan"]
+    assert timed == 1 and ms > 0.0 and kinds["update"][0] == 0
+    assert launches == (2 if dtype == "bf16" else 1)
 
 
-@pytest.mark.parametrize("L", [1, 2, 5, 129])
-def test_short_sequences(L):
-    x = synth.scan_inputs(2, L, 33, 16, dtype="f32", seed=L)
-    check(x)
-    check(x, chunks=L)          # one step per chunk
+@pytest.mark.parametrize("d_inner,lanes", [(33, 0), (40, 4), (48, 2)])
+@pytest.mark.parametrize("L", [1, 2, 5, 7, 8, 9, 31, 32, 33, 129])
+def test_short_sequences(L, d_inner, lanes):
+    x = synth.scan_inputs(2, L, d_inner, 16, dtype="f32", seed=L)
+    check(x, lanes=lanes)
+    check(x, chunks=L, lanes=lanes)   # one step (or one tile) per chunk
 
 
-def test_empty_sequence_zeroes_last_state():
+@pytest.mark.parametrize("path", PATHS)
+def test_empty_sequence_zeroes_last_state(path):
     x = synth.scan_inputs(2, 0, 40, 16, dtype="bf16", seed=1)
-    y, last = run_gpu(x)
+    y, last = run_gpu(x, path=path)
     assert y.size == 0
     assert np.all(last == 0.0)
 
 
+@pytest.mark.parametrize("d_inner", [70, 72])
 @pytest.mark.parametrize("drop", ["z", "D", "dt_bias", "all"])
-def test_optional_inputs_absent(drop):
-    x = synth.scan_inputs(2, 300, 70, 16, dtype="f32", seed=3, D="normal")
+def test_optional_inputs_absent(drop, d_inner):
+    x = synth.scan_inputs(2, 300, d_inner, 16, dtype="f32", seed=3, D="normal")
     if drop in ("z", "all"):
         x.z = None
     if drop in ("D", "all"):
@@ -155,11 +208,23 @@ def test_caller_workspace_variant():
     assert rel_l2(from_device(last), last_ref) <= TOL["f32"]
 
 
-def test_repeatable_bitwise():
+@pytest.mark.parametrize("path", PATHS)
+def test_repeatable_bitwise(path):
     x = synth.scan_inputs(2, 700, 128, 16, dtype="bf16", seed=9)
-    y1, l1 = run_gpu(x, chunks=3)
-    y2, l2 = run_gpu(x, chunks=3)
+    y1, l1 = run_gpu(x, chunks=3, path=path)
+    y2, l2 = run_gpu(x, chunks=3, path=path)
     assert np.array_equal(y1, y2) and np.array_equal(l1, l2)
+
+
+def test_paths_agree():
+    """TMA (both lane splits) and element-load kernels compute the same
+    recurrence; they may differ only by fp32 rounding."""
+    x = synth.scan_inputs(2, 900, 64, 16, dtype="f32", seed=10, D="normal")
+    y0, l0 = run_gpu(x, chunks=2, path=0, lanes=4)
+    y1, l1 = run_gpu(x, chunks=2, path=1)
+    y2, l2 = run_gpu(x, chunks=2, path=0, lanes=2)
+    assert rel_l2(y0, y1) <= 1e-6 and rel_l2(l0, l1) <= 1e-6
+    assert rel_l2(y2, y1) <= 1e-6 and rel_l2(l2, l1) <= 1e-6
 
 
 # ---- the workloads at reduced size (several tiles, ragged tails) ---------
