@@ -63,6 +63,11 @@ def parse():
                     help="target host time of the CPU-oracle sample")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the other workloads")
+    ap.add_argument("--profile", default=None, metavar="WORKLOAD",
+                    help="profiling driver: run only the scan (or, for "
+                         "decode_256x5120, the decode step) on WORKLOAD "
+                         "--warmup + --steps times, print nothing else "
+                         "(for ncu; see profiles/)")
     return ap.parse_args()
 
 
@@ -562,10 +567,60 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
     return res
 
 
+def run_profile(args):
+    """Run one workload's main kernel alone, for ncu captures: W + K calls
+    of the scan (or of the decode step), nothing timed, nothing printed but
+    a completion line."""
+    import torch
+    import selective_state_space_144_b300 as msc
+    from selective_state_space_144_b300 import build as msc_build
+    msc_build.build()
+    dev = torch.device("cuda", 0)
+    name = args.profile
+
+    def dev_t(arr, kind):
+        if kind == "bf16":
+            bits = synth.bf16_bits(arr).view(np.int16)
+            return torch.from_numpy(bits.copy()).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(arr, np.float32)).to(dev)
+
+    w = synth.WORKLOADS[name]
+    if name.startswith("decode"):
+        Bb, Dd, Nn = w["batch"], w["d_inner"], w["d_state"]
+        p = synth.decode_params(Bb, Dd, Nn)
+        s = synth.decode_step(Bb, Dd, Nn, 0)
+        state = torch.from_numpy(p.state0).to(dev)
+        args_ = (dev_t(s.u, "bf16"), dev_t(s.dt_raw, "bf16"), dev_t(p.A, "f32"),
+                 dev_t(s.B, "bf16"), dev_t(s.C, "bf16"), dev_t(p.D, "f32"),
+                 dev_t(s.z, "bf16"), dev_t(p.dt_bias, "f32"))
+        for _ in range(args.warmup + args.steps):
+            msc.selective_state_update(state, *args_)
+    else:
+        x = synth.workload_inputs(name)
+        kind = w["dtype"]
+        a = dict(u=dev_t(x.u, kind), dt=dev_t(x.dt_raw, kind), A=dev_t(x.A, "f32"),
+                 B=dev_t(x.B, kind), C=dev_t(x.C, kind), D=dev_t(x.D, "f32"),
+                 z=dev_t(x.z, kind), dt_bias=dev_t(x.dt_bias, "f32"))
+        del x
+        B_, L_, D_, N_ = w["batch"], w["L"], w["d_inner"], w["d_state"]
+        out = torch.empty_like(a["u"])
+        last = torch.empty(B_, D_, N_, dtype=torch.float32, device=dev)
+        n = msc.scan_workspace_size(B_, L_, D_, N_, a["u"].dtype)
+        wsp = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+        for _ in range(args.warmup + args.steps):
+            msc.selective_scan_fwd_ws(**a, out=out, last_state=last, workspace=wsp)
+    torch.cuda.synchronize(dev)
+    msc.check_device_error()
+    print(f"profile run done: {name}, {args.warmup + args.steps} calls", flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile:
+        return run_profile(args)
     return run_ours(args)
 
 

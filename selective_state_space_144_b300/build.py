@@ -9,6 +9,7 @@ A library is rebuilt when any of its sources or headers is newer than it.
 from __future__ import annotations
 
 import glob
+import hashlib
 import os
 import subprocess
 import sys
@@ -33,11 +34,25 @@ def lib_path(name: str) -> str:
     return os.path.join(PKG, name)
 
 
-def _stale(target: str, deps: list[str]) -> bool:
-    if not os.path.exists(target):
+def _digest(deps: list[str], cmd: list[str]) -> str:
+    """Content hash of the sources, headers and compile command."""
+    h = hashlib.sha256()
+    for d in sorted(deps):
+        h.update(os.path.basename(d).encode())
+        with open(d, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(cmd).encode())
+    return h.hexdigest()
+
+
+def _stale(target: str, digest: str) -> bool:
+    """A library is rebuilt when missing or built from other content (file
+    times are not used: copies of the tree do not preserve them)."""
+    stamp = target + ".sha256"
+    if not os.path.exists(target) or not os.path.exists(stamp):
         return True
-    t = os.path.getmtime(target)
-    return any(os.path.getmtime(d) > t for d in deps)
+    with open(stamp) as f:
+        return f.read().strip() != digest
 
 
 def build(force: bool = False, verbose: bool = False) -> list[str]:
@@ -49,7 +64,8 @@ def build(force: bool = False, verbose: bool = False) -> list[str]:
     for name, srcs in LIBS.items():
         target = lib_path(name)
         paths = [os.path.join(CSRC, s) for s in srcs]
-        if force or _stale(target, paths + headers):
+        digest = _digest(paths + headers, [*ARCH, *FLAGS])
+        if force or _stale(target, digest):
             tmp = target + f".tmp{os.getpid()}"
             cmd = [NVCC, *ARCH, *FLAGS, "-o", tmp, *paths, "-lcudart"]
             res = subprocess.run(cmd, capture_output=True, text=True)
@@ -59,6 +75,8 @@ def build(force: bool = False, verbose: bool = False) -> list[str]:
             if verbose:
                 sys.stderr.write(res.stderr)
             os.replace(tmp, target)
+            with open(target + ".sha256", "w") as f:
+                f.write(digest + "\n")
         out.append(target)
     return out
 

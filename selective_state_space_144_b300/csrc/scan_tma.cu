@@ -144,6 +144,39 @@ __device__ __forceinline__ void reduce_scatter(const float (&y)[kOct], int lane,
     }
 }
 
+// Per-(step, channel) prologue of one octet: delta = softplus(dt + dt_bias)
+// and delta*u for steps g + G*m (m < 8/G) of the octet whose first row is
+// `row0` of the tile at `stage`; written to `dst` (the lane's slot of one
+// sDU buffer, rows CPW apart) for the core.  The u of those steps is
+// returned as pairs for the D*u term.  MASK: steps at or past `nsteps` get
+// delta = 0 (state passes through, no input).
+template <typename T, int G, int TT, bool MASK>
+__device__ __forceinline__ void octet_prologue(const unsigned char* stage, int row0, int lane_x,
+                                               float2* dst, u64 bias2, int s0_first,
+                                               int nsteps, u64 (&uu)[kOct / G / 2]) {
+    constexpr int CPW = 32 / G;
+    constexpr int PPL = kOct / G / 2;
+    const T* sx = reinterpret_cast<const T*>(stage) + row0 * CPW + lane_x;
+#pragma unroll
+    for (int p = 0; p < PPL; ++p) {
+        const int r0 = G * (2 * p) * CPW, r1 = r0 + G * CPW;
+        uu[p] = pk2(lds_elem<T>(sx + r0), lds_elem<T>(sx + r1));
+        const u64 x =
+            add2(pk2(lds_elem<T>(sx + TT * CPW + r0), lds_elem<T>(sx + TT * CPW + r1)), bias2);
+        const u64 dl = softplus2(x);
+        const u64 du = mul2(dl, uu[p]);
+        if (MASK) {
+            const int s0 = s0_first + G * (2 * p);
+            const bool v0 = s0 < nsteps, v1 = s0 + G < nsteps;
+            dst[(2 * p) * G * CPW] = make_float2(v0 ? lo2(dl) : 0.0f, v0 ? lo2(du) : 0.0f);
+            dst[(2 * p + 1) * G * CPW] = make_float2(v1 ? hi2(dl) : 0.0f, v1 ? hi2(du) : 0.0f);
+        } else {
+            dst[(2 * p) * G * CPW] = make_float2(lo2(dl), lo2(du));
+            dst[(2 * p + 1) * G * CPW] = make_float2(hi2(dl), hi2(du));
+        }
+    }
+}
+
 template <typename T, int G, int NS, int TT, int S, bool OUTPUT>
 __global__ void __launch_bounds__(32)
 scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dt,
@@ -227,51 +260,35 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         }
     }
 
-    float2* sDU = reinterpret_cast<float2*>(smem + Lay::kDU);
-    auto stage = [&](int i) -> const unsigned char* { return smem + (i % S) * Lay::kStage; };
+    float2* const sDU = reinterpret_cast<float2*>(smem + Lay::kDU);
     const u64 bias2 = pk2(bias, bias);
+    const int lane_x = g * CPW + ch;  // element (row g, channel ch) of a [row][CPW] tile
 
-    // delta and delta*u of steps g + G*m (m < SPL) of the octet starting at
-    // row `row0` of tile `i` (chunk step `s_base`), posted to buffer `buf`
-    // for its core; the u of those steps is returned as pairs
-    auto prologue = [&](int i, int row0, int s_base, int buf, u64 (&uu)[PPL]) {
-        const T* sx = reinterpret_cast<const T*>(stage(i)) + (row0 + g) * CPW + ch;
-        float2* dst = sDU + buf * (kOct * CPW) + g * CPW + ch;
-#pragma unroll
-        for (int p = 0; p < PPL; ++p) {
-            const int r0 = G * (2 * p) * CPW, r1 = r0 + G * CPW;
-            uu[p] = pk2(lds_elem<T>(sx + r0), lds_elem<T>(sx + r1));
-            const u64 x = add2(pk2(lds_elem<T>(sx + TT * CPW + r0),
-                                   lds_elem<T>(sx + TT * CPW + r1)),
-                               bias2);
-            const u64 dl = softplus2(x);
-            const u64 du = mul2(dl, uu[p]);
-            const int s0 = s_base + g + G * (2 * p);
-            const bool v0 = s0 < nsteps, v1 = s0 + G < nsteps;
-            dst[(2 * p) * G * CPW] = make_float2(v0 ? lo2(dl) : 0.0f, v0 ? lo2(du) : 0.0f);
-            dst[(2 * p + 1) * G * CPW] = make_float2(v1 ? hi2(dl) : 0.0f, v1 ? hi2(du) : 0.0f);
-        }
-    };
 
     bool ok = ntiles == 0 || __all_sync(0xffffffffu, mbar_wait(bar0, 0, kWaitLimit));
     int waited = ntiles > 0 ? 1 : 0;  // tiles [0, waited) are known complete
     u64 u_cur[PPL], u_nxt[PPL];
 #pragma unroll
     for (int p = 0; p < PPL; ++p) u_cur[p] = u_nxt[p] = pk2(0.0f, 0.0f);
-    if (ok && ntiles > 0) prologue(0, 0, 0, 0, u_cur);
+    if (ok && ntiles > 0)
+        octet_prologue<T, G, TT, true>(smem, 0, lane_x, sDU + lane_x, bias2, g, nsteps, u_cur);
     __syncwarp();
 
     const u64 D2 = pk2(Dd, Dd);
-    T* const out_ch = static_cast<T*>(a.out) + ((int64_t)b * a.L + tc0 + g) * a.d_inner + d;
+    const int64_t dinner = a.d_inner;
+    const int64_t gstride = (int64_t)G * dinner;  // output rows G apart
+    T* out_p = static_cast<T*>(a.out) + ((int64_t)b * a.L + tc0 + g) * dinner + d;
+    int st_idx = 0;                               // stage of tile i
 
     // One tile: OPT octets, unrolled so that every shared-memory offset is a
     // constant.  FULL: the tile lies inside the chunk, no step is masked.
     auto tile_body = [&](int i, auto full_tag) {
         constexpr bool FULL = decltype(full_tag)::value;
-        const unsigned char* st = stage(i);
+        const unsigned char* st = smem + st_idx * Lay::kStage;
+        const int nxt_idx = st_idx + 1 == S ? 0 : st_idx + 1;
         const float* sB0 = reinterpret_cast<const float*>(st + 3 * Lay::kX) + n0;
         const float* sC0 = reinterpret_cast<const float*>(st + 3 * Lay::kX + Lay::kBC) + n0;
-        const T* sz0 = reinterpret_cast<const T*>(st + 2 * Lay::kX) + g * CPW + ch;
+        const T* sz0 = reinterpret_cast<const T*>(st + 2 * Lay::kX) + lane_x;
 #pragma unroll
         for (int oo = 0; oo < OPT; ++oo) {
             const int sb = i * TT + kOct * oo;  // chunk step of the octet's first row
@@ -319,32 +336,44 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             }
             // (2) the next octet's step sizes, after the core's reads of this
             //     octet's (next tile: wait for it first)
+            float2* const dnx = sDU + ((oo + 1) & 1) * (kOct * CPW) + lane_x;
             if (oo + 1 < OPT) {
-                prologue(i, kOct * (oo + 1), sb + kOct, (oo + 1) & 1, u_nxt);
+                octet_prologue<T, G, TT, !FULL>(st, kOct * (oo + 1), lane_x, dnx, bias2,
+                                                sb + kOct + g, nsteps, u_nxt);
             } else if (i + 1 < ntiles) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * ((i + 1) % S),
+                ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * nxt_idx,
                                                        ((i + 1) / S) & 1, kWaitLimit));
                 if (!ok) return;
                 waited = i + 2;
-                prologue(i + 1, 0, sb + kOct, (oo + 1) & 1, u_nxt);
+                const unsigned char* stn = smem + nxt_idx * Lay::kStage;
+                if ((i + 2) * TT <= nsteps)
+                    octet_prologue<T, G, TT, false>(stn, 0, lane_x, dnx, bias2, sb + kOct + g,
+                                                    nsteps, u_nxt);
+                else
+                    octet_prologue<T, G, TT, true>(stn, 0, lane_x, dnx, bias2, sb + kOct + g,
+                                                   nsteps, u_nxt);
             }
             // (3) outputs of steps g + G*m of channel ch
             if (OUTPUT) {
                 float ys[SPL];
                 reduce_scatter<G>(yv, lane, ys);
-                T* op = out_ch + (int64_t)sb * a.d_inner;
 #pragma unroll
                 for (int p = 0; p < PPL; ++p) {
                     u64 y2 = fma2(D2, u_cur[p], pk2(ys[2 * p], ys[2 * p + 1]));
                     const int r0 = (kOct * oo + G * (2 * p)) * CPW, r1 = r0 + G * CPW;
                     if (has_z)
                         y2 = mul2(y2, silu2(pk2(lds_elem<T>(sz0 + r0), lds_elem<T>(sz0 + r1))));
-                    const int s0 = sb + g + G * (2 * p);
-                    if (FULL || s0 < nsteps)
-                        Elem<T>::store(op + (int64_t)(G * 2 * p) * a.d_inner, lo2(y2));
-                    if (FULL || s0 + G < nsteps)
-                        Elem<T>::store(op + (int64_t)(G * (2 * p + 1)) * a.d_inner, hi2(y2));
+                    T* op = out_p + (2 * p) * gstride;
+                    if (FULL) {
+                        Elem<T>::store(op, lo2(y2));
+                        Elem<T>::store(op + gstride, hi2(y2));
+                    } else {
+                        const int s0 = sb + g + G * (2 * p);
+                        if (s0 < nsteps) Elem<T>::store(op, lo2(y2));
+                        if (s0 + G < nsteps) Elem<T>::store(op + gstride, hi2(y2));
+                    }
                 }
+                out_p += kOct * dinner;
             }
             __syncwarp();
 #pragma unroll
@@ -358,6 +387,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             }
             issued = i + S + 1;
         }
+        st_idx = nxt_idx;
     };
 
     for (int i = 0; ok && i < ntiles; ++i) {
