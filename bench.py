@@ -186,6 +186,20 @@ def dist_env():
     return ws, rank, local
 
 
+def combine_ranks(elapsed_ms: float, units_per_step: float, steps: int,
+                  world: int, device=None) -> tuple[float, float]:
+    """Whole-job timing of a weak-scaling run: the slowest rank's elapsed
+    time (all_reduce MAX over the default process group when world > 1) and
+    the throughput of all ranks' units over it."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    return elapsed_ms, units_per_step * steps * world / (elapsed_ms * 1e-3)
+
+
 def cpu_oracle_sample(name: str, target_s: float, max_channels=None):
     """Time the fp64 oracle on a channel subset of workload `name` (every
     batch row, every step) sized to about `target_s` seconds of host time.
@@ -349,12 +363,8 @@ def run_ours(args):
     msc.profile_enable(False)
     launches, kinds = msc.profile_read()
     msc.check_device_error()
-    el_ms = e0.elapsed_time(e1)
-    if ws_n > 1:
-        t = torch.tensor([el_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el_ms = float(t.item())
-    value = upd_step * args.steps * ws_n / (el_ms * 1e-3)
+    el_ms, value = combine_ranks(e0.elapsed_time(e1), upd_step, args.steps,
+                                 ws_n, device=dev)
 
     if rank != 0:
         dist.destroy_process_group()
