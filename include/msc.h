@@ -64,8 +64,10 @@ typedef enum msc_status {
     MSC_ERR_ALIGNMENT = 3,    /* a pointer not aligned to its element size */
     MSC_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
     MSC_ERR_WORKSPACE = 5,    /* workspace NULL, smaller than required or misaligned */
-    MSC_ERR_TIMEOUT = 6       /* a kernel gave up waiting for a data copy (see
+    MSC_ERR_TIMEOUT = 6,      /* a kernel gave up waiting for a data copy (see
                                  msc_check_device_error) */
+    MSC_ERR_SCRATCH_LIMIT = 7 /* msc_selective_scan_fwd_noalloc: the problem needs
+                                 more scratch than MSC_NOALLOC_SCRATCH_BYTES */
 } msc_status;
 
 /*
@@ -107,6 +109,38 @@ msc_status msc_selective_scan_fwd_ws(
     void* out, float* last_state, int64_t batch, int64_t L, int64_t d_inner,
     int64_t d_state, msc_dtype dtype, void* workspace,
     size_t workspace_bytes, msc_stream_t stream);
+
+/*
+ * Allocation-free variant of msc_selective_scan_fwd (the pages have no
+ * counterpart: this is a deployment facility of this library).
+ *
+ * Some callers cannot call cudaMalloc or cudaMallocAsync on the path that
+ * runs the scan: a serving runtime that reserves all device memory through
+ * its own allocator at start-up and forbids allocation while requests are
+ * in flight, or a host application whose memory manager owns the device.
+ * This entry point takes the same arguments as msc_selective_scan_fwd and
+ * allocates nothing.  The scratch the scan needs (chunk carries, fp32 copies
+ * of B and C) lives in one file-scope device array of
+ * MSC_NOALLOC_SCRATCH_BYTES (16 MiB), which every GPU that loads the library
+ * holds until the process exits.
+ *   - A problem whose plan needs more scratch than that returns
+ *     MSC_ERR_SCRATCH_LIMIT before anything is launched (query the need with
+ *     msc_selective_scan_workspace_size).
+ *   - The first call on each device looks up the array's device address
+ *     with cudaGetSymbolAddress while that device is current; make that
+ *     first call before any stream capture on that device.
+ *   - All calls share the one array, and it keeps the last call's contents;
+ *     nothing in it needs to start at zero (every byte a call reads was
+ *     written earlier in the same call).  Calls whose executions overlap on
+ *     the GPU (different streams, no ordering between them) race on it.
+ * Other behaviour, layouts and errors are those of msc_selective_scan_fwd.
+ */
+#define MSC_NOALLOC_SCRATCH_BYTES (16u << 20)
+msc_status msc_selective_scan_fwd_noalloc(
+    const void* u, const void* dt, const float* A, const void* B,
+    const void* C, const float* D, const void* z, const float* dt_bias,
+    void* out, float* last_state, int64_t batch, int64_t L, int64_t d_inner,
+    int64_t d_state, msc_dtype dtype, msc_stream_t stream);
 
 /*
  * Single-token selective state update (decode).

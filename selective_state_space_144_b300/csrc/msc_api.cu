@@ -3,6 +3,7 @@
 // include/msc.h.
 #include <cstring>
 #include <limits>
+#include <mutex>
 #include <vector>
 
 #include "msc_internal.h"
@@ -207,7 +208,49 @@ static msc_status run_scan(const void* u, const void* dt, const float* A, const 
     return e == cudaSuccess ? MSC_OK : MSC_ERR_CUDA;
 }
 
+// ---- allocation-free scan: scratch in a file-scope device array ------------
+// Callers that may not allocate device memory (a runtime whose allocator owns
+// the device, no allocation while requests are served) get the scan with its
+// scratch here.  Host code must not use the array's name as an address: its
+// device address is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MSC_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoallocMaxDevices] = {};
+}  // namespace
+
 extern "C" {
+
+msc_status msc_selective_scan_fwd_noalloc(const void* u, const void* dt, const float* A,
+                                          const void* B, const void* C, const float* D,
+                                          const void* z, const float* dt_bias, void* out,
+                                          float* last_state, int64_t batch, int64_t L,
+                                          int64_t d_inner, int64_t d_state, msc_dtype dtype,
+                                          msc_stream_t stream) {
+    ScanCheck c = check_scan(u, dt, A, B, C, D, z, dt_bias, out, last_state, batch, L, d_inner,
+                             d_state, dtype);
+    if (c.st != MSC_OK) return c.st;
+    if (batch == 0 || d_inner == 0) return MSC_OK;
+    if (c.plan.ws_bytes > MSC_NOALLOC_SCRATCH_BYTES) return MSC_ERR_SCRATCH_LIMIT;
+    void* scratch = nullptr;
+    if (c.plan.ws_bytes > 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return MSC_ERR_CUDA;
+        if (dev < 0 || dev >= kNoallocMaxDevices) return MSC_ERR_UNSUPPORTED;
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_addr[dev]) {  // set-up, once per device, that device current
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+                return MSC_ERR_CUDA;
+            g_noalloc_addr[dev] = p;
+        }
+        scratch = g_noalloc_addr[dev];
+    }
+    return run_scan(u, dt, A, B, C, D, z, dt_bias, out, last_state, batch, L, d_inner, d_state,
+                    dtype, scratch, MSC_NOALLOC_SCRATCH_BYTES, false, stream);
+}
 
 msc_status msc_selective_scan_fwd(const void* u, const void* dt, const float* A, const void* B,
                                   const void* C, const float* D, const void* z,
@@ -365,6 +408,8 @@ const char* msc_status_string(msc_status s) {
         case MSC_ERR_CUDA: return "CUDA runtime error";
         case MSC_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
         case MSC_ERR_TIMEOUT: return "a kernel's bounded wait for a data copy gave up";
+        case MSC_ERR_SCRATCH_LIMIT:
+            return "problem needs more scratch than the allocation-free entry point holds";
     }
     return "unknown status";
 }

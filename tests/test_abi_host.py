@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(8):
         s = lib.msc_status_string(code)
         assert s and s != b"unknown status"
     assert lib.msc_status_string(99) == b"unknown status"
@@ -157,3 +157,22 @@ def test_python_binding_fails_loudly_without_cuda_tensors():
     with pytest.raises(ValueError):
         msc.selective_scan_fwd(x, x, torch.zeros(8, 4), torch.zeros(1, 4, 4),
                                torch.zeros(1, 4, 4))
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(lib):
+    """The allocation-free entry point refuses, before any device work, a
+    problem whose scratch exceeds its fixed 16 MiB: 64 time chunks of a
+    4 x 4096 x 1024 x 16 scan need 33 MB of chunk carries under either
+    kernel family."""
+    f = lib.msc_selective_scan_fwd_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = ([ctypes.c_void_p] * 10 + [ctypes.c_int64] * 4
+                  + [ctypes.c_int, ctypes.c_void_p])
+    assert lib.msc_tuning_set(b"scan_chunks", 64) == 0
+    try:
+        st = f(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, None,
+               4, 4096, 1024, 16, 1, None)
+    finally:
+        lib.msc_tuning_set(b"scan_chunks", 0)
+    assert st == 7
+    assert lib.msc_status_string(7) != b"unknown status"
