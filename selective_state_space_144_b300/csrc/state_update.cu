@@ -6,8 +6,10 @@
 //     delta = softplus(dt + dt_bias);  h = exp(delta*A) * h + delta*B*u
 //     out = (C . h + D*u) * silu(z)
 // The step is bound by streaming the fp32 state (8 bytes per state element
-// per step); a thread owns 4 consecutive states of one channel so that the
-// state moves in 16-byte vectors and a warp touches 512 contiguous bytes.
+// per step).  state_update_row_kernel (N = 8, 16, 32, aligned arrays) keeps
+// a whole channel per thread; state_update_kernel is the general form, a
+// thread per 4 consecutive states with a shuffle reduction over the lanes of
+// a channel.
 #include "msc_device.cuh"
 #include "msc_internal.h"
 
@@ -78,8 +80,67 @@ state_update_kernel(UpdateArgs a) {
     }
 }
 
+// Channel-per-thread decode step for N in {8, 16, 32}: a thread keeps all N
+// states of its channel, so softplus and the gate are evaluated once per
+// channel; B and C of the batch row are staged once per CTA in shared memory
+// as fp32.  Grid (d_inner / 128, batch): no index division.  The state moves
+// as N/4 16-byte loads and stores per thread (the warp's 32 x N*4 bytes are
+// contiguous, so every fetched sector is used).
+template <typename T, int N>
+__global__ void __launch_bounds__(128)
+state_update_row_kernel(UpdateArgs a) {
+    __shared__ float sB[N], sC[N];
+    const int b = blockIdx.y;
+    if (threadIdx.x < N) {
+        sB[threadIdx.x] = Elem<T>::load(static_cast<const T*>(a.B) + (int64_t)b * N + threadIdx.x);
+        sC[threadIdx.x] = Elem<T>::load(static_cast<const T*>(a.C) + (int64_t)b * N + threadIdx.x);
+    }
+    __syncthreads();
+    const int64_t d = (int64_t)blockIdx.x * 128 + threadIdx.x;
+    if (d >= a.d_inner) return;
+    const int64_t ch = (int64_t)b * a.d_inner + d;
+    float4* srow = reinterpret_cast<float4*>(a.state + ch * N);
+    const float4* arow = reinterpret_cast<const float4*>(a.A + d * N);
+    float h[N], Av[N];
+#pragma unroll
+    for (int q = 0; q < N / 4; ++q) {
+        const float4 v = srow[q];
+        h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
+        const float4 w = __ldg(arow + q);
+        Av[4 * q] = w.x; Av[4 * q + 1] = w.y; Av[4 * q + 2] = w.z; Av[4 * q + 3] = w.w;
+    }
+    const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
+    const float x = Elem<T>::load(static_cast<const T*>(a.dt) + ch) + bias;
+    const float uu = Elem<T>::load(static_cast<const T*>(a.u) + ch);
+    const float delta = softplus(x);
+    const float du = delta * uu;
+    float y = 0.0f;
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+        const float dA = ex2(delta * (Av[n] * kLog2e));  // same rounding as the scan
+        h[n] = fmaf(dA, h[n], du * sB[n]);
+        y = fmaf(sC[n], h[n], y);
+    }
+#pragma unroll
+    for (int q = 0; q < N / 4; ++q)
+        srow[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+    y = fmaf(a.D ? __ldg(a.D + d) : 0.0f, uu, y);
+    if (a.z) y *= silu(Elem<T>::load(static_cast<const T*>(a.z) + ch));
+    Elem<T>::store(static_cast<T*>(a.out) + ch, y);
+}
+
 template <typename T, bool VEC>
 static cudaError_t launch_update_v(const UpdateArgs& a, cudaStream_t s) {
+    if (VEC && a.batch <= 65535 && (a.N == 8 || a.N == 16 || a.N == 32) &&
+        reinterpret_cast<uintptr_t>(a.A) % 16 == 0) {
+        const dim3 grid((unsigned)((a.d_inner + 127) / 128), (unsigned)a.batch);
+        switch (a.N) {
+            case 8: state_update_row_kernel<T, 8><<<grid, 128, 0, s>>>(a); break;
+            case 16: state_update_row_kernel<T, 16><<<grid, 128, 0, s>>>(a); break;
+            default: state_update_row_kernel<T, 32><<<grid, 128, 0, s>>>(a); break;
+        }
+        return cudaGetLastError();
+    }
     const int G = lanes_per_channel(a.N);
     const int64_t threads = a.batch * a.d_inner * G;
     const unsigned nb = (unsigned)((threads + kUpdateThreads - 1) / kUpdateThreads);

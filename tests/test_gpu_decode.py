@@ -54,7 +54,7 @@ def run_decode(batch, d_inner, d_state, steps, dtype, sel=None, seed=4,
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("d_state", [1, 3, 4, 5, 16, 33, 64])
+@pytest.mark.parametrize("d_state", [1, 3, 4, 5, 8, 16, 32, 33, 64])
 def test_decode_small(dtype, d_state):
     e_out, e_state = run_decode(3, 50, d_state, 6, dtype, seed=10 + d_state)
     assert e_out <= TOL[dtype], e_out
@@ -105,3 +105,24 @@ def test_decode_steps_equal_scan(dtype):
     y_dec = torch.stack(outs, dim=1)
     assert rel_l2(from_device(y_dec), from_device(y)) <= 1e-6
     assert rel_l2(from_device(state), from_device(last)) <= 1e-6
+
+
+def test_decode_general_kernel_with_unaligned_A():
+    """A whose rows are not 16-byte aligned takes the general decode kernel
+    (a thread per 4 states); same parity bar."""
+    batch, d_inner, N = 4, 64, 16
+    p = synth.decode_params(batch, d_inner, N, seed=31, dtype="f32")
+    s = synth.decode_step(batch, d_inner, N, 0, seed=31, dtype="f32")
+    flat = torch.empty(d_inner * N + 1, device="cuda")
+    A_d = flat[1:].view(d_inner, N)
+    A_d.copy_(torch.from_numpy(p.A))
+    state = torch.from_numpy(p.state0).cuda()
+    dv = _step_dev(s, "f32")
+    out = msc.selective_state_update(state, dv["u"], dv["dt"], A_d, dv["B"], dv["C"],
+                                     to_device(p.D, "f32"), dv["z"],
+                                     to_device(p.dt_bias, "f32"))
+    torch.cuda.synchronize()
+    ref_state, ref_out = oracle.state_update(p.state0, s.u, s.dt_raw, p.A, s.B, s.C,
+                                             p.D, s.z, p.dt_bias)
+    assert rel_l2(from_device(out), ref_out) <= TOL["f32"]
+    assert rel_l2(from_device(state), ref_state) <= TOL["f32"]
