@@ -173,8 +173,6 @@ msc_status msc_check_device_error(int clear);
  *   "scan_min_chunk" shortest chunk the automatic plan will make (steps)
  *   "scan_path"     0 = automatic, 1 = element-load kernels only (no TMA)
  *   "scan_lanes"    lanes per channel of the TMA kernels: 0 = automatic, 2, 4
- *   "scan_kernel"   TMA output kernel: 0 = automatic, 1 = one warp per CTA,
- *                   2 = warp-specialised (a core warp and a scalar warp)
  * Process-wide and not thread-safe; returns MSC_ERR_INVALID_ARG for an
  * unknown key or a negative value.
  */

@@ -69,9 +69,9 @@ class Oracle:
         lib.oracle_threads.restype = ctypes.c_int
         lib.oracle_threads.argtypes = [ctypes.c_int]
         lib.oracle_scan_fwd.restype = ctypes.c_int
-        lib.oracle_scan_fwd.argtypes = [dp] * 11 + [i64] * 4 + [ctypes.c_int]
+        lib.oracle_scan_fwd.argtypes = [dp] * 11 + [i64] * 4 + [ctypes.c_int] * 2
         lib.oracle_state_update.restype = ctypes.c_int
-        lib.oracle_state_update.argtypes = [dp] * 10 + [i64] * 3 + [ctypes.c_int]
+        lib.oracle_state_update.argtypes = [dp] * 10 + [i64] * 3 + [ctypes.c_int] * 2
         lib.oracle_scan_fwd_segmented.restype = ctypes.c_int
         lib.oracle_scan_fwd_segmented.argtypes = ([dp] * 10 + [i64] * 5
                                                   + [ctypes.c_int])
@@ -91,8 +91,11 @@ class Oracle:
         return float(self.lib.oracle_silu(float(z)))
 
     def scan_fwd(self, u, dt_raw, A, B, C, D=None, z=None, dt_bias=None,
-                 h0=None, nthreads: int = 0):
-        """Selective scan forward in fp64.  Returns (out, last_state)."""
+                 h0=None, zoh: bool = False, nthreads: int = 0):
+        """Selective scan forward in fp64.  Returns (out, last_state).
+
+        h0: initial state (batch, d_inner, d_state), None for zero.
+        zoh: zero-order-hold input matrix instead of delta*B."""
         u, dt_raw, A, B, C = map(_f64, (u, dt_raw, A, B, C))
         D, z, dt_bias, h0 = map(_f64, (D, z, dt_bias, h0))
         batch, L, d_inner, d_state = _dims(u, B)
@@ -101,7 +104,7 @@ class Oracle:
         rc = self.lib.oracle_scan_fwd(
             _ptr(u), _ptr(dt_raw), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
             _ptr(z), _ptr(dt_bias), _ptr(h0), _ptr(out), _ptr(last), batch,
-            L, d_inner, d_state, int(nthreads))
+            L, d_inner, d_state, int(bool(zoh)), int(nthreads))
         if rc != 0:
             raise ValueError("oracle_scan_fwd rejected its sizes")
         return out, last
@@ -123,7 +126,7 @@ class Oracle:
         return out, last
 
     def state_update(self, state, u, dt_raw, A, B, C, D=None, z=None,
-                     dt_bias=None, nthreads: int = 0):
+                     dt_bias=None, zoh: bool = False, nthreads: int = 0):
         """One decode step in fp64 -> (new_state, out); inputs untouched.
 
         state: (batch, d_inner, d_state); u, dt_raw, z: (batch, d_inner);
@@ -137,7 +140,7 @@ class Oracle:
         rc = self.lib.oracle_state_update(
             _ptr(st), _ptr(u), _ptr(dt_raw), _ptr(A), _ptr(B), _ptr(C),
             _ptr(D), _ptr(z), _ptr(dt_bias), _ptr(out), batch, d_inner,
-            d_state, int(nthreads))
+            d_state, int(bool(zoh)), int(nthreads))
         if rc != 0:
             raise ValueError("oracle_state_update rejected its sizes")
         return st, out

@@ -18,6 +18,12 @@
  *     MambaBlock listing: delta = softplus(.) of the dt projection (whose
  *     Linear carries a bias, here dt_bias), the same scan with
  *     y = einsum('bdn,bn->bd', h, C), then the gate y * silu(z).
+ *   - zero-order hold (the `zoh` flag): "State space models and Mamba",
+ *     section on discretisation (zero-order hold), and "Deep dive into Mamba"
+ *     section 12 (summary of the core formulas) give, with Abar = exp(delta*A),
+ *     Bbar = A^-1 (exp(delta*A) - I) B.  A is diagonal here, so per state
+ *     Bbar_n = (exp(delta*A_n) - 1) / A_n * B_n, which tends to delta*B_n as
+ *     delta*A_n -> 0 (and equals it when A_n = 0).
  *   - Mamba paper-presentation article (hnwysp.cn/news/102080), section 3.2:
  *     h_t = a_t*h_{t-1} + b_t is associative, so the sequence can be cut into
  *     segments, each run serially from a zero state, keeping the segment-end
@@ -26,7 +32,8 @@
  *
  * Readings taken where the pages are silent or disagree (each is listed in
  * the design notes):
- *   - dB = delta*B (the form all listings use), not the zero-order-hold B.
+ *   - dB = delta*B (the form all listings use) unless `zoh` asks for the
+ *     zero-order-hold B above.
  *   - y_t sees u_t: h_t = dA_t*h_{t-1} + dB_t*u_t, y_t = C_t . h_t.
  *   - softplus is applied exactly once, to dt_raw + dt_bias; it is evaluated
  *     exactly (no large-x threshold).
@@ -86,7 +93,7 @@ static void scan_channel(const double* u, const double* dt_raw, const double* A,
                          const double* B, const double* C, const double* D,
                          const double* z, const double* dt_bias, double* out,
                          double* h, int64_t b, int64_t d, int64_t t0, int64_t t1,
-                         int64_t L, int64_t d_inner, int64_t d_state) {
+                         int64_t L, int64_t d_inner, int64_t d_state, int zoh) {
     const double bias = dt_bias ? dt_bias[d] : 0.0;
     const double skip = D ? D[d] : 0.0;
     for (int64_t t = t0; t < t1; ++t) {
@@ -96,8 +103,11 @@ static void scan_channel(const double* u, const double* dt_raw, const double* A,
         const double ut = u[i];
         double y = 0.0;
         for (int64_t n = 0; n < d_state; ++n) {
-            const double dA = exp(delta * A[d * d_state + n]);
-            const double dBu = delta * B[r + n] * ut;
+            const double x = delta * A[d * d_state + n];
+            const double dA = exp(x);
+            /* input gain: delta (Euler) or (exp(x) - 1) / A_n = delta * expm1(x) / x (ZOH) */
+            const double gain = zoh ? (x != 0.0 ? delta * (expm1(x) / x) : delta) : delta;
+            const double dBu = gain * B[r + n] * ut;
             h[n] = dA * h[n] + dBu;
             y += C[r + n] * h[n];
         }
@@ -115,7 +125,7 @@ int oracle_scan_fwd(const double* u, const double* dt_raw, const double* A,
                     const double* B, const double* C, const double* D,
                     const double* z, const double* dt_bias, const double* h0,
                     double* out, double* last_state, int64_t batch, int64_t L,
-                    int64_t d_inner, int64_t d_state, int nthreads) {
+                    int64_t d_inner, int64_t d_state, int zoh, int nthreads) {
     if (batch < 0 || L < 0 || d_inner < 0 || d_state < 1) return -1;
     const int64_t nch = batch * d_inner;
     const int nt = set_threads(nthreads);
@@ -126,7 +136,7 @@ int oracle_scan_fwd(const double* u, const double* dt_raw, const double* A,
         for (int64_t n = 0; n < d_state; ++n)
             h[n] = h0 ? h0[c * d_state + n] : 0.0;
         scan_channel(u, dt_raw, A, B, C, D, z, dt_bias, out, h, b, d, 0, L, L,
-                     d_inner, d_state);
+                     d_inner, d_state, zoh);
         if (last_state)
             memcpy(last_state + c * d_state, h, (size_t)d_state * sizeof(double));
         free(h);
@@ -143,7 +153,7 @@ int oracle_state_update(double* state, const double* u, const double* dt_raw,
                         const double* A, const double* B, const double* C,
                         const double* D, const double* z, const double* dt_bias,
                         double* out, int64_t batch, int64_t d_inner,
-                        int64_t d_state, int nthreads) {
+                        int64_t d_state, int zoh, int nthreads) {
     if (batch < 0 || d_inner < 0 || d_state < 1) return -1;
     const int64_t nch = batch * d_inner;
     const int nt = set_threads(nthreads);
@@ -151,7 +161,7 @@ int oracle_state_update(double* state, const double* u, const double* dt_raw,
     for (int64_t c = 0; c < nch; ++c) {
         const int64_t b = c / d_inner, d = c % d_inner;
         scan_channel(u, dt_raw, A, B, C, D, z, dt_bias, out, state + c * d_state,
-                     b, d, 0, 1, 1, d_inner, d_state);
+                     b, d, 0, 1, 1, d_inner, d_state, zoh);
     }
     return 0;
 }
@@ -166,7 +176,8 @@ int oracle_state_update(double* state, const double* u, const double* dt_raw,
  *      (a1, b1) then (a2, b2)  ->  (a2*a1, a2*b1 + b2), which gives the
  *      state entering every segment;
  *   4. rerun every segment from its entering state to emit the outputs.
- * It must agree with oracle_scan_fwd up to fp64 rounding.
+ * It must agree with oracle_scan_fwd up to fp64 rounding (Euler input
+ * matrix, zero initial state).
  */
 int oracle_scan_fwd_segmented(const double* u, const double* dt_raw,
                               const double* A, const double* B, const double* C,
@@ -210,7 +221,7 @@ int oracle_scan_fwd_segmented(const double* u, const double* dt_raw,
             memcpy(hk, h, (size_t)d_state * sizeof(double));
             /* step 4: rerun the segment from its entering state */
             scan_channel(u, dt_raw, A, B, C, D, z, dt_bias, out, hk, b, d, t0,
-                         t1, L, d_inner, d_state);
+                         t1, L, d_inner, d_state, 0);
             free(hk);
             for (int64_t n = 0; n < d_state; ++n)
                 h[n] = a_seg[k * d_state + n] * h[n] + b_seg[k * d_state + n];

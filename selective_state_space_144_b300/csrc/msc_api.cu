@@ -14,7 +14,6 @@ int64_t g_force_chunks = 0;    // "scan_chunks"
 int64_t g_min_chunk = 512;     // "scan_min_chunk"
 int64_t g_scan_path = 0;       // "scan_path": 0 auto, 1 element-load kernels only
 int64_t g_scan_lanes = 0;      // "scan_lanes": TMA kernels' lanes per channel, 0 auto
-int64_t g_scan_form = 0;       // "scan_kernel": 0 auto, 1 one-warp, 2 warp-specialised
 
 bool aligned(const void* p, size_t a) {
     return (reinterpret_cast<uintptr_t>(p) % a) == 0;
@@ -100,7 +99,7 @@ ScanCheck check_scan(const void* u, const void* dt, const float* A, const void* 
         // fp32 B/C copies unless fp32 inputs already suit 16-byte TMA boxes
         const bool need_bc = dtype == MSC_BF16 || !aligned(B, 16) || !aligned(C, 16);
         r.plan = msc::make_tma_plan(batch, L, d_inner, d_state, sm_count(), g_force_chunks,
-                                    g_min_chunk, need_bc, g_scan_lanes, g_scan_form);
+                                    g_min_chunk, need_bc, g_scan_lanes);
     } else {
         r.plan = msc::make_scan_plan(batch, L, d_inner, d_state, sm_count(), g_force_chunks,
                                      g_min_chunk);
@@ -294,7 +293,7 @@ msc_status msc_selective_scan_workspace_size(int64_t batch, int64_t L, int64_t d
     if (g_scan_path == 0 && msc::tma_scan_supported(d_state, d_inner, dtype, nullptr, nullptr,
                                                     nullptr)) {
         msc::ScanPlan q = msc::make_tma_plan(batch, L, d_inner, d_state, sms, g_force_chunks,
-                                             g_min_chunk, true, g_scan_lanes, g_scan_form);
+                                             g_min_chunk, true, g_scan_lanes);
         need = need > q.ws_bytes ? need : q.ws_bytes;
     }
     *bytes = need;
@@ -342,11 +341,6 @@ msc_status msc_tuning_set(const char* key, int64_t value) {
     if (!key || value < 0) return MSC_ERR_INVALID_ARG;
     if (std::strcmp(key, "scan_chunks") == 0) {
         g_force_chunks = value;
-        return MSC_OK;
-    }
-    if (std::strcmp(key, "scan_kernel") == 0) {
-        if (value > 2) return MSC_ERR_INVALID_ARG;
-        g_scan_form = value;
         return MSC_OK;
     }
     if (std::strcmp(key, "scan_lanes") == 0) {

@@ -34,7 +34,6 @@ struct ScanArgs {
 // How one scan call is cut up.
 struct ScanPlan {
     int tma;           // 1: TMA kernels (8 channels per CTA), 0: element-load kernels
-    int ws;            // TMA output pass: 1 warp-specialised (core + scalar warp), 0 one warp
     int G;             // lanes per channel (element-load kernels: 4 states per lane;
                        // TMA kernels: 2 or 4 lanes, N/G states per lane)
     int K;             // time chunks
@@ -78,7 +77,7 @@ ScanPlan make_scan_plan(int64_t batch, int64_t L, int64_t d_inner, int64_t N,
                         int sm_count, int64_t force_chunks, int64_t min_chunk);
 ScanPlan make_tma_plan(int64_t batch, int64_t L, int64_t d_inner, int64_t N, int sm_count,
                        int64_t force_chunks, int64_t min_chunk, bool need_bc,
-                       int64_t force_lanes, int64_t kernel_form);
+                       int64_t force_lanes);
 
 cudaError_t launch_scan(const ScanArgs& a, const ScanPlan& p, msc_dtype dtype,
                         cudaStream_t stream);

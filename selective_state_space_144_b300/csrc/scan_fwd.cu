@@ -173,11 +173,9 @@ ScanPlan make_scan_plan(int64_t batch, int64_t L, int64_t d_inner, int64_t N,
 static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 ScanPlan make_tma_plan(int64_t batch, int64_t L, int64_t d_inner, int64_t N, int sm_count,
-                       int64_t force_chunks, int64_t min_chunk, bool need_bc, int64_t force_lanes,
-                       int64_t kernel_form) {
+                       int64_t force_chunks, int64_t min_chunk, bool need_bc, int64_t force_lanes) {
     ScanPlan p{};
     p.tma = 1;
-    p.ws = kernel_form == 2 ? 1 : 0;
     const int64_t target = (int64_t)sm_count * 8;  // 2 warps per SM sub-partition
     // 2 lanes per channel (8 states each for N = 16) need half the shared-
     // memory traffic and shuffles per update of 4 lanes; take them when the

@@ -181,7 +181,7 @@ __device__ __forceinline__ void octet_prologue(const unsigned char* stage, int r
     }
 }
 
-template <typename T, int G, int NS, int TT, int S, bool OUTPUT>
+template <typename T, int G, int NS, int TT, int S>
 __global__ void __launch_bounds__(32)
 scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dt,
                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
@@ -209,9 +209,8 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const int64_t tc0 = (int64_t)k * a.chunk;
     const int nsteps = (int)min(a.chunk, a.L - tc0);
     const int ntiles = (nsteps + TT - 1) / TT;
-    const bool has_z = OUTPUT && a.z != nullptr;
-    const uint32_t tx_bytes =
-        (uint32_t)((2 + (has_z ? 1 : 0)) * Lay::kX + (OUTPUT ? 2 : 1) * Lay::kBC);
+    const bool has_z = a.z != nullptr;
+    const uint32_t tx_bytes = (uint32_t)((2 + (has_z ? 1 : 0)) * Lay::kX + 2 * Lay::kBC);
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + Lay::kBar;
@@ -221,8 +220,8 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         prefetch_tensormap(&tm_u);
         prefetch_tensormap(&tm_dt);
         prefetch_tensormap(&tm_B);
+        prefetch_tensormap(&tm_C);
         if (has_z) prefetch_tensormap(&tm_z);
-        if (OUTPUT) prefetch_tensormap(&tm_C);
     }
     __syncwarp();
 
@@ -235,7 +234,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         tma_load_3d(st + Lay::kX, &tm_dt, bar, d0, tt, b);
         if (has_z) tma_load_3d(st + 2 * Lay::kX, &tm_z, bar, d0, tt, b);
         tma_load_3d(st + 3 * Lay::kX, &tm_B, bar, 0, tt, b);
-        if (OUTPUT) tma_load_3d(st + 3 * Lay::kX + Lay::kBC, &tm_C, bar, 0, tt, b);
+        tma_load_3d(st + 3 * Lay::kX + Lay::kBC, &tm_C, bar, 0, tt, b);
     };
     int issued = min(S, ntiles);
     if (lane == 0)
@@ -243,16 +242,15 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 
     // per-channel constants and the starting state
     const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
-    const float Dd = (OUTPUT && a.D) ? __ldg(a.D + d) : 0.0f;
-    u64 A2[NP], hp[NP], Pp[NP];
+    const float Dd = a.D ? __ldg(a.D + d) : 0.0f;
+    u64 A2[NP], hp[NP];
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
         const float* Ar = a.A + d * N + n0 + 2 * i;
         A2[i] = pk2(__ldg(Ar) * kLog2e, __ldg(Ar + 1) * kLog2e);
         hp[i] = pk2(0.0f, 0.0f);
-        Pp[i] = pk2(1.0f, 1.0f);
     }
-    if (OUTPUT && k > 0) {
+    if (k > 0) {
         for (int j2 = 0; j2 < k; ++j2) {
             const int64_t w = ((int64_t)(b * (a.K - 1) + j2) * a.d_inner + d) * N + n0;
 #pragma unroll
@@ -312,7 +310,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 u64 Bp[NP], Cp[NP];
                 if constexpr (NP == 1) {  // 2 states: one 8-byte read each
                     Bp[0] = *reinterpret_cast<const u64*>(sB + j * N);
-                    if (OUTPUT) Cp[0] = *reinterpret_cast<const u64*>(sC + j * N);
+                    Cp[0] = *reinterpret_cast<const u64*>(sC + j * N);
                 } else {                  // 16-byte reads, two pairs each
 #pragma unroll
                     for (int i2 = 0; i2 < NP; i2 += 2) {
@@ -320,12 +318,10 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                             *reinterpret_cast<const ulonglong2*>(sB + j * N + 2 * i2);
                         Bp[i2] = bq.x;
                         Bp[i2 + 1] = bq.y;
-                        if (OUTPUT) {
-                            const ulonglong2 cq =
-                                *reinterpret_cast<const ulonglong2*>(sC + j * N + 2 * i2);
-                            Cp[i2] = cq.x;
-                            Cp[i2 + 1] = cq.y;
-                        }
+                        const ulonglong2 cq =
+                            *reinterpret_cast<const ulonglong2*>(sC + j * N + 2 * i2);
+                        Cp[i2] = cq.x;
+                        Cp[i2 + 1] = cq.y;
                     }
                 }
                 u64 y2 = pk2(0.0f, 0.0f);
@@ -334,10 +330,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                     const u64 x2 = mul2(dl2, A2[i2]);
                     const u64 dA = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
                     hp[i2] = fma2(dA, hp[i2], mul2(du2, Bp[i2]));
-                    if (OUTPUT)
-                        y2 = fma2(Cp[i2], hp[i2], y2);
-                    else
-                        Pp[i2] = mul2(Pp[i2], dA);
+                    y2 = fma2(Cp[i2], hp[i2], y2);
                 }
                 yv[j] = lo2(y2) + hi2(y2);
             }
@@ -361,27 +354,25 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                                                    nsteps, u_nxt);
             }
             // (3) outputs of steps g + G*m of channel ch
-            if (OUTPUT) {
-                float ys[SPL];
-                reduce_scatter<G>(yv, lane, ys);
+            float ys[SPL];
+            reduce_scatter<G>(yv, lane, ys);
 #pragma unroll
-                for (int p = 0; p < PPL; ++p) {
-                    u64 y2 = fma2(D2, u_cur[p], pk2(ys[2 * p], ys[2 * p + 1]));
-                    const int r0 = (kOct * oo + G * (2 * p)) * CPW, r1 = r0 + G * CPW;
-                    if (has_z)
-                        y2 = mul2(y2, silu2(pk2(lds_elem<T>(sz0 + r0), lds_elem<T>(sz0 + r1))));
-                    T* op = out_p + (2 * p) * gstride;
-                    if (FULL) {
-                        Elem<T>::store(op, lo2(y2));
-                        Elem<T>::store(op + gstride, hi2(y2));
-                    } else {
-                        const int s0 = sb + g + G * (2 * p);
-                        if (s0 < nsteps) Elem<T>::store(op, lo2(y2));
-                        if (s0 + G < nsteps) Elem<T>::store(op + gstride, hi2(y2));
-                    }
+            for (int p = 0; p < PPL; ++p) {
+                u64 y2 = fma2(D2, u_cur[p], pk2(ys[2 * p], ys[2 * p + 1]));
+                const int r0 = (kOct * oo + G * (2 * p)) * CPW, r1 = r0 + G * CPW;
+                if (has_z)
+                    y2 = mul2(y2, silu2(pk2(lds_elem<T>(sz0 + r0), lds_elem<T>(sz0 + r1))));
+                T* op = out_p + (2 * p) * gstride;
+                if (FULL) {
+                    Elem<T>::store(op, lo2(y2));
+                    Elem<T>::store(op + gstride, hi2(y2));
+                } else {
+                    const int s0 = sb + g + G * (2 * p);
+                    if (s0 < nsteps) Elem<T>::store(op, lo2(y2));
+                    if (s0 + G < nsteps) Elem<T>::store(op + gstride, hi2(y2));
                 }
-                out_p += kOct * dinner;
             }
+            out_p += kOct * dinner;
             __syncwarp();
 #pragma unroll
             for (int p = 0; p < PPL; ++p) u_cur[p] = u_nxt[p];
@@ -412,273 +403,6 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         return;
     }
 
-    if (OUTPUT) {
-        if (k == a.K - 1 && a.last_state) {
-            float* ls = a.last_state + ((int64_t)b * a.d_inner + d) * N + n0;
-#pragma unroll
-            for (int i = 0; i < NP; ++i)
-                *reinterpret_cast<float2*>(ls + 2 * i) = make_float2(lo2(hp[i]), hi2(hp[i]));
-        }
-    } else {
-        const int64_t w = ((int64_t)(b * (a.K - 1) + k) * a.d_inner + d) * N + n0;
-#pragma unroll
-        for (int i = 0; i < NP; ++i) {
-            *reinterpret_cast<float2*>(a.ws_a + w + 2 * i) = make_float2(lo2(Pp[i]), hi2(Pp[i]));
-            *reinterpret_cast<float2*>(a.ws_b + w + 2 * i) = make_float2(lo2(hp[i]), hi2(hp[i]));
-        }
-    }
-}
-
-// Warp-specialised form of the output pass: a CTA is two warps on the same
-// CPW channels.  Warp 1 (scalar) issues the TMA loads, computes each octet's
-// delta and delta*u one octet ahead of the core (sDU, double buffered) and
-// finishes each octet one octet behind it (D*u, gate, stores, reading the
-// C.h sums from sY, double buffered).  Warp 0 (core) runs only the state
-// updates and the reduce-scatter of C.h.  The hand-offs are mbarriers with
-// 32 arrivals (every lane of the producing warp): du_ready / du_free and
-// y_ready / y_free, one pair per buffer; the TMA stage barriers are shared.
-// All waits are bounded.  Same arithmetic, same result as scan_tma_kernel.
-template <typename T, int G, int NS, int TT, int S>
-struct WsLayout {
-    using Base = TmaLayout<T, G, NS, TT, S>;
-    static constexpr int CPW = Base::CPW;
-    static constexpr int kStage = Base::kStage;
-    static constexpr int kX = Base::kX;
-    static constexpr int kBC = Base::kBC;
-    static constexpr int kDU = S * kStage;                        // float2 [2][CPW][kDUStride]
-    static constexpr int kY = kDU + 2 * CPW * kDUStride * 8;      // float [2][8 steps][CPW]
-    static constexpr int kBar = kY + 2 * kOct * CPW * 4;          // u64 [S + 8]
-    static constexpr int kTotal = kBar + (S + 8) * 8;
-};
-
-template <typename T, int G, int NS, int TT, int S>
-__global__ void __launch_bounds__(64)
-scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dt,
-               const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
-               const __grid_constant__ CUtensorMap tm_C, const ScanArgs a, const int kgrid) {
-    using Lay = WsLayout<T, G, NS, TT, S>;
-    constexpr int CPW = Lay::CPW;
-    constexpr int N = G * NS;
-    constexpr int NP = NS / 2;
-    constexpr int SPL = kOct / G;
-    constexpr int PPL = SPL / 2;
-    extern __shared__ __align__(128) unsigned char smem[];
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int ch = lane % CPW;
-    const int g = lane / CPW;
-    const int n0 = g * NS;
-    int64_t bid = blockIdx.x;
-    const int tile = (int)(bid % a.ntile);
-    bid /= a.ntile;
-    const int k = (int)(bid % kgrid);
-    const int b = (int)(bid / kgrid);
-    const int d0 = tile * CPW;
-    const int64_t d = d0 + ch;
-    const int64_t tc0 = (int64_t)k * a.chunk;
-    const int nsteps = (int)min(a.chunk, a.L - tc0);
-    const int ntiles = (nsteps + TT - 1) / TT;
-    const int noct = (nsteps + kOct - 1) / kOct;
-    const bool has_z = a.z != nullptr;
-    const uint32_t tx_bytes = (uint32_t)((2 + (has_z ? 1 : 0)) * Lay::kX + 2 * Lay::kBC);
-
-    const uint32_t sbase = smem_u32(smem);
-    const uint32_t full0 = sbase + Lay::kBar;          // [S]  TMA stages
-    const uint32_t dur0 = full0 + 8 * S;               // [2]  sDU written
-    const uint32_t duf0 = dur0 + 16;                   // [2]  sDU read
-    const uint32_t yr0 = duf0 + 16;                    // [2]  sY written
-    const uint32_t yf0 = yr0 + 16;                     // [2]  sY read
-    if (threadIdx.x == 0) {
-        for (int s2 = 0; s2 < S; ++s2) mbar_init(full0 + 8 * s2, 1);
-        for (int s2 = 0; s2 < 8; ++s2) mbar_init(dur0 + 8 * s2, 32);
-        fence_mbar_init();
-    }
-    __syncthreads();
-
-    float2* const sDU = reinterpret_cast<float2*>(smem + Lay::kDU);
-    float* const sY = reinterpret_cast<float*>(smem + Lay::kY);
-    auto stage = [&](int i) -> const unsigned char* { return smem + (i % S) * Lay::kStage; };
-    auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
-        return __all_sync(0xffffffffu, mbar_wait(bar, parity, kWaitLimit));
-    };
-    bool ok = true;
-
-    if (warp == 1) {
-        // ---------------- scalar warp: loads, step sizes, outputs ----------
-        if (lane == 0) {
-            prefetch_tensormap(&tm_u);
-            prefetch_tensormap(&tm_dt);
-            prefetch_tensormap(&tm_B);
-            prefetch_tensormap(&tm_C);
-            if (has_z) prefetch_tensormap(&tm_z);
-        }
-        auto issue = [&](int i) {
-            const uint32_t st = sbase + (i % S) * Lay::kStage;
-            const uint32_t bar = full0 + 8 * (i % S);
-            const int32_t tt = (int32_t)(tc0 + (int64_t)i * TT);
-            mbar_expect_tx(bar, tx_bytes);
-            tma_load_3d(st, &tm_u, bar, d0, tt, b);
-            tma_load_3d(st + Lay::kX, &tm_dt, bar, d0, tt, b);
-            if (has_z) tma_load_3d(st + 2 * Lay::kX, &tm_z, bar, d0, tt, b);
-            tma_load_3d(st + 3 * Lay::kX, &tm_B, bar, 0, tt, b);
-            tma_load_3d(st + 3 * Lay::kX + Lay::kBC, &tm_C, bar, 0, tt, b);
-        };
-        int issued = min(S, ntiles);
-        int waited = 0;
-        if (lane == 0)
-            for (int i = 0; i < issued; ++i) issue(i);
-        const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
-        const u64 bias2 = pk2(bias, bias);
-        const float Dd = a.D ? __ldg(a.D + d) : 0.0f;
-        const u64 D2 = pk2(Dd, Dd);
-        const int lane_x = g * CPW + ch;
-        const int64_t dinner = a.d_inner;
-        const int64_t gstride = (int64_t)G * dinner;
-        T* const out0 = static_cast<T*>(a.out) + ((int64_t)b * a.L + tc0 + g) * dinner + d;
-        u64 uc[PPL], un[PPL];  // u of the octet being finished / being prepared
-        for (int o = 0; ok && o <= noct; ++o) {
-            if (o < noct) {  // step sizes of octet o
-                const int i = (kOct * o) / TT;
-                const int row0 = kOct * o - i * TT;
-                if (row0 == 0) {
-                    ok = wait(full0 + 8 * (i % S), (i / S) & 1);
-                    if (!ok) break;
-                    waited = i + 1;
-                }
-                if (o >= 2) {
-                    ok = wait(duf0 + 8 * (o & 1), ((o - 2) >> 1) & 1);
-                    if (!ok) break;
-                }
-                octet_prologue<T, G, TT, true>(stage(i), row0, lane_x,
-                                               sDU + ((o & 1) * CPW + ch) * kDUStride + g, bias2,
-                                               kOct * o + g, nsteps, un);
-                mbar_arrive(dur0 + 8 * (o & 1));
-            }
-            if (o >= 1) {  // outputs of octet q = o - 1
-                const int q = o - 1;
-                const int iq = (kOct * q) / TT;
-                const int rq = kOct * q - iq * TT;
-                ok = wait(yr0 + 8 * (q & 1), (q >> 1) & 1);
-                if (!ok) break;
-                const float* sy = sY + (q & 1) * (kOct * CPW) + g * CPW + ch;
-                float ys[SPL];
-#pragma unroll
-                for (int m = 0; m < SPL; ++m) ys[m] = sy[m * G * CPW];
-                mbar_arrive(yf0 + 8 * (q & 1));
-                const T* sz = reinterpret_cast<const T*>(stage(iq) + 2 * Lay::kX) + lane_x;
-                T* op = out0 + (int64_t)(kOct * q) * dinner;
-#pragma unroll
-                for (int p = 0; p < PPL; ++p) {
-                    u64 y2 = fma2(D2, uc[p], pk2(ys[2 * p], ys[2 * p + 1]));
-                    const int r0 = (rq + G * (2 * p)) * CPW, r1 = r0 + G * CPW;
-                    if (has_z)
-                        y2 = mul2(y2, silu2(pk2(lds_elem<T>(sz + r0), lds_elem<T>(sz + r1))));
-                    const int s0 = kOct * q + g + G * (2 * p);
-                    if (s0 < nsteps) Elem<T>::store(op + (2 * p) * gstride, lo2(y2));
-                    if (s0 + G < nsteps) Elem<T>::store(op + (2 * p + 1) * gstride, hi2(y2));
-                }
-                // the last octet of tile iq is finished by both warps (the core
-                // signalled y_ready after its last read of the tile): refill
-                if (rq + kOct == TT && iq + S < ntiles) {
-                    __syncwarp();
-                    if (lane == 0) {
-                        fence_proxy_async_smem();
-                        issue(iq + S);
-                    }
-                    issued = iq + S + 1;
-                }
-            }
-#pragma unroll
-            for (int p = 0; p < PPL; ++p) uc[p] = un[p];
-        }
-        if (!ok) {
-            if (lane == 0) atomicOr(&g_scan_error, 1u);
-            for (int i = waited; i < issued; ++i)
-                mbar_wait(full0 + 8 * (i % S), (i / S) & 1, kWaitLimit);
-        }
-        return;
-    }
-
-    // -------------------- core warp: state updates --------------------------
-    u64 A2[NP], hp[NP];
-#pragma unroll
-    for (int i = 0; i < NP; ++i) {
-        const float* Ar = a.A + d * N + n0 + 2 * i;
-        A2[i] = pk2(__ldg(Ar) * kLog2e, __ldg(Ar + 1) * kLog2e);
-        hp[i] = pk2(0.0f, 0.0f);
-    }
-    if (k > 0) {
-        for (int j2 = 0; j2 < k; ++j2) {
-            const int64_t w = ((int64_t)(b * (a.K - 1) + j2) * a.d_inner + d) * N + n0;
-#pragma unroll
-            for (int i = 0; i < NP; ++i) {
-                const float2 av = *reinterpret_cast<const float2*>(a.ws_a + w + 2 * i);
-                const float2 bv = *reinterpret_cast<const float2*>(a.ws_b + w + 2 * i);
-                hp[i] = fma2(pk2(av.x, av.y), hp[i], pk2(bv.x, bv.y));
-            }
-        }
-    }
-    for (int o = 0; ok && o < noct; ++o) {
-        const int i = (kOct * o) / TT;
-        const int rb = kOct * o - i * TT;
-        if (rb == 0) {
-            ok = wait(full0 + 8 * (i % S), (i / S) & 1);
-            if (!ok) break;
-        }
-        ok = wait(dur0 + 8 * (o & 1), (o >> 1) & 1);
-        if (!ok) break;
-        const unsigned char* st = stage(i);
-        const float* sB = reinterpret_cast<const float*>(st + 3 * Lay::kX) + rb * N + n0;
-        const float* sC = reinterpret_cast<const float*>(st + 3 * Lay::kX + Lay::kBC) + rb * N + n0;
-        const float4* sd = reinterpret_cast<const float4*>(sDU + ((o & 1) * CPW + ch) * kDUStride);
-        float yv[kOct];
-#pragma unroll
-        for (int j = 0; j < kOct; ++j) {
-            const float4 v2 = sd[j >> 1];
-            const float vdl = (j & 1) ? v2.z : v2.x, vdu = (j & 1) ? v2.w : v2.y;
-            const u64 dl2 = pk2(vdl, vdl), du2 = pk2(vdu, vdu);
-            u64 Bp[NP], Cp[NP];
-            if constexpr (NP == 1) {
-                Bp[0] = *reinterpret_cast<const u64*>(sB + j * N);
-                Cp[0] = *reinterpret_cast<const u64*>(sC + j * N);
-            } else {
-#pragma unroll
-                for (int i2 = 0; i2 < NP; i2 += 2) {
-                    const ulonglong2 bq = *reinterpret_cast<const ulonglong2*>(sB + j * N + 2 * i2);
-                    const ulonglong2 cq = *reinterpret_cast<const ulonglong2*>(sC + j * N + 2 * i2);
-                    Bp[i2] = bq.x;
-                    Bp[i2 + 1] = bq.y;
-                    Cp[i2] = cq.x;
-                    Cp[i2 + 1] = cq.y;
-                }
-            }
-            u64 y2 = pk2(0.0f, 0.0f);
-#pragma unroll
-            for (int i2 = 0; i2 < NP; ++i2) {
-                const u64 x2 = mul2(dl2, A2[i2]);
-                const u64 dA = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
-                hp[i2] = fma2(dA, hp[i2], mul2(du2, Bp[i2]));
-                y2 = fma2(Cp[i2], hp[i2], y2);
-            }
-            yv[j] = lo2(y2) + hi2(y2);
-        }
-        mbar_arrive(duf0 + 8 * (o & 1));  // this octet's sDU is read
-        float ys[SPL];
-        reduce_scatter<G>(yv, lane, ys);
-        if (o >= 2) {
-            ok = wait(yf0 + 8 * (o & 1), ((o - 2) >> 1) & 1);
-            if (!ok) break;
-        }
-        float* sy = sY + (o & 1) * (kOct * CPW) + g * CPW + ch;
-#pragma unroll
-        for (int m = 0; m < SPL; ++m) sy[m * G * CPW] = ys[m];
-        mbar_arrive(yr0 + 8 * (o & 1));
-    }
-    if (!ok) {
-        if (lane == 0) atomicOr(&g_scan_error, 1u);
-        return;
-    }
     if (k == a.K - 1 && a.last_state) {
         float* ls = a.last_state + ((int64_t)b * a.d_inner + d) * N + n0;
 #pragma unroll
@@ -951,19 +675,10 @@ static cudaError_t launch_tma_ns(const ScanArgs& a, const ScanPlan& p, const flo
     }
     const int64_t nb = a.batch * (int64_t)p.K * p.ntile;
     const ProfileMark m = profile_begin(s, MSC_PROF_SCAN);
-    if (p.ws) {
-        using WL = WsLayout<T, G, NS, TT, S>;
-        auto kern = scan_ws_kernel<T, G, NS, TT, S>;
-        const size_t wsmem = WL::kTotal;
-        if (wsmem > 48 * 1024)
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsmem);
-        kern<<<(unsigned)nb, 64, wsmem, s>>>(mu, mdt, mz, mB, mC, a, p.K);
-    } else {
-        auto kern = scan_tma_kernel<T, G, NS, TT, S, true>;
-        if (smem > 48 * 1024)
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<(unsigned)nb, 32, smem, s>>>(mu, mdt, mz, mB, mC, a, p.K);
-    }
+    auto kern = scan_tma_kernel<T, G, NS, TT, S>;
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<(unsigned)nb, 32, smem, s>>>(mu, mdt, mz, mB, mC, a, p.K);
     profile_end(m, s);
     profile_count(p.K > 1 ? 2 : 1);
     return cudaGetLastError();

@@ -19,7 +19,16 @@ different evaluation that the pages or plain mathematics fix:
   * decode steps == scan ("State space models and Mamba", Mamba decoding);
   * the stability bound |h| <= sum |dt B u| when A < 0;
   * a hand-worked example with exactly representable decays
-    (tests/golden/hand_worked_l3_n2.json).
+    (tests/golden/hand_worked_l3_n2.json);
+  * split prefill: a scan over [0, k) whose last state seeds (h0) the scan
+    over [k, L) reproduces the scan over [0, L);
+  * zero-order hold ("State space models and Mamba", discretisation; "Deep
+    dive into Mamba" section 12): with the input held constant over each
+    step, the discrete state equals the continuous system's solution at the
+    step ends -- checked against a fine Runge-Kutta integration of
+    h' = A h + B u and against the closed-form step response
+    h(t) = B (e^(A t) - 1) / A; ZOH reduces to delta*B when A = 0 and as
+    delta -> 0.
 """
 from __future__ import annotations
 
@@ -259,6 +268,104 @@ def check_hand_worked(orc):
     assert np.allclose(last[0, 0], last_ref, rtol=1e-14, atol=1e-15)
 
 
+def check_split_prefill(orc):
+    """Scanning [0, k) and then [k, L) from the first part's last state (the
+    h0 input) gives the outputs and last state of one scan over [0, L)."""
+    L = 90
+    x = _random_case(2, L, 3, 4, seed=17)
+    y0, last0 = orc.scan_fwd(x.u, x.dt_raw, x.A, x.B, x.C, x.D, x.z, x.dt_bias)
+    for k in (1, 37, 89):
+        sl = lambda a, lo, hi: a[:, lo:hi]
+        ya, la = orc.scan_fwd(sl(x.u, 0, k), sl(x.dt_raw, 0, k), x.A, sl(x.B, 0, k),
+                              sl(x.C, 0, k), x.D, sl(x.z, 0, k), x.dt_bias)
+        yb, lb = orc.scan_fwd(sl(x.u, k, L), sl(x.dt_raw, k, L), x.A, sl(x.B, k, L),
+                              sl(x.C, k, L), x.D, sl(x.z, k, L), x.dt_bias, h0=la)
+        assert rel_l2(np.concatenate([ya, yb], axis=1), y0) < 1e-13, k
+        assert rel_l2(lb, last0) < 1e-13, k
+
+
+def _rk4_piecewise(A, B, u, delta, h0, substeps=400):
+    """Integrate h' = A h + B_t u_t (A diagonal, per state) over consecutive
+    intervals of length delta_t with the input held constant on each, by the
+    classical 4-stage Runge-Kutta method; return the state at every interval
+    end.  Shapes: A (N,), B (L, N), u (L,), delta (L,), h0 (N,)."""
+    h = np.array(h0, dtype=np.float64)
+    out = np.zeros((len(u), len(h)))
+    for t in range(len(u)):
+        s = delta[t] / substeps
+        f = lambda y: A * y + B[t] * u[t]
+        for _ in range(substeps):
+            k1 = f(h)
+            k2 = f(h + 0.5 * s * k1)
+            k3 = f(h + 0.5 * s * k2)
+            k4 = f(h + s * k3)
+            h = h + (s / 6.0) * (k1 + 2.0 * k2 + 2.0 * k3 + k4)
+        out[t] = h
+    return out
+
+
+def check_zoh_matches_ode(orc):
+    """Zero-order hold is exact for an input held over each step: the scan's
+    states (and y = C.h + D u) match a fine RK4 integration of the continuous
+    system, with step sizes up to ~2, both signs of A and a state with A = 0."""
+    rng = np.random.default_rng(18)
+    batch, L, d_inner, N = 1, 10, 2, 4
+    u = rng.standard_normal((batch, L, d_inner))
+    dt_raw = rng.normal(0.0, 1.0, (batch, L, d_inner))
+    A = np.array([[-1.7, -0.4, 0.0, 0.3], [-3.0, -1.0, -0.05, 0.6]])
+    B = rng.standard_normal((batch, L, N))
+    C = rng.standard_normal((batch, L, N))
+    Dv = np.array([0.5, -1.25])
+    y, last = orc.scan_fwd(u, dt_raw, A, B, C, Dv, None, None, zoh=True)
+    delta = _softplus_np(dt_raw)
+    for d in range(d_inner):
+        hs = _rk4_piecewise(A[d], B[0], u[0, :, d], delta[0, :, d], np.zeros(N))
+        y_ref = np.sum(C[0] * hs, axis=1) + Dv[d] * u[0, :, d]
+        assert rel_l2(y[0, :, d], y_ref) < 1e-10, (d, rel_l2(y[0, :, d], y_ref))
+        assert rel_l2(last[0, d], hs[-1]) < 1e-10
+    # and it is not the Euler input matrix at these step sizes
+    ye, _ = orc.scan_fwd(u, dt_raw, A, B, C, Dv, None, None)
+    assert rel_l2(ye, y) > 1e-2
+
+
+def check_zoh_step_response(orc):
+    """u = B = C = 1, N = 1, constant step size: the state after t+1 steps
+    is the continuous step response (e^(A (t+1) delta) - 1) / A."""
+    batch, L, d_inner = 1, 30, 3
+    A = np.array([[-0.9], [-4.0], [0.2]])
+    raw = np.array([0.4, -0.8, 1.3])
+    u = np.ones((batch, L, d_inner))
+    dt_raw = np.broadcast_to(raw, (batch, L, d_inner)).copy()
+    ones = np.ones((batch, L, 1))
+    y, last = orc.scan_fwd(u, dt_raw, A, ones, ones, None, None, None, zoh=True)
+    dt = _softplus_np(raw)
+    tt = (np.arange(L, dtype=np.float64)[:, None] + 1.0) * dt
+    h = np.expm1(A[:, 0] * tt) / A[:, 0]
+    assert rel_l2(y[0], h) < 1e-13, rel_l2(y[0], h)
+    assert rel_l2(last[0, :, 0], h[-1]) < 1e-13
+
+
+def check_zoh_limits(orc):
+    """ZOH equals the Euler input matrix delta*B exactly when A = 0, to fp64
+    rounding as delta -> 0; and its decode steps reproduce its scan."""
+    x = _random_case(2, 20, 3, 4, seed=19)
+    A0 = np.zeros_like(x.A)
+    ye, le = orc.scan_fwd(x.u, x.dt_raw, A0, x.B, x.C, x.D, x.z, x.dt_bias)
+    yz, lz = orc.scan_fwd(x.u, x.dt_raw, A0, x.B, x.C, x.D, x.z, x.dt_bias, zoh=True)
+    assert np.array_equal(ye, yz) and np.array_equal(le, lz)
+    small = np.full_like(x.dt_raw, -30.0)
+    ye, le = orc.scan_fwd(x.u, small, x.A, x.B, x.C, x.D, x.z, None)
+    yz, lz = orc.scan_fwd(x.u, small, x.A, x.B, x.C, x.D, x.z, None, zoh=True)
+    assert rel_l2(lz, le) < 1e-12 and rel_l2(yz, ye) < 1e-14
+    y, last = orc.scan_fwd(x.u, x.dt_raw, x.A, x.B, x.C, x.D, x.z, x.dt_bias, zoh=True)
+    st = np.zeros_like(last)
+    for t in range(x.u.shape[1]):
+        st, o = orc.state_update(st, x.u[:, t], x.dt_raw[:, t], x.A, x.B[:, t],
+                                 x.C[:, t], x.D, x.z[:, t], x.dt_bias, zoh=True)
+        assert np.array_equal(o, y[:, t]), t
+    assert np.array_equal(st, last)
+
+
 ALL_CHECKS = [
     check_softplus,
     check_silu,
@@ -270,4 +377,8 @@ ALL_CHECKS = [
     check_decode_equals_scan,
     check_stability_bound,
     check_hand_worked,
+    check_split_prefill,
+    check_zoh_matches_ode,
+    check_zoh_step_response,
+    check_zoh_limits,
 ]

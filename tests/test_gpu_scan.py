@@ -23,7 +23,6 @@ def _defaults():
     msc.tuning_set("scan_min_chunk", 512)
     msc.tuning_set("scan_path", 0)
     msc.tuning_set("scan_lanes", 0)
-    msc.tuning_set("scan_kernel", 0)
 
 
 @pytest.fixture(autouse=True)
@@ -39,14 +38,11 @@ def _reset_tuning():
 PATHS = [0, 1]
 # lanes per channel of the TMA kernels: 4 (N/4 states each) or 2 (N/2 each)
 LANES = [4, 2]
-# TMA output kernel: 1 one warp per CTA, 2 warp-specialised (core + scalar warp)
-FORMS = [1, 2]
 
 
-def run_gpu(x, chunks=0, with_last=True, path=0, lanes=0, form=0):
+def run_gpu(x, chunks=0, with_last=True, path=0, lanes=0):
     msc.tuning_set("scan_path", path)
     msc.tuning_set("scan_lanes", lanes)
-    msc.tuning_set("scan_kernel", form)
     if chunks:
         msc.tuning_set("scan_chunks", chunks)
     a = scan_device_args(x)
@@ -62,8 +58,8 @@ def run_gpu(x, chunks=0, with_last=True, path=0, lanes=0, form=0):
     return from_device(out), (from_device(last) if with_last else None)
 
 
-def check(x, chunks=0, with_last=True, path=0, lanes=0, form=0):
-    y, last = run_gpu(x, chunks, with_last, path, lanes, form)
+def check(x, chunks=0, with_last=True, path=0, lanes=0):
+    y, last = run_gpu(x, chunks, with_last, path, lanes)
     y_ref, last_ref = oracle.scan_fwd(x.u, x.dt_raw, x.A, x.B, x.C, x.D, x.z,
                                       x.dt_bias)
     tol = TOL[x.dtype]
@@ -249,50 +245,6 @@ def test_paths_agree():
     y2, l2 = run_gpu(x, chunks=2, path=0, lanes=2)
     assert rel_l2(y0, y1) <= 1e-6 and rel_l2(l0, l1) <= 1e-6
     assert rel_l2(y2, y1) <= 1e-6 and rel_l2(l2, l1) <= 1e-6
-
-
-# ---- the warp-specialised output kernel -----------------------------------
-@pytest.mark.parametrize("lanes", LANES)
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("d_state", [8, 16, 32, 64])
-def test_ws_state_sizes(dtype, d_state, lanes):
-    x = synth.scan_inputs(2, 333, 96, d_state, dtype=dtype,
-                          seed=300 + d_state, D="normal", A_kind="random")
-    check(x, form=2, lanes=lanes)
-    check(x, chunks=3, form=2, lanes=lanes)
-
-
-@pytest.mark.parametrize("lanes", LANES)
-@pytest.mark.parametrize("L", [1, 7, 8, 9, 31, 32, 33, 64, 65, 129])
-def test_ws_short_sequences(L, lanes):
-    """One octet, a ragged octet, exactly one and two tiles, ragged tiles:
-    the hand-offs between the two warps at every boundary."""
-    x = synth.scan_inputs(2, L, 48, 16, dtype="bf16", seed=400 + L)
-    check(x, form=2, lanes=lanes)
-    check(x, chunks=L, form=2, lanes=lanes)
-
-
-@pytest.mark.parametrize("drop", ["z", "D", "dt_bias", "all"])
-def test_ws_optional_inputs_absent(drop):
-    x = synth.scan_inputs(2, 150, 64, 16, dtype="f32", seed=33,
-                          with_z=drop not in ("z", "all"),
-                          with_D=drop not in ("D", "all"),
-                          with_bias=drop not in ("dt_bias", "all"))
-    check(x, form=2)
-    check(x, form=2, with_last=False)
-
-
-@pytest.mark.parametrize("lanes", LANES)
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("chunks", [1, 4, 64])
-def test_ws_equals_one_warp_bitwise(dtype, chunks, lanes):
-    """Both kernel forms evaluate the same operations in the same order on
-    each value, so their outputs and last states agree bit for bit."""
-    x = synth.scan_inputs(3, 517, 208, 16, dtype=dtype, seed=60 + chunks,
-                          D="normal")
-    y1, l1 = run_gpu(x, chunks=chunks, lanes=lanes, form=1)
-    y2, l2 = run_gpu(x, chunks=chunks, lanes=lanes, form=2)
-    assert np.array_equal(y1, y2) and np.array_equal(l1, l2)
 
 
 # ---- the workloads at reduced size (several tiles, ragged tails) ---------

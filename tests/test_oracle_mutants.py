@@ -14,11 +14,9 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 # (name, text in oracle.c, replacement).  Only the first occurrence is edited.
 MUTANTS = [
     ("dropped_decay", "h[n] = dA * h[n] + dBu;", "h[n] = h[n] + dBu;"),
-    ("decay_sign", "const double dA = exp(delta * A[d * d_state + n]);",
-     "const double dA = exp(-delta * A[d * d_state + n]);"),
+    ("decay_sign", "const double dA = exp(x);", "const double dA = exp(-x);"),
     ("C_for_B_in_output", "y += C[r + n] * h[n];", "y += B[r + n] * h[n];"),
-    ("dropped_delta_in_input", "const double dBu = delta * B[r + n] * ut;",
-     "const double dBu = B[r + n] * ut;"),
+    ("dropped_delta_in_input", ": delta) : delta;", ": delta) : 1.0;"),
     ("dropped_skip", "y += skip * ut;", ";"),
     ("gate_without_sigmoid", "if (z) y *= oracle_silu(z[i]);",
      "if (z) y *= z[i];"),
@@ -26,8 +24,7 @@ MUTANTS = [
     ("softplus_as_exp", "return log1p(exp(x));", "return exp(x);"),
     ("softplus_pos_branch", "if (x > 0.0) return x + log1p(exp(-x));",
      "if (x > 0.0) return log1p(exp(-x));"),
-    ("A_transposed", "exp(delta * A[d * d_state + n])",
-     "exp(delta * A[n * d_inner + d])"),
+    ("A_transposed", "delta * A[d * d_state + n];", "delta * A[n * d_inner + d];"),
     ("BC_ignore_batch", "const int64_t r = (b * L + t) * d_state;",
      "const int64_t r = t * d_state;"),
     ("dropped_bias", "oracle_softplus(dt_raw[i] + bias)",
@@ -43,6 +40,15 @@ MUTANTS = [
     ("segment_merge_no_decay",
      "h[n] = a_seg[k * d_state + n] * h[n] + b_seg[k * d_state + n];",
      "h[n] = h[n] + b_seg[k * d_state + n];"),
+    ("zoh_ignored", "const double gain = zoh ?", "const double gain = 0 ?"),
+    ("zoh_exp_for_expm1", "delta * (expm1(x) / x)", "delta * (exp(x) / x)"),
+    ("zoh_gain_without_delta", "delta * (expm1(x) / x)", "(expm1(x) / x)"),
+    ("zoh_zero_limit", "(x != 0.0 ? delta * (expm1(x) / x) : delta)",
+     "(x != 0.0 ? delta * (expm1(x) / x) : 0.0)"),
+    ("zoh_on_decay_too", "const double dA = exp(x);",
+     "const double dA = zoh ? expm1(x) : exp(x);"),
+    ("decode_ignores_zoh", "b, d, 0, 1, 1, d_inner, d_state, zoh);",
+     "b, d, 0, 1, 1, d_inner, d_state, 0);"),
     ("segment_rerun_from_zero", "memcpy(hk, h, (size_t)d_state * sizeof(double));",
      "memset(hk, 0, (size_t)d_state * sizeof(double));"),
 ]
