@@ -21,6 +21,15 @@
  *     constant memory per token), reading and writing the fp32 state in
  *     place.
  *
+ *   The _ex forms add an initial state h0 (split prefill: a long prompt
+ *   scanned in pieces, each seeded with the previous piece's last_state)
+ *   and a choice of discretisation of B: delta*B as above (the form every
+ *   listing on the pages uses), or the zero-order hold that the formulas of
+ *   "State space models and Mamba" (section on discretisation) and "Deep
+ *   dive into Mamba" (section 12) give, Bbar = A^-1 (exp(delta*A) - I) B,
+ *   i.e. per state (exp(delta*A[d,n]) - 1) / A[d,n] * B[b,t,n] (delta*B
+ *   where A[d,n] = 0).
+ *
  * Conventions shared by every entry point:
  *   - All tensor pointers are DEVICE pointers to contiguous row-major arrays.
  *     The caller owns every buffer; the library never frees caller memory.
@@ -142,6 +151,32 @@ msc_status msc_selective_scan_fwd_noalloc(
     void* out, float* last_state, int64_t batch, int64_t L, int64_t d_inner,
     int64_t d_state, msc_dtype dtype, msc_stream_t stream);
 
+/* Discretisation of the input matrix B (the _ex entry points). */
+typedef enum msc_discretization {
+    MSC_DISC_EULER = 0,  /* delta * B                                    */
+    MSC_DISC_ZOH = 1     /* (exp(delta*A) - 1) / A * B  (zero-order hold) */
+} msc_discretization;
+
+/*
+ * The scan of msc_selective_scan_fwd with two additions:
+ *   h0   : (batch, d_inner, d_state) fp32, the state before t = 0.
+ *          Nullable: zero.  Must not overlap last_state or out (every time
+ *          chunk of the plan reads it).  With L == 0, last_state = h0.
+ *   disc : MSC_DISC_EULER or MSC_DISC_ZOH; anything else is
+ *          MSC_ERR_INVALID_ARG.
+ * workspace: NULL takes the scratch stream-ordered as msc_selective_scan_fwd
+ * does; otherwise as msc_selective_scan_fwd_ws (size from
+ * msc_selective_scan_workspace_size, which does not depend on h0 or disc).
+ * Other arguments, layouts and errors as msc_selective_scan_fwd.
+ */
+msc_status msc_selective_scan_fwd_ex(
+    const void* u, const void* dt, const float* A, const void* B,
+    const void* C, const float* D, const void* z, const float* dt_bias,
+    const float* h0, void* out, float* last_state, int64_t batch, int64_t L,
+    int64_t d_inner, int64_t d_state, msc_dtype dtype,
+    msc_discretization disc, void* workspace, size_t workspace_bytes,
+    msc_stream_t stream);
+
 /*
  * Single-token selective state update (decode).
  *   state         : (batch, d_inner, d_state) fp32, read and written in place
@@ -156,6 +191,18 @@ msc_status msc_selective_state_update(
     const void* B, const void* C, const float* D, const void* z,
     const float* dt_bias, void* out, int64_t batch, int64_t d_inner,
     int64_t d_state, msc_dtype dtype, msc_stream_t stream);
+
+/*
+ * msc_selective_state_update with a choice of discretisation (`disc` as in
+ * msc_selective_scan_fwd_ex); a ZOH scan's last_state continues with ZOH
+ * decode steps.  Same arguments and errors otherwise.
+ */
+msc_status msc_selective_state_update_ex(
+    float* state, const void* u, const void* dt, const float* A,
+    const void* B, const void* C, const float* D, const void* z,
+    const float* dt_bias, void* out, int64_t batch, int64_t d_inner,
+    int64_t d_state, msc_dtype dtype, msc_discretization disc,
+    msc_stream_t stream);
 
 /*
  * Kernels never spin without bound: every wait for an asynchronous copy

@@ -31,11 +31,13 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIBNAME = "libmsc.so"
 
 MSC_F32, MSC_BF16 = 0, 1
+MSC_DISC_EULER, MSC_DISC_ZOH = 0, 1
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported size",
            3: "pointer not aligned to its element size",
            4: "CUDA runtime error",
            5: "workspace missing, too small or misaligned",
-           6: "a kernel's bounded wait for a data copy gave up"}
+           6: "a kernel's bounded wait for a data copy gave up",
+           7: "scratch need exceeds the allocation-free entry point's buffer"}
 
 
 class MscError(RuntimeError):
@@ -73,6 +75,11 @@ def load():
     lib.msc_selective_scan_fwd_ws.restype = st
     lib.msc_selective_scan_fwd_ws.argtypes = ([vp] * 10 + [i64] * 4
                                               + [st, vp, sz, vp])
+    lib.msc_selective_scan_fwd_ex.restype = st
+    lib.msc_selective_scan_fwd_ex.argtypes = ([vp] * 11 + [i64] * 4
+                                              + [st, st, vp, ctypes.c_size_t, vp])
+    lib.msc_selective_state_update_ex.restype = st
+    lib.msc_selective_state_update_ex.argtypes = [vp] * 10 + [i64] * 3 + [st, st, vp]
     lib.msc_selective_scan_workspace_size.restype = st
     lib.msc_selective_scan_workspace_size.argtypes = [i64] * 4 + [
         st, ctypes.POINTER(sz)]
@@ -171,14 +178,37 @@ def _scan_args(u, dt, A, B, C, D, z, dt_bias, out, last_state,
     return p, out, last_state, (batch, L, d_inner, d_state), code, dev
 
 
+def _scan_ex(fn, u, dt, A, B, C, D, z, dt_bias, out, last_state,
+             return_last_state, h0, zoh, workspace):
+    lib = load()
+    p, out, last_state, dims, code, dev = _scan_args(
+        u, dt, A, B, C, D, z, dt_bias, out, last_state, return_last_state)
+    batch, _, d_inner, d_state = dims
+    h0p = _ptr(h0, "h0", _torch().float32, (batch, d_inner, d_state), dev)
+    wp = _ptr(workspace, "workspace", None, None, dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.msc_selective_scan_fwd_ex(
+        p["u"], p["dt"], p["A"], p["B"], p["C"], p["D"], p["z"],
+        p["dt_bias"], h0p, p["out"], p["last_state"], *dims, code,
+        MSC_DISC_ZOH if zoh else MSC_DISC_EULER, wp, wbytes, _stream(dev))
+    _check(fn, st)
+    return out, last_state
+
+
 def selective_scan_fwd(u, dt, A, B, C, D=None, z=None, dt_bias=None,
-                       out=None, last_state=None, return_last_state=True):
+                       out=None, last_state=None, return_last_state=True,
+                       h0=None, zoh=False):
     """Selective scan forward on the GPU -> (out, last_state).
 
     Enqueued on the current CUDA stream of u's device; returns at once.
     Scratch for the inter-chunk carry (when needed) is taken stream-ordered
-    by the library.
+    by the library.  h0: initial state (batch, d_inner, d_state) fp32, None
+    for zero; zoh: zero-order-hold input matrix instead of delta*B.
     """
+    if h0 is not None or zoh:
+        return _scan_ex("msc_selective_scan_fwd_ex", u, dt, A, B, C, D, z,
+                        dt_bias, out, last_state, return_last_state, h0, zoh,
+                        None)
     lib = load()
     p, out, last_state, dims, code, dev = _scan_args(
         u, dt, A, B, C, D, z, dt_bias, out, last_state, return_last_state)
@@ -202,8 +232,15 @@ def scan_workspace_size(batch, L, d_inner, d_state, dtype) -> int:
 
 def selective_scan_fwd_ws(u, dt, A, B, C, D=None, z=None, dt_bias=None,
                           out=None, last_state=None, workspace=None,
-                          return_last_state=True):
+                          return_last_state=True, h0=None, zoh=False):
     """As selective_scan_fwd with a caller-owned uint8 CUDA workspace."""
+    if h0 is not None or zoh:
+        if workspace is None and scan_workspace_size(
+                u.shape[0], u.shape[1], u.shape[2], B.shape[-1], u.dtype) > 0:
+            raise MscError("msc_selective_scan_fwd_ex", 5)
+        return _scan_ex("msc_selective_scan_fwd_ex", u, dt, A, B, C, D, z,
+                        dt_bias, out, last_state, return_last_state, h0, zoh,
+                        workspace)
     lib = load()
     p, out, last_state, dims, code, dev = _scan_args(
         u, dt, A, B, C, D, z, dt_bias, out, last_state, return_last_state)
@@ -218,8 +255,9 @@ def selective_scan_fwd_ws(u, dt, A, B, C, D=None, z=None, dt_bias=None,
 
 
 def selective_state_update(state, u, dt, A, B, C, D=None, z=None,
-                           dt_bias=None, out=None):
-    """One decode step on the GPU; updates ``state`` in place -> out."""
+                           dt_bias=None, out=None, zoh=False):
+    """One decode step on the GPU; updates ``state`` in place -> out.
+    zoh: zero-order-hold input matrix instead of delta*B."""
     torch = _torch()
     lib = load()
     if state.dim() != 3:
@@ -231,7 +269,9 @@ def selective_state_update(state, u, dt, A, B, C, D=None, z=None,
     f32 = torch.float32
     if out is None:
         out = torch.empty((batch, d_inner), dtype=sdt, device=dev)
-    st = lib.msc_selective_state_update(
+    fn = "msc_selective_state_update_ex" if zoh else "msc_selective_state_update"
+    extra = (MSC_DISC_ZOH,) if zoh else ()
+    st = getattr(lib, fn)(
         _ptr(state, "state", f32, (batch, d_inner, d_state), dev),
         _ptr(u, "u", sdt, (batch, d_inner), dev),
         _ptr(dt, "dt", sdt, (batch, d_inner), dev),
@@ -242,8 +282,8 @@ def selective_state_update(state, u, dt, A, B, C, D=None, z=None,
         _ptr(z, "z", sdt, (batch, d_inner), dev),
         _ptr(dt_bias, "dt_bias", f32, (d_inner,), dev),
         _ptr(out, "out", sdt, (batch, d_inner), dev),
-        batch, d_inner, d_state, code, _stream(dev))
-    _check("msc_selective_state_update", st)
+        batch, d_inner, d_state, code, *extra, _stream(dev))
+    _check(fn, st)
     return out
 
 

@@ -51,7 +51,8 @@ struct ScanCheck {
 ScanCheck check_scan(const void* u, const void* dt, const float* A, const void* B,
                      const void* C, const float* D, const void* z, const float* dt_bias,
                      void* out, float* last_state, int64_t batch, int64_t L,
-                     int64_t d_inner, int64_t d_state, msc_dtype dtype) {
+                     int64_t d_inner, int64_t d_state, msc_dtype dtype,
+                     const float* h0 = nullptr) {
     ScanCheck r{};
     r.st = MSC_OK;
     if (dtype != MSC_F32 && dtype != MSC_BF16) {
@@ -89,7 +90,7 @@ ScanCheck check_scan(const void* u, const void* dt, const float* A, const void* 
             r.st = MSC_ERR_ALIGNMENT;
             return r;
         }
-    const void* f32[] = {A, D, dt_bias, last_state};
+    const void* f32[] = {A, D, dt_bias, last_state, h0};
     for (const void* p : f32)
         if (p && !aligned(p, 4)) {
             r.st = MSC_ERR_ALIGNMENT;
@@ -165,9 +166,10 @@ static msc_status run_scan(const void* u, const void* dt, const float* A, const 
                            const void* C, const float* D, const void* z,
                            const float* dt_bias, void* out, float* last_state, int64_t batch,
                            int64_t L, int64_t d_inner, int64_t d_state, msc_dtype dtype,
-                           void* ws, size_t ws_bytes, bool own_ws, msc_stream_t stream) {
+                           void* ws, size_t ws_bytes, bool own_ws, msc_stream_t stream,
+                           const float* h0 = nullptr, int zoh = 0) {
     ScanCheck c = check_scan(u, dt, A, B, C, D, z, dt_bias, out, last_state, batch, L, d_inner,
-                             d_state, dtype);
+                             d_state, dtype, h0);
     if (c.st != MSC_OK) return c.st;
     if (batch == 0 || d_inner == 0) return MSC_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -182,7 +184,7 @@ static msc_status run_scan(const void* u, const void* dt, const float* A, const 
     }
     msc::ScanArgs a{};
     a.u = u; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.dt_bias = dt_bias;
-    a.out = out; a.last_state = last_state;
+    a.out = out; a.last_state = last_state; a.h0 = h0; a.zoh = zoh;
     const size_t half = c.plan.ws_carry / 2 / sizeof(float);
     a.ws_a = c.plan.ws_carry ? static_cast<float*>(w) : nullptr;
     a.ws_b = c.plan.ws_carry ? static_cast<float*>(w) + half : nullptr;
@@ -272,6 +274,19 @@ msc_status msc_selective_scan_fwd_ws(const void* u, const void* dt, const float*
                     dtype, workspace, workspace_bytes, false, stream);
 }
 
+msc_status msc_selective_scan_fwd_ex(const void* u, const void* dt, const float* A,
+                                     const void* B, const void* C, const float* D,
+                                     const void* z, const float* dt_bias, const float* h0,
+                                     void* out, float* last_state, int64_t batch, int64_t L,
+                                     int64_t d_inner, int64_t d_state, msc_dtype dtype,
+                                     msc_discretization disc, void* workspace,
+                                     size_t workspace_bytes, msc_stream_t stream) {
+    if (disc != MSC_DISC_EULER && disc != MSC_DISC_ZOH) return MSC_ERR_INVALID_ARG;
+    return run_scan(u, dt, A, B, C, D, z, dt_bias, out, last_state, batch, L, d_inner, d_state,
+                    dtype, workspace, workspace_bytes, workspace == nullptr, stream, h0,
+                    disc == MSC_DISC_ZOH ? 1 : 0);
+}
+
 msc_status msc_selective_scan_workspace_size(int64_t batch, int64_t L, int64_t d_inner,
                                              int64_t d_state, msc_dtype dtype, size_t* bytes) {
     if (!bytes) return MSC_ERR_INVALID_ARG;
@@ -300,11 +315,10 @@ msc_status msc_selective_scan_workspace_size(int64_t batch, int64_t L, int64_t d
     return MSC_OK;
 }
 
-msc_status msc_selective_state_update(float* state, const void* u, const void* dt,
-                                      const float* A, const void* B, const void* C,
-                                      const float* D, const void* z, const float* dt_bias,
-                                      void* out, int64_t batch, int64_t d_inner,
-                                      int64_t d_state, msc_dtype dtype, msc_stream_t stream) {
+static msc_status run_update(float* state, const void* u, const void* dt, const float* A,
+                             const void* B, const void* C, const float* D, const void* z,
+                             const float* dt_bias, void* out, int64_t batch, int64_t d_inner,
+                             int64_t d_state, msc_dtype dtype, int zoh, msc_stream_t stream) {
     if (dtype != MSC_F32 && dtype != MSC_BF16) return MSC_ERR_INVALID_ARG;
     if (batch < 0 || d_inner < 0 || d_state < 0) return MSC_ERR_INVALID_ARG;
     if (d_state < 1 || d_state > 64) return MSC_ERR_UNSUPPORTED;
@@ -329,12 +343,33 @@ msc_status msc_selective_state_update(float* state, const void* u, const void* d
     a.state = state; a.u = u; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
     a.dt_bias = dt_bias; a.out = out; a.batch = batch; a.d_inner = d_inner; a.N = d_state;
     a.vec = (d_state % 4 == 0) && aligned(state, 16) && aligned(B, 4 * es) && aligned(C, 4 * es);
+    a.zoh = zoh;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     msc::ProfileMark m = msc::profile_begin(s, MSC_PROF_UPDATE);
     cudaError_t e = msc::launch_state_update(a, dtype, s);
     msc::profile_end(m, s);
     msc::profile_count(1);
     return e == cudaSuccess ? MSC_OK : MSC_ERR_CUDA;
+}
+
+msc_status msc_selective_state_update(float* state, const void* u, const void* dt,
+                                      const float* A, const void* B, const void* C,
+                                      const float* D, const void* z, const float* dt_bias,
+                                      void* out, int64_t batch, int64_t d_inner,
+                                      int64_t d_state, msc_dtype dtype, msc_stream_t stream) {
+    return run_update(state, u, dt, A, B, C, D, z, dt_bias, out, batch, d_inner, d_state, dtype,
+                      0, stream);
+}
+
+msc_status msc_selective_state_update_ex(float* state, const void* u, const void* dt,
+                                         const float* A, const void* B, const void* C,
+                                         const float* D, const void* z, const float* dt_bias,
+                                         void* out, int64_t batch, int64_t d_inner,
+                                         int64_t d_state, msc_dtype dtype,
+                                         msc_discretization disc, msc_stream_t stream) {
+    if (disc != MSC_DISC_EULER && disc != MSC_DISC_ZOH) return MSC_ERR_INVALID_ARG;
+    return run_update(state, u, dt, A, B, C, D, z, dt_bias, out, batch, d_inner, d_state, dtype,
+                      disc == MSC_DISC_ZOH ? 1 : 0, stream);
 }
 
 msc_status msc_tuning_set(const char* key, int64_t value) {

@@ -22,6 +22,8 @@ struct ScanArgs {
     const float* dt_bias;
     void* out;
     float* last_state;
+    const float* h0;   // initial state (batch, d_inner, N) or nullptr for zero
+    int zoh;           // 1: zero-order-hold input matrix, 0: delta*B
     float* ws_a;       // chunk transfer coefficients, (batch, K-1, d_inner, N)
     float* ws_b;       // chunk end states from zero,   (batch, K-1, d_inner, N)
     int64_t batch, L, d_inner, N;
@@ -57,6 +59,7 @@ struct UpdateArgs {
     void* out;
     int64_t batch, d_inner, N;
     int vec;           // 1: state and B/C rows can be read 4 elements at a time
+    int zoh;           // 1: zero-order-hold input matrix, 0: delta*B
 };
 
 // Measurement hook (msc_api.cu): while enabled, launchers count kernels and

@@ -5,7 +5,8 @@
 // bias from the MambaBlock of "State space models and Mamba"):
 //     delta = softplus(dt + dt_bias);  h = exp(delta*A) * h + delta*B*u
 //     y = C . h + D*u;  out = y * silu(z)
-// fused in one pass per time chunk: nothing of size (batch, L, d_inner, N)
+// (optionally with the zero-order-hold input matrix in place of delta*B, and
+// an initial state h0 in place of zero) fused in one pass per time chunk: nothing of size (batch, L, d_inner, N)
 // ever exists in memory; the state lives in registers.
 //
 // Work split.  A thread owns one channel d and 4 consecutive states of it;
@@ -46,12 +47,15 @@ scan_chunk_kernel(ScanArgs a, int kgrid) {
     const int64_t t0 = (int64_t)k * a.chunk;
     const int64_t t1 = min(t0 + a.chunk, a.L);
 
-    float A2[4], h[4], P[4];
+    float A2[4], iA[4], h[4], P[4];
+    const float* h0 = OUTPUT ? a.h0 : nullptr;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int n = n0 + j;
-        A2[j] = (n < N) ? __ldg(a.A + d * N + n) * kLog2e : 0.0f;
-        h[j] = 0.0f;
+        const float Av = (n < N) ? __ldg(a.A + d * N + n) : 0.0f;
+        A2[j] = Av * kLog2e;
+        iA[j] = a.zoh ? 1.0f / Av : 0.0f;
+        h[j] = (h0 && n < N) ? h0[(b * a.d_inner + d) * N + n] : 0.0f;
         P[j] = 1.0f;
     }
     if (OUTPUT && k > 0) {
@@ -91,8 +95,11 @@ scan_chunk_kernel(ScanArgs a, int kgrid) {
             float y = 0.0f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float dA = ex2(delta * A2[j]);
-                h[j] = fmaf(dA, h[j], du * Bv[j]);
+                const float x2 = delta * A2[j];
+                const float dA = ex2(x2);
+                const float inj = a.zoh ? zoh_gain(x2, dA, delta, iA[j]) * uu * Bv[j]
+                                        : du * Bv[j];
+                h[j] = fmaf(dA, h[j], inj);
                 y = fmaf(Cv[j], h[j], y);
             }
 #pragma unroll
@@ -106,8 +113,11 @@ scan_chunk_kernel(ScanArgs a, int kgrid) {
         } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float dA = ex2(delta * A2[j]);
-                h[j] = fmaf(dA, h[j], du * Bv[j]);
+                const float x2 = delta * A2[j];
+                const float dA = ex2(x2);
+                const float inj = a.zoh ? zoh_gain(x2, dA, delta, iA[j]) * uu * Bv[j]
+                                        : du * Bv[j];
+                h[j] = fmaf(dA, h[j], inj);
                 P[j] *= dA;
             }
         }

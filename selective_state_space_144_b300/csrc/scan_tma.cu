@@ -6,6 +6,9 @@
 // bias from the MambaBlock of "State space models and Mamba"):
 //     delta = softplus(dt + dt_bias);  h = exp(delta*A) * h + delta*B*u
 //     y = C . h + D*u;  out = y * silu(z)
+// optionally with the zero-order-hold input matrix (exp(delta*A) - 1)/A * B
+// in place of delta*B ("State space models and Mamba", discretisation) and
+// an initial state h0 in place of zero (split prefill);
 // all fused: the discretised A and B, and the states, never leave the chip
 // (the kernel fusion and SRAM residency of the presentation article,
 // section 3.3 -- restated here for TMA and registers).
@@ -112,6 +115,31 @@ __device__ __forceinline__ u64 silu2(u64 z2) {
     return mul2(z2, pk2(rcp_approx(lo2(d)), rcp_approx(hi2(d))));
 }
 
+// Zero-order-hold input gain of a state pair: zoh_gain (msc_device.cuh) on
+// both halves, same operations in the same order.
+__device__ __forceinline__ u64 zoh_gain2(u64 x2, u64 dA, u64 dl2, u64 iA2) {
+    u64 p = pk2(kZohC5, kZohC5);
+    p = fma2(p, x2, pk2(kZohC4, kZohC4));
+    p = fma2(p, x2, pk2(kZohC3, kZohC3));
+    p = fma2(p, x2, pk2(kZohC2, kZohC2));
+    p = fma2(p, x2, pk2(kZohC1, kZohC1));
+    p = fma2(p, x2, pk2(1.0f, 1.0f));
+    const u64 small = mul2(dl2, p);
+    const u64 large = mul2(add2(dA, pk2(-1.0f, -1.0f)), iA2);
+    return pk2(fabsf(lo2(x2)) < kZohSwitch ? lo2(small) : lo2(large),
+               fabsf(hi2(x2)) < kZohSwitch ? hi2(small) : hi2(large));
+}
+
+// Input term of a state pair: (delta*u)*B, or with zero-order hold
+// (gain*u)*B, where `du2` carries delta*u, respectively u (see octet_prologue).
+template <bool ZOH>
+__device__ __forceinline__ u64 injection2(u64 x2, u64 dA, u64 dl2, u64 du2, u64 iA2, u64 B2) {
+    if constexpr (ZOH)
+        return mul2(mul2(zoh_gain2(x2, dA, dl2, iA2), du2), B2);
+    else
+        return mul2(du2, B2);
+}
+
 // Reduce-scatter of the 8 per-step partial sums over the G lanes of a
 // channel (lanes ch, ch + CPW, ...): afterwards out[m] holds the full sum of
 // step g + G*m, m < 8/G.
@@ -149,12 +177,13 @@ __device__ __forceinline__ void reduce_scatter(const float (&y)[kOct], int lane,
 }
 
 // Per-(step, channel) prologue of one octet: delta = softplus(dt + dt_bias)
-// and delta*u for steps g + G*m (m < 8/G) of the octet whose first row is
-// `row0` of the tile at `stage`; written to `dst` (the lane's channel row of
-// one sDU buffer, indexed by step) for the core.  The u of those steps is
-// returned as pairs for the D*u term.  MASK: steps at or past `nsteps` get
-// delta = 0 (state passes through, no input).
-template <typename T, int G, int TT, bool MASK>
+// and delta*u (ZOH: u, the gain being per state) for steps g + G*m
+// (m < 8/G) of the octet whose first row is `row0` of the tile at `stage`;
+// written to `dst` (the lane's channel row of one sDU buffer, indexed by
+// step) for the core.  The u of those steps is returned as pairs for the D*u
+// term.  MASK: steps at or past `nsteps` get delta = 0 and no input (the
+// state passes through).
+template <typename T, int G, int TT, bool MASK, bool ZOH>
 __device__ __forceinline__ void octet_prologue(const unsigned char* stage, int row0, int lane_x,
                                                float2* dst, u64 bias2, int s0_first,
                                                int nsteps, u64 (&uu)[kOct / G / 2]) {
@@ -168,7 +197,7 @@ __device__ __forceinline__ void octet_prologue(const unsigned char* stage, int r
         const u64 x =
             add2(pk2(lds_elem<T>(sx + TT * CPW + r0), lds_elem<T>(sx + TT * CPW + r1)), bias2);
         const u64 dl = softplus2(x);
-        const u64 du = mul2(dl, uu[p]);
+        const u64 du = ZOH ? uu[p] : mul2(dl, uu[p]);
         if (MASK) {
             const int s0 = s0_first + G * (2 * p);
             const bool v0 = s0 < nsteps, v1 = s0 + G < nsteps;
@@ -181,7 +210,7 @@ __device__ __forceinline__ void octet_prologue(const unsigned char* stage, int r
     }
 }
 
-template <typename T, int G, int NS, int TT, int S>
+template <typename T, int G, int NS, int TT, int S, bool ZOH>
 __global__ void __launch_bounds__(32)
 scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dt,
                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
@@ -243,12 +272,15 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     // per-channel constants and the starting state
     const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
     const float Dd = a.D ? __ldg(a.D + d) : 0.0f;
-    u64 A2[NP], hp[NP];
+    u64 A2[NP], iA2[NP], hp[NP];
+    const float* h0 = a.h0 ? a.h0 + ((int64_t)b * a.d_inner + d) * N + n0 : nullptr;
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
         const float* Ar = a.A + d * N + n0 + 2 * i;
-        A2[i] = pk2(__ldg(Ar) * kLog2e, __ldg(Ar + 1) * kLog2e);
-        hp[i] = pk2(0.0f, 0.0f);
+        const float a0 = __ldg(Ar), a1 = __ldg(Ar + 1);
+        A2[i] = pk2(a0 * kLog2e, a1 * kLog2e);
+        iA2[i] = ZOH ? pk2(1.0f / a0, 1.0f / a1) : pk2(0.0f, 0.0f);
+        hp[i] = h0 ? pk2(h0[2 * i], h0[2 * i + 1]) : pk2(0.0f, 0.0f);
     }
     if (k > 0) {
         for (int j2 = 0; j2 < k; ++j2) {
@@ -273,7 +305,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 #pragma unroll
     for (int p = 0; p < PPL; ++p) u_cur[p] = u_nxt[p] = pk2(0.0f, 0.0f);
     if (ok && ntiles > 0)
-        octet_prologue<T, G, TT, true>(smem, 0, lane_x, sDU + ch * kDUStride + g, bias2, g,
+        octet_prologue<T, G, TT, true, ZOH>(smem, 0, lane_x, sDU + ch * kDUStride + g, bias2, g,
                                        nsteps, u_cur);
     __syncwarp();
 
@@ -329,7 +361,8 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 for (int i2 = 0; i2 < NP; ++i2) {
                     const u64 x2 = mul2(dl2, A2[i2]);
                     const u64 dA = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
-                    hp[i2] = fma2(dA, hp[i2], mul2(du2, Bp[i2]));
+                    hp[i2] = fma2(dA, hp[i2],
+                                  injection2<ZOH>(x2, dA, dl2, du2, iA2[i2], Bp[i2]));
                     y2 = fma2(Cp[i2], hp[i2], y2);
                 }
                 yv[j] = lo2(y2) + hi2(y2);
@@ -338,7 +371,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             //     octet's (next tile: wait for it first)
             float2* const dnx = sDU + (((oo + 1) & 1) * CPW + ch) * kDUStride + g;
             if (oo + 1 < OPT) {
-                octet_prologue<T, G, TT, !FULL>(st, kOct * (oo + 1), lane_x, dnx, bias2,
+                octet_prologue<T, G, TT, !FULL, ZOH>(st, kOct * (oo + 1), lane_x, dnx, bias2,
                                                 sb + kOct + g, nsteps, u_nxt);
             } else if (i + 1 < ntiles) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * nxt_idx,
@@ -347,10 +380,10 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 waited = i + 2;
                 const unsigned char* stn = smem + nxt_idx * Lay::kStage;
                 if ((i + 2) * TT <= nsteps)
-                    octet_prologue<T, G, TT, false>(stn, 0, lane_x, dnx, bias2, sb + kOct + g,
+                    octet_prologue<T, G, TT, false, ZOH>(stn, 0, lane_x, dnx, bias2, sb + kOct + g,
                                                     nsteps, u_nxt);
                 else
-                    octet_prologue<T, G, TT, true>(stn, 0, lane_x, dnx, bias2, sb + kOct + g,
+                    octet_prologue<T, G, TT, true, ZOH>(stn, 0, lane_x, dnx, bias2, sb + kOct + g,
                                                    nsteps, u_nxt);
             }
             // (3) outputs of steps g + G*m of channel ch
@@ -424,7 +457,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 // prologue as scan_tma_kernel; only u, dt and B are loaded.
 constexpr float kSummaryCut = 9.094947e-13f;  // 2^-40
 
-template <typename T, int G, int NS, int TT, int S>
+template <typename T, int G, int NS, int TT, int S, bool ZOH>
 __global__ void __launch_bounds__(32)
 scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
                     const __grid_constant__ CUtensorMap tm_dt,
@@ -478,11 +511,13 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
 
     const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
     const u64 bias2 = pk2(bias, bias);
-    u64 A2[NP], Pp[NP], bp[NP];
+    u64 A2[NP], iA2[NP], Pp[NP], bp[NP];
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
         const float* Ar = a.A + d * N + n0 + 2 * i;
-        A2[i] = pk2(__ldg(Ar) * kLog2e, __ldg(Ar + 1) * kLog2e);
+        const float a0 = __ldg(Ar), a1 = __ldg(Ar + 1);
+        A2[i] = pk2(a0 * kLog2e, a1 * kLog2e);
+        iA2[i] = ZOH ? pk2(1.0f / a0, 1.0f / a1) : pk2(0.0f, 0.0f);
         Pp[i] = pk2(1.0f, 1.0f);
         bp[i] = pk2(0.0f, 0.0f);
     }
@@ -493,7 +528,7 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
     bool ok = ntiles == 0 || __all_sync(0xffffffffu, mbar_wait(bar0, 0, kWaitLimit));
     int waited = ntiles > 0 ? 1 : 0;
     if (ok && ntiles > 0)
-        octet_prologue<T, G, TT, false>(smem, kOct * (OPT - 1), lane_x, sDU + ch * kDUStride + g,
+        octet_prologue<T, G, TT, false, ZOH>(smem, kOct * (OPT - 1), lane_x, sDU + ch * kDUStride + g,
                                         bias2, 0, 0, uu);
     __syncwarp();
 
@@ -529,20 +564,21 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
                 for (int i2 = 0; i2 < NP; ++i2) {
                     const u64 x2 = mul2(dl2, A2[i2]);
                     const u64 dA = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
-                    bp[i2] = fma2(Pp[i2], mul2(du2, Bp[i2]), bp[i2]);
+                    bp[i2] = fma2(Pp[i2], injection2<ZOH>(x2, dA, dl2, du2, iA2[i2], Bp[i2]),
+                                  bp[i2]);
                     Pp[i2] = mul2(Pp[i2], dA);
                 }
             }
             // (2) the previous octet's step sizes (previous tile: wait first)
             float2* const dnx = sDU + (((c + 1) & 1) * CPW + ch) * kDUStride + g;
             if (oo > 0) {
-                octet_prologue<T, G, TT, false>(st, kOct * (oo - 1), lane_x, dnx, bias2, 0, 0, uu);
+                octet_prologue<T, G, TT, false, ZOH>(st, kOct * (oo - 1), lane_x, dnx, bias2, 0, 0, uu);
             } else if (r + 1 < ntiles) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * ((r + 1) % S),
                                                        ((r + 1) / S) & 1, kWaitLimit));
                 if (!ok) break;
                 waited = r + 2;
-                octet_prologue<T, G, TT, false>(smem + ((r + 1) % S) * Lay::kStage,
+                octet_prologue<T, G, TT, false, ZOH>(smem + ((r + 1) % S) * Lay::kStage,
                                                 kOct * (OPT - 1), lane_x, dnx, bias2, 0, 0, uu);
             }
             __syncwarp();
@@ -667,7 +703,8 @@ static cudaError_t launch_tma_ns(const ScanArgs& a, const ScanPlan& p, const flo
         return cudaErrorInvalidValue;
     const size_t smem = Lay::kTotal;
     if (p.K > 1) {
-        auto kern = scan_summary_kernel<T, G, NS, TT, S>;
+        auto kern = a.zoh ? scan_summary_kernel<T, G, NS, TT, S, true>
+                          : scan_summary_kernel<T, G, NS, TT, S, false>;
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         const int64_t nb = a.batch * (int64_t)(p.K - 1) * p.ntile;
@@ -675,7 +712,8 @@ static cudaError_t launch_tma_ns(const ScanArgs& a, const ScanPlan& p, const flo
     }
     const int64_t nb = a.batch * (int64_t)p.K * p.ntile;
     const ProfileMark m = profile_begin(s, MSC_PROF_SCAN);
-    auto kern = scan_tma_kernel<T, G, NS, TT, S>;
+    auto kern = a.zoh ? scan_tma_kernel<T, G, NS, TT, S, true>
+                      : scan_tma_kernel<T, G, NS, TT, S, false>;
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     kern<<<(unsigned)nb, 32, smem, s>>>(mu, mdt, mz, mB, mC, a, p.K);

@@ -5,6 +5,7 @@
 // and Mamba": constant memory per generated token):
 //     delta = softplus(dt + dt_bias);  h = exp(delta*A) * h + delta*B*u
 //     out = (C . h + D*u) * silu(z)
+// (delta*B is replaced by the zero-order-hold input matrix when asked).
 // The step is bound by streaming the fp32 state (8 bytes per state element
 // per step).  state_update_row_kernel (N = 8, 16, 32, aligned arrays) keeps
 // a whole channel per thread; state_update_kernel is the general form, a
@@ -42,10 +43,13 @@ state_update_kernel(UpdateArgs a) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) h[j] = (n0 + j < N) ? srow[n0 + j] : 0.0f;
     }
-    float A2[4];
+    float A2[4], iA[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        A2[j] = (n0 + j < N) ? __ldg(a.A + d * N + n0 + j) * kLog2e : 0.0f;
+    for (int j = 0; j < 4; ++j) {
+        const float Av = (n0 + j < N) ? __ldg(a.A + d * N + n0 + j) : 0.0f;
+        A2[j] = Av * kLog2e;
+        iA[j] = a.zoh ? 1.0f / Av : 0.0f;
+    }
 
     const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
     const float x = Elem<T>::load(static_cast<const T*>(a.dt) + ch) + bias;
@@ -58,8 +62,10 @@ state_update_kernel(UpdateArgs a) {
     float y = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float dA = ex2(delta * A2[j]);
-        h[j] = fmaf(dA, h[j], du * Bv[j]);
+        const float x2 = delta * A2[j];
+        const float dA = ex2(x2);
+        const float inj = a.zoh ? zoh_gain(x2, dA, delta, iA[j]) * uu * Bv[j] : du * Bv[j];
+        h[j] = fmaf(dA, h[j], inj);
         y = fmaf(Cv[j], h[j], y);
     }
 #pragma unroll
@@ -115,11 +121,21 @@ state_update_row_kernel(UpdateArgs a) {
     const float delta = softplus(x);
     const float du = delta * uu;
     float y = 0.0f;
+    if (a.zoh) {
 #pragma unroll
-    for (int n = 0; n < N; ++n) {
-        const float dA = ex2(delta * (Av[n] * kLog2e));  // same rounding as the scan
-        h[n] = fmaf(dA, h[n], du * sB[n]);
-        y = fmaf(sC[n], h[n], y);
+        for (int n = 0; n < N; ++n) {
+            const float x2 = delta * (Av[n] * kLog2e);
+            const float dA = ex2(x2);
+            h[n] = fmaf(dA, h[n], zoh_gain(x2, dA, delta, 1.0f / Av[n]) * uu * sB[n]);
+            y = fmaf(sC[n], h[n], y);
+        }
+    } else {
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+            const float dA = ex2(delta * (Av[n] * kLog2e));  // same rounding as the scan
+            h[n] = fmaf(dA, h[n], du * sB[n]);
+            y = fmaf(sC[n], h[n], y);
+        }
     }
 #pragma unroll
     for (int q = 0; q < N / 4; ++q)

@@ -176,3 +176,28 @@ def test_noalloc_rejects_problems_beyond_its_scratch(lib):
         lib.msc_tuning_set(b"scan_chunks", 0)
     assert st == 7
     assert lib.msc_status_string(7) != b"unknown status"
+
+
+def test_extended_entry_points_validate(lib):
+    """msc_selective_scan_fwd_ex / msc_selective_state_update_ex: unknown
+    discretisation and a misaligned h0 are refused before any launch."""
+    f = lib.msc_selective_scan_fwd_ex
+    f.restype = ctypes.c_int
+    f.argtypes = ([ctypes.c_void_p] * 11 + [ctypes.c_int64] * 4
+                  + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                     ctypes.c_void_p])
+    args = lambda h0, disc: (FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, h0,
+                             FAKE, None, 2, 8, 16, 16, 1, disc, None, 0, None)
+    assert f(*args(None, 2)) == 1
+    assert f(*args(None, -1)) == 1
+    assert f(*args(FAKE + 2, 1)) == 3               # h0 is fp32
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, FAKE, None,
+             0, 8, 16, 16, 1, 1, None, 0, None) == 0   # empty batch: no-op
+    g = lib.msc_selective_state_update_ex
+    g.restype = ctypes.c_int
+    g.argtypes = [ctypes.c_void_p] * 10 + [ctypes.c_int64] * 3 + [ctypes.c_int] * 2 + [
+        ctypes.c_void_p]
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE,
+             4, 16, 16, 1, 7, None) == 1
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE,
+             4, 16, 0, 1, 1, None) == 2
