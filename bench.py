@@ -481,7 +481,10 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
             return torch.from_numpy(bits.copy()).to(dev).view(torch.bfloat16)
         return torch.from_numpy(np.ascontiguousarray(arr, np.float32)).to(dev)
 
-    for name in ("long_seq_64k", "mamba2p8b_layer"):
+    # (workload, zero-order hold): the other two scan workloads, and the
+    # 8 x 2048 x 1536 x 16 layer once more with the ZOH input matrix
+    for name, zoh in (("long_seq_64k", False), ("mamba2p8b_layer", False),
+                      ("mamba130m_layer", True)):
         w = synth.WORKLOADS[name]
         x = synth.workload_inputs(name)
         a = dict(u=dev_t(x.u, "bf16"), dt=dev_t(x.dt_raw, "bf16"),
@@ -495,7 +498,7 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
         nws = msc.scan_workspace_size(B_, L_, D_, N_, torch.bfloat16)
         wsp = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
         for _ in range(3):
-            msc.selective_scan_fwd_ws(**a, out=out, last_state=last, workspace=wsp)
+            msc.selective_scan_fwd_ws(**a, out=out, last_state=last, workspace=wsp, zoh=zoh)
         times, total = [], []
         for _ in range(7):
             flush()
@@ -505,7 +508,7 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
-            msc.selective_scan_fwd_ws(**a, out=out, last_state=last, workspace=wsp)
+            msc.selective_scan_fwd_ws(**a, out=out, last_state=last, workspace=wsp, zoh=zoh)
             e1.record()
             e1.synchronize()
             msc.profile_enable(False)
@@ -515,8 +518,9 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
         upd, mufu, byt = algorithmic(B_, L_, D_, N_)
         ms = statistics.median(total)
         kms = statistics.median(times)
-        res[name] = {
-            "shape": [B_, L_, D_, N_], "ms": ms,
+        res[name + ("_zoh" if zoh else "")] = {
+            "shape": [B_, L_, D_, N_], "discretization": "zoh" if zoh else "euler",
+            "ms": ms,
             "updates_per_s": upd / (ms * 1e-3),
             "output_kernel_ms": kms,
             "mufu_frac": (mufu / (ms * 1e-3)) / ex2_peak,

@@ -82,6 +82,8 @@ ScanPlan make_tma_plan(int64_t batch, int64_t L, int64_t d_inner, int64_t N, int
                        int64_t force_chunks, int64_t min_chunk, bool need_bc,
                        int64_t force_lanes);
 
+// States entering chunks 1..K-1, written over ws_b (K > 1; h0 or zero first).
+cudaError_t launch_carry_prefix(const ScanArgs& a, cudaStream_t s);
 cudaError_t launch_scan(const ScanArgs& a, const ScanPlan& p, msc_dtype dtype,
                         cudaStream_t stream);
 

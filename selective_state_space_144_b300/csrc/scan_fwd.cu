@@ -17,10 +17,11 @@
 // chunk + recompute scheme of "Deep dive into Mamba", section 7.3):
 //   pass 1 (chunks 0..K-2): run each chunk from a zero state, keep its end
 //          state b_k and its transfer coefficient a_k = prod of the decays;
-//   pass 2 (all chunks):    fold (a_j, b_j), j < k, in order into the state
-//          entering chunk k -- the associative combine
-//          (a1, b1) then (a2, b2) -> (a2*a1, a2*b1 + b2) --
-//          then rerun the chunk from it and emit outputs.
+//   prefix:  fold (a_j, b_j) in order into the state entering every chunk
+//          -- the associative combine (a1, b1) then (a2, b2) ->
+//          (a2*a1, a2*b1 + b2) -- one thread per (batch, channel, state);
+//   pass 2 (all chunks): rerun each chunk from its entering state and emit
+//          outputs.
 // The exponential uses the MUFU ex2 unit with log2(e) folded into A once.
 #include "msc_device.cuh"
 #include "msc_internal.h"
@@ -48,7 +49,7 @@ scan_chunk_kernel(ScanArgs a, int kgrid) {
     const int64_t t1 = min(t0 + a.chunk, a.L);
 
     float A2[4], iA[4], h[4], P[4];
-    const float* h0 = OUTPUT ? a.h0 : nullptr;
+    const float* h0 = (OUTPUT && k == 0) ? a.h0 : nullptr;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int n = n0 + j;
@@ -59,15 +60,11 @@ scan_chunk_kernel(ScanArgs a, int kgrid) {
         P[j] = 1.0f;
     }
     if (OUTPUT && k > 0) {
-        // state entering chunk k, from the chunk summaries of pass 1
-        for (int j2 = 0; j2 < k; ++j2) {
-            const int64_t w = ((b * (a.K - 1) + j2) * a.d_inner + d) * N;
+        // state entering chunk k (carry_prefix_kernel, from the summaries)
+        const int64_t w = ((b * (a.K - 1) + k - 1) * a.d_inner + d) * N;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (n0 + j < N)
-                    h[j] = fmaf(a.ws_a[w + n0 + j], h[j], a.ws_b[w + n0 + j]);
-            }
-        }
+        for (int j = 0; j < 4; ++j)
+            if (n0 + j < N) h[j] = a.ws_b[w + n0 + j];
     }
 
     const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
@@ -142,6 +139,36 @@ scan_chunk_kernel(ScanArgs a, int kgrid) {
     }
 }
 
+// Entering states of the time chunks from their summaries: one thread per
+// (batch, channel, state) folds (a_k, b_k), k = 0..K-2, in order with the
+// combine (a1, b1) then (a2, b2) -> (a2*a1, a2*b1 + b2) applied to a state
+// (presentation article, section 3.2), starting from h0 (or zero), and
+// overwrites b_k with the state entering chunk k+1.  The output kernels then
+// read one state per chunk instead of folding all earlier summaries.
+__global__ void __launch_bounds__(256)
+carry_prefix_kernel(const float* __restrict__ ws_a, float* ws_b, const float* __restrict__ h0,
+                    int64_t batch, int K, int64_t dn) {
+    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;  // (b, d, n) flat
+    if (i >= batch * dn) return;
+    const int64_t b = i / dn, e = i - b * dn;
+    float h = h0 ? h0[i] : 0.0f;
+    const int64_t base = b * (int64_t)(K - 1) * dn + e;
+#pragma unroll 8
+    for (int k = 0; k < K - 1; ++k) {
+        const int64_t w = base + (int64_t)k * dn;
+        h = fmaf(ws_a[w], h, ws_b[w]);
+        ws_b[w] = h;
+    }
+}
+
+cudaError_t launch_carry_prefix(const ScanArgs& a, cudaStream_t s) {
+    const int64_t dn = a.d_inner * a.N;
+    const int64_t n = a.batch * dn;
+    carry_prefix_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.ws_a, a.ws_b, a.h0,
+                                                                   a.batch, a.K, dn);
+    return cudaGetLastError();
+}
+
 int lanes_per_channel(int64_t N) {
     return N <= 4 ? 1 : N <= 8 ? 2 : N <= 16 ? 4 : N <= 32 ? 8 : 16;
 }
@@ -207,7 +234,12 @@ ScanPlan make_tma_plan(int64_t batch, int64_t L, int64_t d_inner, int64_t N, int
         if (force_chunks > 0) {
             K = force_chunks;
         } else {
-            K = warps1 >= target ? 1 : (target + warps1 - 1) / warps1;
+            // Once time must be cut, cut it finer than the minimum that fills
+            // the GPU: the summary pass of a chunk whose decays stay near 1
+            // walks all of it, so shorter chunks shorten the slowest warps'
+            // walks, and several waves of CTAs even out the rest.
+            constexpr int64_t kChunkWaves = 7;
+            K = warps1 >= target ? 1 : (kChunkWaves * target + warps1 - 1) / warps1;
             const int64_t maxK = L / (min_chunk > 0 ? min_chunk : 1);
             K = K < maxK ? K : maxK;
         }
@@ -235,12 +267,14 @@ static cudaError_t launch_scan_g(const ScanArgs& a, const ScanPlan& p,
         const int64_t nb = a.batch * (int64_t)(p.K - 1) * p.ntile;
         scan_chunk_kernel<T, G, VEC, false>
             <<<(unsigned)nb, kScanThreads, 0, s>>>(a, p.K - 1);
+        const cudaError_t e = launch_carry_prefix(a, s);
+        if (e != cudaSuccess) return e;
     }
     const int64_t nb = a.batch * (int64_t)p.K * p.ntile;
     const ProfileMark m = profile_begin(s, MSC_PROF_SCAN);
     scan_chunk_kernel<T, G, VEC, true><<<(unsigned)nb, kScanThreads, 0, s>>>(a, p.K);
     profile_end(m, s);
-    profile_count(p.K > 1 ? 2 : 1);
+    profile_count(p.K > 1 ? 3 : 1);
     return cudaGetLastError();
 }
 

@@ -39,9 +39,9 @@
 //
 // Time chunks (K > 1) follow the segmented scan of the presentation
 // article, section 3.2: the summary kernel runs chunks 0..K-2 from a zero
-// state and records (prod dA, end state); the output kernel folds the
-// summaries of the chunks before its own into its starting state with the
-// combine (a1, b1) then (a2, b2) -> (a2*a1, a2*b1 + b2).
+// state and records (prod dA, end state); carry_prefix_kernel folds them in
+// order with the combine (a1, b1) then (a2, b2) -> (a2*a1, a2*b1 + b2) into
+// the state entering every chunk; the output kernel starts from it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -273,7 +273,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
     const float Dd = a.D ? __ldg(a.D + d) : 0.0f;
     u64 A2[NP], iA2[NP], hp[NP];
-    const float* h0 = a.h0 ? a.h0 + ((int64_t)b * a.d_inner + d) * N + n0 : nullptr;
+    const float* h0 = (a.h0 && k == 0) ? a.h0 + ((int64_t)b * a.d_inner + d) * N + n0 : nullptr;
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
         const float* Ar = a.A + d * N + n0 + 2 * i;
@@ -282,15 +282,12 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         iA2[i] = ZOH ? pk2(1.0f / a0, 1.0f / a1) : pk2(0.0f, 0.0f);
         hp[i] = h0 ? pk2(h0[2 * i], h0[2 * i + 1]) : pk2(0.0f, 0.0f);
     }
-    if (k > 0) {
-        for (int j2 = 0; j2 < k; ++j2) {
-            const int64_t w = ((int64_t)(b * (a.K - 1) + j2) * a.d_inner + d) * N + n0;
+    if (k > 0) {  // state entering chunk k (carry_prefix_kernel)
+        const int64_t w = ((int64_t)(b * (a.K - 1) + k - 1) * a.d_inner + d) * N + n0;
 #pragma unroll
-            for (int i = 0; i < NP; ++i) {
-                const float2 av = *reinterpret_cast<const float2*>(a.ws_a + w + 2 * i);
-                const float2 bv = *reinterpret_cast<const float2*>(a.ws_b + w + 2 * i);
-                hp[i] = fma2(pk2(av.x, av.y), hp[i], pk2(bv.x, bv.y));
-            }
+        for (int i = 0; i < NP; ++i) {
+            const float2 v = *reinterpret_cast<const float2*>(a.ws_b + w + 2 * i);
+            hp[i] = pk2(v.x, v.y);
         }
     }
 
@@ -709,6 +706,8 @@ static cudaError_t launch_tma_ns(const ScanArgs& a, const ScanPlan& p, const flo
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         const int64_t nb = a.batch * (int64_t)(p.K - 1) * p.ntile;
         kern<<<(unsigned)nb, 32, smem, s>>>(mu, mdt, mB, a, p.K - 1);
+        const cudaError_t e = launch_carry_prefix(a, s);
+        if (e != cudaSuccess) return e;
     }
     const int64_t nb = a.batch * (int64_t)p.K * p.ntile;
     const ProfileMark m = profile_begin(s, MSC_PROF_SCAN);
@@ -718,7 +717,7 @@ static cudaError_t launch_tma_ns(const ScanArgs& a, const ScanPlan& p, const flo
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     kern<<<(unsigned)nb, 32, smem, s>>>(mu, mdt, mz, mB, mC, a, p.K);
     profile_end(m, s);
-    profile_count(p.K > 1 ? 2 : 1);
+    profile_count(p.K > 1 ? 3 : 1);
     return cudaGetLastError();
 }
 

@@ -91,35 +91,40 @@ state_update_kernel(UpdateArgs a) {
 // channel; B and C of the batch row are staged once per CTA in shared memory
 // as fp32.  Grid (d_inner / 128, batch): no index division.  The state moves
 // as N/4 16-byte loads and stores per thread (the warp's 32 x N*4 bytes are
-// contiguous, so every fetched sector is used).
+// contiguous, so every fetched sector is used).  The kernel is bound by the
+// latency of those loads, so every global load of the thread -- state, A,
+// u, dt, z, bias, D -- is issued before the barrier that publishes B and C.
 template <typename T, int N>
 __global__ void __launch_bounds__(128)
 state_update_row_kernel(UpdateArgs a) {
     __shared__ float sB[N], sC[N];
     const int b = blockIdx.y;
-    if (threadIdx.x < N) {
-        sB[threadIdx.x] = Elem<T>::load(static_cast<const T*>(a.B) + (int64_t)b * N + threadIdx.x);
-        sC[threadIdx.x] = Elem<T>::load(static_cast<const T*>(a.C) + (int64_t)b * N + threadIdx.x);
-    }
-    __syncthreads();
-    const int64_t d = (int64_t)blockIdx.x * 128 + threadIdx.x;
-    if (d >= a.d_inner) return;
+    const int64_t d_raw = (int64_t)blockIdx.x * 128 + threadIdx.x;
+    const bool valid = d_raw < a.d_inner;
+    const int64_t d = valid ? d_raw : a.d_inner - 1;  // idle threads read in bounds
     const int64_t ch = (int64_t)b * a.d_inner + d;
     float4* srow = reinterpret_cast<float4*>(a.state + ch * N);
     const float4* arow = reinterpret_cast<const float4*>(a.A + d * N);
     float h[N], Av[N];
 #pragma unroll
     for (int q = 0; q < N / 4; ++q) {
-        const float4 v = srow[q];
+        const float4 v = __ldcs(srow + q);  // streamed: read once, written once
         h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
         const float4 w = __ldg(arow + q);
         Av[4 * q] = w.x; Av[4 * q + 1] = w.y; Av[4 * q + 2] = w.z; Av[4 * q + 3] = w.w;
     }
     const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
+    const float Dd = a.D ? __ldg(a.D + d) : 0.0f;
     const float x = Elem<T>::load(static_cast<const T*>(a.dt) + ch) + bias;
     const float uu = Elem<T>::load(static_cast<const T*>(a.u) + ch);
+    const float zz = a.z ? Elem<T>::load(static_cast<const T*>(a.z) + ch) : 0.0f;
+    if (threadIdx.x < N) {
+        sB[threadIdx.x] = Elem<T>::load(static_cast<const T*>(a.B) + (int64_t)b * N + threadIdx.x);
+        sC[threadIdx.x] = Elem<T>::load(static_cast<const T*>(a.C) + (int64_t)b * N + threadIdx.x);
+    }
     const float delta = softplus(x);
     const float du = delta * uu;
+    __syncthreads();
     float y = 0.0f;
     if (a.zoh) {
 #pragma unroll
@@ -137,11 +142,12 @@ state_update_row_kernel(UpdateArgs a) {
             y = fmaf(sC[n], h[n], y);
         }
     }
+    if (!valid) return;
 #pragma unroll
     for (int q = 0; q < N / 4; ++q)
-        srow[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-    y = fmaf(a.D ? __ldg(a.D + d) : 0.0f, uu, y);
-    if (a.z) y *= silu(Elem<T>::load(static_cast<const T*>(a.z) + ch));
+        __stcs(srow + q, make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]));
+    y = fmaf(Dd, uu, y);
+    if (a.z) y *= silu(zz);
     Elem<T>::store(static_cast<T*>(a.out) + ch, y);
 }
 
