@@ -75,6 +75,10 @@ class Oracle:
         lib.oracle_scan_fwd_segmented.restype = ctypes.c_int
         lib.oracle_scan_fwd_segmented.argtypes = ([dp] * 10 + [i64] * 5
                                                   + [ctypes.c_int])
+        lib.oracle_causal_conv1d.restype = ctypes.c_int
+        lib.oracle_causal_conv1d.argtypes = [dp] * 6 + [i64] * 4 + [ctypes.c_int] * 2
+        lib.oracle_conv1d_update.restype = ctypes.c_int
+        lib.oracle_conv1d_update.argtypes = [dp] * 5 + [i64] * 3 + [ctypes.c_int] * 2
         self.lib = lib
         self.path = lib_path
 
@@ -145,6 +149,40 @@ class Oracle:
             raise ValueError("oracle_state_update rejected its sizes")
         return st, out
 
+    def causal_conv1d(self, x, w, bias=None, state_in=None, silu: bool = True,
+                      nthreads: int = 0):
+        """Causal depthwise conv1d (+ SiLU) in fp64 -> (out, state_out).
+
+        x: (batch, L, d_inner); w: (d_inner, d_conv); bias: (d_inner);
+        state_in / state_out: (batch, d_inner, d_conv - 1), oldest first."""
+        x, w = _f64(x), _f64(w)
+        bias, state_in = _f64(bias), _f64(state_in)
+        batch, L, d_inner = x.shape
+        d_conv = w.shape[1]
+        out = np.zeros((batch, L, d_inner), dtype=np.float64)
+        st = np.zeros((batch, d_inner, d_conv - 1), dtype=np.float64)
+        rc = self.lib.oracle_causal_conv1d(
+            _ptr(x), _ptr(w), _ptr(bias), _ptr(state_in), _ptr(out), _ptr(st),
+            batch, L, d_inner, d_conv, int(bool(silu)), int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_causal_conv1d rejected its sizes")
+        return out, st
+
+    def conv1d_update(self, state, x, w, bias=None, silu: bool = True,
+                      nthreads: int = 0):
+        """One decode step of the conv -> (new_state, out); inputs untouched."""
+        st = np.array(state, dtype=np.float64, copy=True, order="C")
+        x, w, bias = _f64(x), _f64(w), _f64(bias)
+        batch, d_inner = x.shape
+        d_conv = w.shape[1]
+        out = np.zeros((batch, d_inner), dtype=np.float64)
+        rc = self.lib.oracle_conv1d_update(
+            _ptr(st), _ptr(x), _ptr(w), _ptr(bias), _ptr(out), batch, d_inner,
+            d_conv, int(bool(silu)), int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_conv1d_update rejected its sizes")
+        return st, out
+
 
 _default = None
 
@@ -179,3 +217,11 @@ def scan_fwd_segmented(*args, **kwargs):
 
 def state_update(*args, **kwargs):
     return default().state_update(*args, **kwargs)
+
+
+def causal_conv1d(*args, **kwargs):
+    return default().causal_conv1d(*args, **kwargs)
+
+
+def conv1d_update(*args, **kwargs):
+    return default().conv1d_update(*args, **kwargs)

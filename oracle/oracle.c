@@ -234,3 +234,71 @@ int oracle_scan_fwd_segmented(const double* u, const double* dt_raw,
     }
     return 0;
 }
+
+/*
+ * Causal depthwise conv1d before the scan ("Deep dive into Mamba" section 3.2,
+ * the block's Conv1d with kernel d_conv, padding d_conv - 1, one group per
+ * channel, with bias; section 5.2 and the MambaBlock of "State space models
+ * and Mamba": the first L outputs are kept, then SiLU).  PyTorch's Conv1d is a
+ * cross-correlation, so with the left padding it reads, for output step t,
+ * the inputs t-(d_conv-1) ... t:
+ *     out[b,t,d] = bias[d] + sum_k w[d,k] * x[b, t - (d_conv-1) + k, d]
+ *     out        = silu(out) when `silu` is set.
+ * Inputs before t = 0 are zero, or, when state_in is given, the d_conv-1
+ * inputs that preceded the sequence (state_in[b,d,j] is input step
+ * j - (d_conv-1), oldest first).  state_out, when given, receives the last
+ * d_conv-1 inputs in the same layout (the state a decode step continues
+ * from).  x, out: (batch, L, d_inner); w: (d_inner, d_conv); bias (d_inner)
+ * nullable; state_in, state_out: (batch, d_inner, d_conv-1) nullable.
+ */
+int oracle_causal_conv1d(const double* x, const double* w, const double* bias,
+                         const double* state_in, double* out, double* state_out,
+                         int64_t batch, int64_t L, int64_t d_inner, int64_t d_conv,
+                         int silu, int nthreads) {
+    if (batch < 0 || L < 0 || d_inner < 0 || d_conv < 1) return -1;
+    const int64_t nch = batch * d_inner, H = d_conv - 1;
+    const int nt = set_threads(nthreads);
+#pragma omp parallel for schedule(static) num_threads(nt)
+    for (int64_t c = 0; c < nch; ++c) {
+        const int64_t b = c / d_inner, d = c % d_inner;
+        /* the input at step s, for s in [-H, L) */
+        #define XAT(s) ((s) >= 0 ? x[(b * L + (s)) * d_inner + d] \
+                                 : (state_in ? state_in[c * H + H + (s)] : 0.0))
+        for (int64_t t = 0; t < L; ++t) {
+            double acc = bias ? bias[d] : 0.0;
+            for (int64_t k = 0; k < d_conv; ++k)
+                acc += w[d * d_conv + k] * XAT(t - H + k);
+            out[(b * L + t) * d_inner + d] = silu ? oracle_silu(acc) : acc;
+        }
+        if (state_out)
+            for (int64_t j = 0; j < H; ++j) state_out[c * H + j] = XAT(L - H + j);
+        #undef XAT
+    }
+    return 0;
+}
+
+/*
+ * One decode step of the same conv: the window is the d_conv-1 stored inputs
+ * followed by x[b,d]; out[b,d] = (silu of) bias + sum_k w[d,k] * window[k];
+ * then the state drops its oldest input and appends x (in place).
+ * state: (batch, d_inner, d_conv-1); x, out: (batch, d_inner).
+ */
+int oracle_conv1d_update(double* state, const double* x, const double* w,
+                         const double* bias, double* out, int64_t batch,
+                         int64_t d_inner, int64_t d_conv, int silu, int nthreads) {
+    if (batch < 0 || d_inner < 0 || d_conv < 1) return -1;
+    const int64_t nch = batch * d_inner, H = d_conv - 1;
+    const int nt = set_threads(nthreads);
+#pragma omp parallel for schedule(static) num_threads(nt)
+    for (int64_t c = 0; c < nch; ++c) {
+        const int64_t d = c % d_inner;
+        double* st = state + c * H;
+        double acc = bias ? bias[d] : 0.0;
+        for (int64_t k = 0; k < H; ++k) acc += w[d * d_conv + k] * st[k];
+        acc += w[d * d_conv + H] * x[c];
+        out[c] = silu ? oracle_silu(acc) : acc;
+        for (int64_t k = 0; k + 1 < H; ++k) st[k] = st[k + 1];
+        if (H > 0) st[H - 1] = x[c];
+    }
+    return 0;
+}

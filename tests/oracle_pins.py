@@ -28,7 +28,12 @@ different evaluation that the pages or plain mathematics fix:
     step ends -- checked against a fine Runge-Kutta integration of
     h' = A h + B u and against the closed-form step response
     h(t) = B (e^(A t) - 1) / A; ZOH reduces to delta*B when A = 0 and as
-    delta -> 0.
+    delta -> 0;
+  * the causal depthwise conv1d before the scan ("Deep dive into Mamba"
+    sections 3.2 and 5.2): against torch's own conv1d in fp64 (groups =
+    channels, padding d_conv - 1, first L outputs), identity and pure-delay
+    kernels, its conv state equal to convolving the concatenated sequence,
+    and decode steps equal to the prefill.
 """
 from __future__ import annotations
 
@@ -366,6 +371,73 @@ def check_zoh_limits(orc):
     assert np.array_equal(st, last)
 
 
+
+def _conv_case(batch, L, d_inner, d_conv, seed):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((batch, L, d_inner)),
+            rng.standard_normal((d_inner, d_conv)),
+            rng.standard_normal(d_inner))
+
+
+def check_conv_against_torch(orc):
+    """The pages' module: nn.Conv1d(d, d, kernel_size=d_conv, padding=d_conv-1,
+    groups=d, bias) on (batch, d, L), first L outputs, then SiLU -- here
+    torch's functional conv1d in fp64 on the CPU."""
+    import torch
+    for d_conv, L in ((4, 37), (2, 5), (3, 2), (1, 6)):
+        x, w, bias = _conv_case(2, L, 5, d_conv, seed=30 + d_conv)
+        ref = torch.nn.functional.conv1d(
+            torch.from_numpy(x).transpose(1, 2), torch.from_numpy(w)[:, None, :],
+            torch.from_numpy(bias), padding=d_conv - 1, groups=5)[:, :, :L]
+        ref = ref.transpose(1, 2).numpy()
+        y, _ = orc.causal_conv1d(x, w, bias, silu=False)
+        assert np.allclose(y, ref, rtol=1e-13, atol=1e-13), d_conv
+        y, _ = orc.causal_conv1d(x, w, bias, silu=True)
+        assert np.allclose(y, _silu_np(ref), rtol=1e-13, atol=1e-13), d_conv
+
+
+def check_conv_special_kernels(orc):
+    """w = e_last is the identity, w = e_first delays by d_conv - 1 steps
+    (zeros enter first)."""
+    x, _, _ = _conv_case(2, 20, 3, 4, seed=35)
+    ident = np.zeros((3, 4)); ident[:, 3] = 1.0
+    y, st = orc.causal_conv1d(x, ident, None, silu=False)
+    assert np.array_equal(y, x)
+    assert np.array_equal(st, np.transpose(x[:, -3:, :], (0, 2, 1)))
+    delay = np.zeros((3, 4)); delay[:, 0] = 1.0
+    y, _ = orc.causal_conv1d(x, delay, None, silu=False)
+    assert np.array_equal(y[:, 3:], x[:, :-3]) and np.all(y[:, :3] == 0.0)
+
+
+def check_conv_state(orc):
+    """A conv state (the d_conv-1 inputs before t = 0, oldest first) acts as
+    a prefix of the sequence; state_out holds the last d_conv-1 inputs, also
+    when L < d_conv - 1; prefill in two pieces equals one prefill."""
+    x, w, bias = _conv_case(2, 30, 4, 4, seed=36)
+    prev = np.random.default_rng(37).standard_normal((2, 3, 4))   # (batch, time, d)
+    st_in = np.transpose(prev, (0, 2, 1)).copy()                   # (batch, d, 3)
+    y, st = orc.causal_conv1d(x, w, bias, state_in=st_in)
+    y_cat, st_cat = orc.causal_conv1d(np.concatenate([prev, x], axis=1), w, bias)
+    assert np.allclose(y, y_cat[:, 3:], rtol=1e-14, atol=1e-14)
+    assert np.array_equal(st, st_cat)
+    for k in (1, 2, 29):
+        ya, sa = orc.causal_conv1d(x[:, :k], w, bias)
+        yb, sb = orc.causal_conv1d(x[:, k:], w, bias, state_in=sa)
+        y0, s0 = orc.causal_conv1d(x, w, bias)
+        assert np.allclose(np.concatenate([ya, yb], axis=1), y0, rtol=1e-14, atol=1e-14)
+        assert np.array_equal(sb, s0), k
+
+
+def check_conv_decode_equals_prefill(orc):
+    x, w, bias = _conv_case(3, 12, 5, 4, seed=38)
+    y, st_ref = orc.causal_conv1d(x, w, bias)
+    st = np.zeros((3, 5, 3))
+    for t in range(12):
+        st, o = orc.conv1d_update(st, x[:, t], w, bias)
+        assert np.allclose(o, y[:, t], rtol=1e-14, atol=1e-14), t
+    assert np.array_equal(st, st_ref)
+
+
 ALL_CHECKS = [
     check_softplus,
     check_silu,
@@ -381,4 +453,8 @@ ALL_CHECKS = [
     check_zoh_matches_ode,
     check_zoh_step_response,
     check_zoh_limits,
+    check_conv_against_torch,
+    check_conv_special_kernels,
+    check_conv_state,
+    check_conv_decode_equals_prefill,
 ]

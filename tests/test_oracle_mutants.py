@@ -49,6 +49,19 @@ MUTANTS = [
      "const double dA = zoh ? expm1(x) : exp(x);"),
     ("decode_ignores_zoh", "b, d, 0, 1, 1, d_inner, d_state, zoh);",
      "b, d, 0, 1, 1, d_inner, d_state, 0);"),
+    ("conv_kernel_flipped", "acc += w[d * d_conv + k] * XAT(t - H + k);",
+     "acc += w[d * d_conv + (d_conv - 1 - k)] * XAT(t - H + k);"),
+    ("conv_no_bias", "double acc = bias ? bias[d] : 0.0;\n            for",
+     "double acc = 0.0;\n            for"),
+    ("conv_no_silu", "out[(b * L + t) * d_inner + d] = silu ? oracle_silu(acc) : acc;",
+     "out[(b * L + t) * d_inner + d] = acc;"),
+    ("conv_state_in_reversed", "state_in[c * H + H + (s)]", "state_in[c * H - 1 - (s)]"),
+    ("conv_state_out_reversed", "state_out[c * H + j] = XAT(L - H + j);",
+     "state_out[c * H + j] = XAT(L - 1 - j);"),
+    ("conv_update_no_shift", "st[k] = st[k + 1];", "st[k] = st[k];"),
+    ("conv_update_no_append", "if (H > 0) st[H - 1] = x[c];", ";"),
+    ("conv_update_window_reversed", "acc += w[d * d_conv + k] * st[k];",
+     "acc += w[d * d_conv + k] * st[H - 1 - k];"),
     ("segment_rerun_from_zero", "memcpy(hk, h, (size_t)d_state * sizeof(double));",
      "memset(hk, 0, (size_t)d_state * sizeof(double));"),
 ]
