@@ -481,6 +481,74 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
             return torch.from_numpy(bits.copy()).to(dev).view(torch.bfloat16)
         return torch.from_numpy(np.ascontiguousarray(arr, np.float32)).to(dev)
 
+    def hook_cold_ms(call, kind, reps=20):
+        """Median device time of one launch after an L2 flush, from the event
+        pair the library records around its kernel (no host time inside)."""
+        ts = []
+        for k in range(reps):
+            flush()
+            torch.cuda.synchronize(dev)
+            msc.profile_read()
+            msc.profile_enable(True)
+            call(k)
+            torch.cuda.synchronize(dev)
+            msc.profile_enable(False)
+            _, kinds = msc.profile_read()
+            ts.append(kinds[kind][1])
+        return statistics.median(ts)
+
+    def back_to_back_ms(call, n):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        for k in range(10):
+            call(k)
+        torch.cuda.synchronize(dev)
+        e0.record()
+        for k in range(n):
+            call(k)
+        e1.record()
+        e1.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    # causal conv1d (+ SiLU) before the scan: prefill on the layer's shape,
+    # and the decode token on the decode shape; d_conv 4, bf16
+    rng = np.random.default_rng(12)
+    Bc, Lc, Dc, Kc = 8, 2048, 1536, 4
+    xc = dev_t(synth.round_bf16(rng.standard_normal((Bc, Lc, Dc)).astype(np.float32)), "bf16")
+    wc = dev_t((rng.standard_normal((Dc, Kc)) / 2).astype(np.float32), "f32")
+    bc = dev_t((0.1 * rng.standard_normal(Dc)).astype(np.float32), "f32")
+    oc = torch.empty_like(xc)
+    sc = torch.empty(Bc, Dc, Kc - 1, dtype=torch.bfloat16, device=dev)
+    cstep = lambda k: msc.causal_conv1d_fwd(xc, wc, bc, out=oc, state_out=sc)
+    c_cold = hook_cold_ms(cstep, "conv")
+    c_b2b = back_to_back_ms(cstep, 200)
+    c_bytes = 2 * Bc * Lc * Dc * 2 + Dc * Kc * 4 + Dc * 4 + Bc * Dc * (Kc - 1) * 2
+    res["conv1d_prefill_8x2048x1536_k4"] = {
+        "shape": [Bc, Lc, Dc, Kc], "us_l2_flushed": c_cold * 1e3, "us_back_to_back": c_b2b * 1e3,
+        "algorithmic_bytes": c_bytes,
+        "hbm_frac_l2_flushed": (c_bytes / (c_cold * 1e-3)) / (peaks["hbm_gbs"] * 1e9),
+        "note": "x read and u written once (50 MB each); back to back, part of x stays in L2",
+    }
+    del xc, oc
+    Bu, Du = 256, 5120
+    xu = [dev_t(synth.round_bf16(rng.standard_normal((Bu, Du)).astype(np.float32)), "bf16")
+          for _ in range(4)]
+    wu = dev_t((rng.standard_normal((Du, Kc)) / 2).astype(np.float32), "f32")
+    bu = dev_t((0.1 * rng.standard_normal(Du)).astype(np.float32), "f32")
+    su = torch.zeros(Bu, Du, Kc - 1, dtype=torch.bfloat16, device=dev)
+    ou = torch.empty(Bu, Du, dtype=torch.bfloat16, device=dev)
+    ustep = lambda k: msc.causal_conv1d_update(su, xu[k % 4], wu, bu, out=ou)
+    u_cold = hook_cold_ms(ustep, "conv_update")
+    u_b2b = back_to_back_ms(ustep, 1000)
+    u_bytes = 2 * Bu * Du * (Kc - 1) * 2 + 2 * Bu * Du * 2 + Du * Kc * 4 + Du * 4
+    res["conv1d_update_256x5120_k4"] = {
+        "shape": [Bu, Du, Kc], "us_l2_flushed": u_cold * 1e3, "us_back_to_back": u_b2b * 1e3,
+        "algorithmic_bytes": u_bytes,
+        "hbm_frac_l2_flushed": (u_bytes / (u_cold * 1e-3)) / (peaks["hbm_gbs"] * 1e9),
+        "note": "21 MB per token: launch latency is a large part of a 3 us kernel",
+    }
+    del xu, su, ou
+
     # (workload, zero-order hold): the other two scan workloads, and the
     # 8 x 2048 x 1536 x 16 layer once more with the ZOH input matrix
     for name, zoh in (("long_seq_64k", False), ("mamba2p8b_layer", False),
@@ -562,15 +630,7 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
     msc.profile_enable(False)
     _, kinds = msc.profile_read()
     b2b_ms = e0.elapsed_time(e1) / steps
-    cold = []
-    for k in range(20):
-        flush()
-        e0.record()
-        dstep(k)
-        e1.record()
-        e1.synchronize()
-        cold.append(e0.elapsed_time(e1))
-    cold_ms = statistics.median(cold)
+    cold_ms = hook_cold_ms(dstep, "update")
     byt = 2 * Bb * Dd * Nn * 4 + 4 * Bb * Dd * 2 + 2 * Bb * Nn * 2 + Dd * Nn * 4 + 2 * Dd * 4
     upd = Bb * Dd * Nn
     res[name] = {

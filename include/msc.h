@@ -1,7 +1,8 @@
 /*
  * msc.h -- C ABI of the Mamba selective scan (S6) for NVIDIA B300 (sm_103a).
  *
- * Two operations, both defined by the web pages on the subject:
+ * Two operations, both defined by the web pages on the subject (and the
+ * causal conv1d that produces the scan's input, declared further down):
  *
  *   msc_selective_scan_fwd   -- the selective scan forward of "Deep dive into
  *     Mamba: architecture and implementation of selective state-space models"
@@ -151,6 +152,44 @@ msc_status msc_selective_scan_fwd_noalloc(
     void* out, float* last_state, int64_t batch, int64_t L, int64_t d_inner,
     int64_t d_state, msc_dtype dtype, msc_stream_t stream);
 
+/*
+ * Causal depthwise conv1d (+ SiLU) that produces the scan's input u from the
+ * block's projected input x ("Deep dive into Mamba", section 3.2: Conv1d
+ * with kernel d_conv, padding d_conv - 1, one group per channel, bias;
+ * section 5.2 and the MambaBlock of "State space models and Mamba": the
+ * first L outputs, then SiLU):
+ *     out[b,t,d] = silu(bias[d] + sum_k w[d,k] * x[b, t - (d_conv-1) + k, d])
+ *   x, out        : (batch, L, d_inner), `dtype`
+ *   w             : (d_inner, d_conv) fp32;  bias: (d_inner) fp32, nullable
+ *   state_in      : (batch, d_inner, d_conv-1), `dtype`, nullable: the
+ *                   d_conv-1 inputs before t = 0, oldest first (zero if NULL)
+ *   state_out     : same layout, nullable: receives the last d_conv-1
+ *                   inputs (the state msc_causal_conv1d_update continues
+ *                   from); with L < d_conv-1 it includes state_in's tail
+ *   silu          : 1 apply SiLU, 0 return the linear conv; else
+ *                   MSC_ERR_INVALID_ARG
+ * 1 <= d_conv <= 8 (MSC_ERR_UNSUPPORTED otherwise); batch <= 65535 and
+ * L <= 4,194,240.  out must not overlap x or the states; state_in and
+ * state_out must not overlap each other.  Arithmetic fp32, out rounded once.
+ */
+msc_status msc_causal_conv1d_fwd(
+    const void* x, const float* w, const float* bias, const void* state_in,
+    void* out, void* state_out, int64_t batch, int64_t L, int64_t d_inner,
+    int64_t d_conv, int silu, msc_dtype dtype, msc_stream_t stream);
+
+/*
+ * One decode token of the same conv: the window is the d_conv-1 inputs in
+ * `state` followed by x; out = (SiLU of) bias + sum_k w[d,k] * window[k];
+ * then `state` drops its oldest input and appends x, in place.
+ *   state         : (batch, d_inner, d_conv-1), `dtype` (NULL allowed only
+ *                   for d_conv == 1)
+ *   x, out        : (batch, d_inner), `dtype`;  w, bias as above.
+ */
+msc_status msc_causal_conv1d_update(
+    void* state, const void* x, const float* w, const float* bias, void* out,
+    int64_t batch, int64_t d_inner, int64_t d_conv, int silu, msc_dtype dtype,
+    msc_stream_t stream);
+
 /* Discretisation of the input matrix B (the _ex entry points). */
 typedef enum msc_discretization {
     MSC_DISC_EULER = 0,  /* delta * B                                    */
@@ -227,15 +266,21 @@ msc_status msc_tuning_set(const char* key, int64_t value);
 
 /*
  * Measurement hook.  While enabled, every call records a CUDA event pair
- * on its stream around its main kernel -- kind MSC_PROF_SCAN for the scan's
- * output kernel, MSC_PROF_UPDATE for the decode kernel -- and counts every
+ * on its stream around its main kernel (the kinds below) and counts every
  * kernel it launches.  msc_profile_read synchronises those events and
  * returns, since the last read: the number of kernels launched, and per
  * kind the number of timed main kernels and their summed device time in
- * milliseconds (arrays of 2, indexed by kind; NULL outputs are skipped);
+ * milliseconds (arrays of MSC_PROF_KINDS, indexed by kind; NULL outputs are
+ * skipped);
  * then it resets.  Process-wide and not thread-safe.  Disabled by default.
  */
-enum { MSC_PROF_SCAN = 0, MSC_PROF_UPDATE = 1 };
+enum {
+    MSC_PROF_SCAN = 0,         /* scan output kernel                 */
+    MSC_PROF_UPDATE = 1,       /* decode state-update kernel         */
+    MSC_PROF_CONV = 2,         /* causal conv1d prefill kernel       */
+    MSC_PROF_CONV_UPDATE = 3,  /* causal conv1d decode-update kernel */
+    MSC_PROF_KINDS = 4
+};
 msc_status msc_profile_enable(int on);
 msc_status msc_profile_read(int64_t* launches, int64_t* timed, double* total_ms);
 

@@ -80,6 +80,10 @@ def load():
                                               + [st, st, vp, ctypes.c_size_t, vp])
     lib.msc_selective_state_update_ex.restype = st
     lib.msc_selective_state_update_ex.argtypes = [vp] * 10 + [i64] * 3 + [st, st, vp]
+    lib.msc_causal_conv1d_fwd.restype = st
+    lib.msc_causal_conv1d_fwd.argtypes = [vp] * 6 + [i64] * 4 + [ctypes.c_int, st, vp]
+    lib.msc_causal_conv1d_update.restype = st
+    lib.msc_causal_conv1d_update.argtypes = [vp] * 5 + [i64] * 3 + [ctypes.c_int, st, vp]
     lib.msc_selective_scan_workspace_size.restype = st
     lib.msc_selective_scan_workspace_size.argtypes = [i64] * 4 + [
         st, ctypes.POINTER(sz)]
@@ -287,6 +291,57 @@ def selective_state_update(state, u, dt, A, B, C, D=None, z=None,
     return out
 
 
+def causal_conv1d_fwd(x, w, bias=None, state_in=None, out=None, state_out=None,
+                      silu=True, return_state=True):
+    """Causal depthwise conv1d (+ SiLU) on the GPU -> (out, state_out).
+
+    x: (batch, L, d_inner) bf16/fp32; w: (d_inner, d_conv) fp32; bias:
+    (d_inner) fp32; state_in / state_out: (batch, d_inner, d_conv - 1) in
+    x's dtype (the inputs before t = 0 / the last d_conv - 1 inputs)."""
+    torch = _torch()
+    if x.dim() != 3 or w.dim() != 2:
+        raise ValueError("x must be (batch, L, d_inner), w (d_inner, d_conv)")
+    batch, L, d_inner = x.shape
+    d_conv = w.shape[1]
+    dev, sdt, f32 = x.device, x.dtype, torch.float32
+    code = _dtype_code(x)
+    if out is None:
+        out = torch.empty_like(x)
+    if state_out is None and return_state:
+        state_out = torch.empty((batch, d_inner, d_conv - 1), dtype=sdt, device=dev)
+    st = load().msc_causal_conv1d_fwd(
+        _ptr(x, "x", sdt, (batch, L, d_inner), dev),
+        _ptr(w, "w", f32, (d_inner, d_conv), dev),
+        _ptr(bias, "bias", f32, (d_inner,), dev),
+        _ptr(state_in, "state_in", sdt, (batch, d_inner, d_conv - 1), dev),
+        _ptr(out, "out", sdt, (batch, L, d_inner), dev),
+        _ptr(state_out, "state_out", sdt, (batch, d_inner, d_conv - 1), dev),
+        batch, L, d_inner, d_conv, int(bool(silu)), code, _stream(dev))
+    _check("msc_causal_conv1d_fwd", st)
+    return out, state_out
+
+
+def causal_conv1d_update(state, x, w, bias=None, out=None, silu=True):
+    """One decode token of the conv; updates ``state`` in place -> out."""
+    if x.dim() != 2:
+        raise ValueError("x must be (batch, d_inner)")
+    batch, d_inner = x.shape
+    d_conv = w.shape[1]
+    dev, sdt = x.device, x.dtype
+    code = _dtype_code(x)
+    if out is None:
+        out = _torch().empty_like(x)
+    st = load().msc_causal_conv1d_update(
+        _ptr(state, "state", sdt, (batch, d_inner, d_conv - 1), dev),
+        _ptr(x, "x", sdt, (batch, d_inner), dev),
+        _ptr(w, "w", _torch().float32, (d_inner, d_conv), dev),
+        _ptr(bias, "bias", _torch().float32, (d_inner,), dev),
+        _ptr(out, "out", sdt, (batch, d_inner), dev),
+        batch, d_inner, d_conv, int(bool(silu)), code, _stream(dev))
+    _check("msc_causal_conv1d_update", st)
+    return out
+
+
 def check_device_error(clear: bool = True):
     """Raise MscError(MSC_ERR_TIMEOUT) if a kernel's bounded wait gave up.
     Synchronise the streams used first."""
@@ -298,16 +353,19 @@ def profile_enable(on: bool = True):
     _check("msc_profile_enable", load().msc_profile_enable(int(on)))
 
 
+_PROF_KINDS = ("scan", "update", "conv", "conv_update")   # msc.h MSC_PROF_* order
+
+
 def profile_read():
-    """Since the last read: (kernels launched, {"scan": (timed, ms),
-    "update": (timed, ms)}) -- main-kernel counts and summed device time.
-    Synchronises the recorded events, then resets the counters."""
+    """Since the last read: (kernels launched, {kind: (timed, ms)}) for the
+    kinds "scan", "update", "conv", "conv_update" -- main-kernel counts and
+    summed device time.  Synchronises the recorded events, then resets."""
     n = ctypes.c_int64(0)
-    timed = (ctypes.c_int64 * 2)()
-    ms = (ctypes.c_double * 2)()
+    timed = (ctypes.c_int64 * len(_PROF_KINDS))()
+    ms = (ctypes.c_double * len(_PROF_KINDS))()
     _check("msc_profile_read", load().msc_profile_read(ctypes.byref(n), timed, ms))
-    return int(n.value), {"scan": (int(timed[0]), float(ms[0])),
-                          "update": (int(timed[1]), float(ms[1]))}
+    return int(n.value), {k: (int(timed[i]), float(ms[i]))
+                          for i, k in enumerate(_PROF_KINDS)}
 
 
 def tuning_set(key: str, value: int):

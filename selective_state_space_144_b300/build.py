@@ -25,7 +25,8 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}", "-Xptxas", "-v"]
 
 LIBS = {
-    "libmsc.so": ["msc_api.cu", "scan_fwd.cu", "scan_tma.cu", "state_update.cu"],
+    "libmsc.so": ["msc_api.cu", "scan_fwd.cu", "scan_tma.cu", "state_update.cu",
+                  "conv1d.cu"],
     "libmsc_peaks.so": ["peaks.cu"],
 }
 

@@ -372,6 +372,59 @@ msc_status msc_selective_state_update_ex(float* state, const void* u, const void
                       disc == MSC_DISC_ZOH ? 1 : 0, stream);
 }
 
+static msc_status run_conv(const void* x, const float* w, const float* bias,
+                           const void* state_in, void* out, void* state, int64_t batch,
+                           int64_t L, int64_t d_inner, int64_t d_conv, int silu,
+                           msc_dtype dtype, bool update, msc_stream_t stream) {
+    if (dtype != MSC_F32 && dtype != MSC_BF16) return MSC_ERR_INVALID_ARG;
+    if (batch < 0 || L < 0 || d_inner < 0 || d_conv < 0 || (silu != 0 && silu != 1))
+        return MSC_ERR_INVALID_ARG;
+    if (d_conv < 1 || d_conv > 8) return MSC_ERR_UNSUPPORTED;
+    int64_t bl, bld, bdk;
+    if (!mul_ok(batch, L, &bl) || !mul_ok(bl, d_inner, &bld) || !mul_ok(batch, d_inner, &bdk) ||
+        !mul_ok(bdk, d_conv, &bdk) || bld > std::numeric_limits<int64_t>::max() / 8)
+        return MSC_ERR_UNSUPPORTED;
+    if (batch == 0 || d_inner == 0) return MSC_OK;
+    if (!w || ((update || L > 0) && (!x || !out)) || (update && d_conv > 1 && !state))
+        return MSC_ERR_INVALID_ARG;
+    if (batch > 65535 || (!update && (L + 63) / 64 > 65535)) return MSC_ERR_UNSUPPORTED;
+    const size_t es = elem_size(dtype);
+    const void* typed[] = {x, out, state_in, state};
+    for (const void* p : typed)
+        if (p && !aligned(p, es)) return MSC_ERR_ALIGNMENT;
+    if (!aligned(w, 4) || (bias && !aligned(bias, 4))) return MSC_ERR_ALIGNMENT;
+    msc::ConvArgs a{};
+    a.x = x; a.w = w; a.bias = bias; a.state_in = update ? nullptr : state_in;
+    a.out = out; a.state_out = state;
+    a.batch = batch; a.L = update ? 1 : L; a.d_inner = d_inner; a.d_conv = d_conv;
+    a.silu = silu;
+    a.vec = !update && (d_inner % (int64_t)(8 / es) == 0) && (!x || aligned(x, 8)) &&
+            (!out || aligned(out, 8));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    msc::ProfileMark m = msc::profile_begin(s, update ? MSC_PROF_CONV_UPDATE : MSC_PROF_CONV);
+    cudaError_t e = update ? msc::launch_conv1d_update(a, dtype, s)
+                           : msc::launch_causal_conv1d(a, dtype, s);
+    msc::profile_end(m, s);
+    msc::profile_count(1);
+    return e == cudaSuccess ? MSC_OK : MSC_ERR_CUDA;
+}
+
+msc_status msc_causal_conv1d_fwd(const void* x, const float* w, const float* bias,
+                                 const void* state_in, void* out, void* state_out,
+                                 int64_t batch, int64_t L, int64_t d_inner, int64_t d_conv,
+                                 int silu, msc_dtype dtype, msc_stream_t stream) {
+    return run_conv(x, w, bias, state_in, out, state_out, batch, L, d_inner, d_conv, silu,
+                    dtype, false, stream);
+}
+
+msc_status msc_causal_conv1d_update(void* state, const void* x, const float* w,
+                                    const float* bias, void* out, int64_t batch,
+                                    int64_t d_inner, int64_t d_conv, int silu, msc_dtype dtype,
+                                    msc_stream_t stream) {
+    return run_conv(x, w, bias, nullptr, out, state, batch, 1, d_inner, d_conv, silu, dtype,
+                    true, stream);
+}
+
 msc_status msc_tuning_set(const char* key, int64_t value) {
     if (!key || value < 0) return MSC_ERR_INVALID_ARG;
     if (std::strcmp(key, "scan_chunks") == 0) {
@@ -401,8 +454,8 @@ msc_status msc_profile_enable(int on) {
 }
 
 msc_status msc_profile_read(int64_t* launches, int64_t* timed, double* total_ms) {
-    double ms[2] = {0.0, 0.0};
-    int64_t n[2] = {0, 0};
+    double ms[MSC_PROF_KINDS] = {};
+    int64_t n[MSC_PROF_KINDS] = {};
     msc_status st = MSC_OK;
     for (auto& pr : g_prof_pairs) {
         float t = 0.0f;
@@ -415,13 +468,9 @@ msc_status msc_profile_read(int64_t* launches, int64_t* timed, double* total_ms)
         g_prof_free.push_back(pr.b);
     }
     if (launches) *launches = g_prof_launches;
-    if (timed) {
-        timed[0] = n[0];
-        timed[1] = n[1];
-    }
-    if (total_ms) {
-        total_ms[0] = ms[0];
-        total_ms[1] = ms[1];
+    for (int k = 0; k < MSC_PROF_KINDS; ++k) {
+        if (timed) timed[k] = n[k];
+        if (total_ms) total_ms[k] = ms[k];
     }
     g_prof_pairs.clear();
     g_prof_launches = 0;

@@ -62,11 +62,27 @@ struct UpdateArgs {
     int zoh;           // 1: zero-order-hold input matrix, 0: delta*B
 };
 
+// The causal depthwise conv1d before the scan (conv1d.cu).  For the decode
+// update, state_out is the conv state updated in place and state_in unused.
+struct ConvArgs {
+    const void* x;
+    const float* w;
+    const float* bias;
+    const void* state_in;
+    void* out;
+    void* state_out;
+    int64_t batch, L, d_inner, d_conv;
+    int silu;          // 1: SiLU on the output
+    int vec;           // 1: 8-byte vectors of channels (d_inner and x/out allow)
+};
+cudaError_t launch_causal_conv1d(const ConvArgs& a, msc_dtype dtype, cudaStream_t s);
+cudaError_t launch_conv1d_update(const ConvArgs& a, msc_dtype dtype, cudaStream_t s);
+
 // Measurement hook (msc_api.cu): while enabled, launchers count kernels and
 // bracket their main kernel with an event pair on the launch stream.
 struct ProfileMark {
     void* begin;  // cudaEvent_t or nullptr when profiling is off
-    int kind;     // MSC_PROF_SCAN or MSC_PROF_UPDATE
+    int kind;     // MSC_PROF_SCAN, _UPDATE, _CONV or _CONV_UPDATE
 };
 ProfileMark profile_begin(cudaStream_t s, int kind);
 void profile_end(const ProfileMark& m, cudaStream_t s);

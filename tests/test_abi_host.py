@@ -201,3 +201,25 @@ def test_extended_entry_points_validate(lib):
              4, 16, 16, 1, 7, None) == 1
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE,
              4, 16, 0, 1, 1, None) == 2
+
+
+def test_conv_entry_points_validate(lib):
+    f = lib.msc_causal_conv1d_fwd
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int64] * 4 + [ctypes.c_int] * 2 + [
+        ctypes.c_void_p]
+    c = lambda **k: f(k.get("x", FAKE), k.get("w", FAKE), None, k.get("st", None),
+                      k.get("out", FAKE), None, k.get("batch", 2), k.get("L", 8),
+                      k.get("d", 16), k.get("K", 4), k.get("silu", 1), k.get("dt", 1), None)
+    assert c(K=0) == 2 and c(K=9) == 2 and c(K=-1) == 1
+    assert c(silu=2) == 1 and c(dt=3) == 1 and c(L=-1) == 1
+    assert c(x=None) == 1 and c(w=None) == 1
+    assert c(x=FAKE + 1) == 3 and c(st=FAKE + 1) == 3
+    assert c(batch=70000) == 2
+    assert c(batch=0) == 0
+    g = lib.msc_causal_conv1d_update
+    g.restype = ctypes.c_int
+    g.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 3 + [ctypes.c_int] * 2 + [
+        ctypes.c_void_p]
+    assert g(None, FAKE, FAKE, None, FAKE, 2, 16, 4, 1, 1, None) == 1   # state needed
+    assert g(FAKE, FAKE, FAKE, None, FAKE, 2, 16, 12, 1, 1, None) == 2
