@@ -65,7 +65,8 @@ def parse():
                     help="skip the other workloads")
     ap.add_argument("--profile", default=None, metavar="WORKLOAD",
                     help="profiling driver: run only the scan (or, for "
-                         "decode_256x5120, the decode step) on WORKLOAD "
+                         "decode_256x5120, the decode step; for conv1d_prefill "
+                         "/ conv1d_update, the conv) on WORKLOAD "
                          "--warmup + --steps times, print nothing else "
                          "(for ncu; see profiles/)")
     return ap.parse_args()
@@ -664,6 +665,29 @@ def run_profile(args):
             return torch.from_numpy(bits.copy()).to(dev).view(torch.bfloat16)
         return torch.from_numpy(np.ascontiguousarray(arr, np.float32)).to(dev)
 
+    if name in ("conv1d_prefill", "conv1d_update"):
+        # the conv before the scan: prefill on the 8 x 2048 x 1536 layer, or
+        # the decode token on 256 x 5120; d_conv 4, bf16
+        rng = np.random.default_rng(12)
+        if name == "conv1d_prefill":
+            Bc, Lc, Dc = 8, 2048, 1536
+            x = dev_t(synth.round_bf16(rng.standard_normal((Bc, Lc, Dc)).astype(np.float32)),
+                      "bf16")
+        else:
+            Bc, Dc = 256, 5120
+            x = dev_t(synth.round_bf16(rng.standard_normal((Bc, Dc)).astype(np.float32)), "bf16")
+        wc = dev_t((rng.standard_normal((Dc, 4)) / 2).astype(np.float32), "f32")
+        bc = dev_t((0.1 * rng.standard_normal(Dc)).astype(np.float32), "f32")
+        st = torch.zeros(Bc, Dc, 3, dtype=torch.bfloat16, device=dev)
+        for _ in range(args.warmup + args.steps):
+            if name == "conv1d_prefill":
+                msc.causal_conv1d_fwd(x, wc, bc, state_out=st)
+            else:
+                msc.causal_conv1d_update(st, x, wc, bc)
+        torch.cuda.synchronize(dev)
+        msc.check_device_error()
+        print(f"profile run done: {name}, {args.warmup + args.steps} calls", flush=True)
+        return 0
     w = synth.WORKLOADS[name]
     if name.startswith("decode"):
         Bb, Dd, Nn = w["batch"], w["d_inner"], w["d_state"]

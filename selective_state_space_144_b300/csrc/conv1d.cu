@@ -17,6 +17,8 @@
 // rows (plus a halo of d_conv-1 rows) it loads into registers all at once
 // before computing; a warp's loads of one time row are 32 consecutive 8-byte
 // words.
+#include <type_traits>
+
 #include "msc_device.cuh"
 #include "msc_internal.h"
 
@@ -34,42 +36,30 @@ template <> struct Vec<__nv_bfloat16, 4> { using type = uint2; };
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 
-// Raw 8-byte word of V channels (V = 8 / sizeof(T)) <-> V floats.
-template <typename T>
-__device__ __forceinline__ void unpack_word(uint2 q, float* v) {
-    if constexpr (sizeof(T) == 4) {
-        v[0] = __uint_as_float(q.x);
-        v[1] = __uint_as_float(q.y);
+// Input word of a thread (V channels) as channel pairs.
+template <typename T, int V>
+__device__ __forceinline__ void word_pairs(const typename Vec<T, V>::type& q,
+                                           u64 (&p)[(V + 1) / 2]) {
+    if constexpr (V == 1) {
+        const float v = to_f32(q);
+        p[0] = pk2(v, v);
+    } else if constexpr (sizeof(T) == 4) {
+        p[0] = *reinterpret_cast<const u64*>(&q);
     } else {
-        v[0] = __uint_as_float(q.x << 16);
-        v[1] = __uint_as_float(q.x & 0xffff0000u);
-        v[2] = __uint_as_float(q.y << 16);
-        v[3] = __uint_as_float(q.y & 0xffff0000u);
+        p[0] = pk2(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xffff0000u));
+        p[1] = pk2(__uint_as_float(q.y << 16), __uint_as_float(q.y & 0xffff0000u));
     }
-}
-
-template <typename T>
-__device__ __forceinline__ uint2 pack_word(const float* v) {
-    uint2 q;
-    if constexpr (sizeof(T) == 4) {
-        q.x = __float_as_uint(v[0]);
-        q.y = __float_as_uint(v[1]);
-    } else {
-        const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
-        const __nv_bfloat162 c = __floats2bfloat162_rn(v[2], v[3]);
-        q.x = *reinterpret_cast<const uint32_t*>(&a);
-        q.y = *reinterpret_cast<const uint32_t*>(&c);
-    }
-    return q;
 }
 
 // Prefill.  Grid (channel groups of kConvThreads * V, time tiles of kTileT,
 // batch).  KC = d_conv, H = KC - 1.  A thread first loads the H + kTileT
 // input rows of its channels that its tile needs (the H halo rows from the
-// previous tile or the conv state) -- all loads in flight together, the
-// kernel being bound by memory latency and bandwidth -- then computes and
-// stores kTileT outputs.  The CTA whose tile holds the last step writes the
-// conv state (the last H inputs); with L == 0 one tile of no steps does that.
+// previous tile) -- all loads in flight together -- then computes kTileT
+// outputs on channel pairs (fma.rn.f32x2) and stores them.  Interior tiles
+// (halo inside the sequence, tile full) run without any per-step test; the
+// first tile takes its halo from the conv state (or zeros) and the last may
+// be partial.  The CTA whose tile holds the last step writes the conv state
+// (the last H inputs); with L == 0 one tile of no steps does that.
 template <typename T, int V, int KC>
 __global__ void __launch_bounds__(kConvThreads)
 causal_conv1d_kernel(const T* __restrict__ x, const float* __restrict__ w,
@@ -78,6 +68,7 @@ causal_conv1d_kernel(const T* __restrict__ x, const float* __restrict__ w,
                      int64_t d_inner, int silu_on) {
     constexpr int H = KC - 1;
     constexpr int R = H + kTileT;  // rows held: halo, then the tile
+    constexpr int P = (V + 1) / 2; // channel pairs (V = 1: one, upper half unused)
     using W = typename Vec<T, V>::type;
     const int64_t d0 = ((int64_t)blockIdx.x * kConvThreads + threadIdx.x) * V;
     if (d0 >= d_inner) return;
@@ -85,67 +76,88 @@ causal_conv1d_kernel(const T* __restrict__ x, const float* __restrict__ w,
     const int64_t t0 = (int64_t)blockIdx.y * kTileT;
     const int nt = (int)min((int64_t)kTileT, L - t0 > 0 ? L - t0 : 0);  // steps here
 
-    W raw[R];
+    u64 w2[P][KC], b2[P];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int64_t s = t0 - H + r;
-        if (s >= 0 && r < H + nt) raw[r] = *reinterpret_cast<const W*>(x + (b * L + s) * d_inner + d0);
+    for (int p = 0; p < P; ++p) {
+        const int64_t c0 = d0 + 2 * p, c1 = V == 1 ? c0 : c0 + 1;
+#pragma unroll
+        for (int k = 0; k < KC; ++k) w2[p][k] = pk2(__ldg(w + c0 * KC + k), __ldg(w + c1 * KC + k));
+        b2[p] = bias ? pk2(__ldg(bias + c0), __ldg(bias + c1)) : pk2(0.0f, 0.0f);
     }
-    float wv[V][KC], bv[V];
+    const T* xb = x + (b * L + t0 - H) * d_inner + d0;  // row r of the tile: xb + r * d_inner
+    T* op = out + (b * L + t0) * d_inner + d0;
+    u64 win[H + 1][P];  // rows t .. t + H of output step t
+
+    auto tile = [&](auto edge_tag) {
+        constexpr bool EDGE = decltype(edge_tag)::value;
+        W raw[R];
 #pragma unroll
-    for (int c = 0; c < V; ++c) {
+        for (int r = 0; r < R; ++r) {
+            if (!EDGE || (t0 - H + r >= 0 && r < H + nt))
+                raw[r] = *reinterpret_cast<const W*>(xb + (int64_t)r * d_inner);
+        }
 #pragma unroll
-        for (int k = 0; k < KC; ++k) wv[c][k] = __ldg(w + (d0 + c) * KC + k);
-        bv[c] = bias ? __ldg(bias + d0 + c) : 0.0f;
-    }
-    auto row = [&](int r, float (&v)[V]) {  // input row t0 - H + r as floats
-        const int64_t s = t0 - H + r;
-        if (s >= 0) {
-            if constexpr (V == 1) {
-                v[0] = to_f32(raw[r]);  // a register value: no memory load
-            } else {
-                unpack_word<T>(*reinterpret_cast<const uint2*>(&raw[r]), v);
+        for (int j = 0; j < H; ++j) {
+            if (!EDGE || t0 - H + j >= 0) {
+                word_pairs<T, V>(raw[j], win[j]);
+            } else {  // before the sequence: conv state, oldest first, or zero
+                const int64_t s = t0 - H + j;
+                float v[2 * P];
+#pragma unroll
+                for (int c = 0; c < 2 * P; ++c)
+                    v[c] = (state_in && c < V)
+                        ? Elem<T>::load(state_in + ((b * d_inner + d0 + c) * H + H + s))
+                        : 0.0f;
+#pragma unroll
+                for (int p = 0; p < P; ++p) win[j][p] = pk2(v[2 * p], v[2 * p + 1]);
             }
-        } else {
+        }
 #pragma unroll
-            for (int c = 0; c < V; ++c)
-                v[c] = state_in ? Elem<T>::load(state_in + ((b * d_inner + d0 + c) * H + H + s))
-                                : 0.0f;
+        for (int t = 0; t < kTileT; ++t) {
+            if (EDGE && t >= nt) break;
+            word_pairs<T, V>(raw[H + t], win[H]);
+            u64 y[P];
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                u64 acc = b2[p];
+#pragma unroll
+                for (int k = 0; k <= H; ++k) acc = fma2(w2[p][k], win[k][p], acc);
+                y[p] = silu_on ? silu2(acc) : acc;
+            }
+            T* o = op + (int64_t)t * d_inner;
+            if constexpr (V == 1) {
+                Elem<T>::store(o, lo2(y[0]));
+            } else if constexpr (sizeof(T) == 4) {
+                *reinterpret_cast<u64*>(o) = y[0];
+            } else {
+                const __nv_bfloat162 a2 = __floats2bfloat162_rn(lo2(y[0]), hi2(y[0]));
+                const __nv_bfloat162 c2 = __floats2bfloat162_rn(lo2(y[1]), hi2(y[1]));
+                uint2 q;
+                q.x = *reinterpret_cast<const uint32_t*>(&a2);
+                q.y = *reinterpret_cast<const uint32_t*>(&c2);
+                *reinterpret_cast<uint2*>(o) = q;
+            }
+#pragma unroll
+            for (int j = 0; j < H; ++j)
+#pragma unroll
+                for (int p = 0; p < P; ++p) win[j][p] = win[j + 1][p];
         }
     };
-    float win[H + 1][V];  // rows j .. j + H of the current output step
-#pragma unroll
-    for (int j = 0; j < H; ++j) row(j, win[j]);
-    T* op = out + (b * L + t0) * d_inner + d0;
-#pragma unroll
-    for (int t = 0; t < kTileT; ++t) {
-        if (t < nt) {
-            row(H + t, win[H]);
-            float y[V];
-#pragma unroll
-            for (int c = 0; c < V; ++c) {
-                float acc = bv[c];
-#pragma unroll
-                for (int k = 0; k <= H; ++k) acc = fmaf(wv[c][k], win[k][c], acc);
-                y[c] = silu_on ? silu(acc) : acc;
-            }
-            if constexpr (V == 1) {
-                Elem<T>::store(op + (int64_t)t * d_inner, y[0]);
-            } else {
-                *reinterpret_cast<uint2*>(op + (int64_t)t * d_inner) = pack_word<T>(y);
-            }
-#pragma unroll
-            for (int j = 0; j < H; ++j)
-#pragma unroll
-                for (int c = 0; c < V; ++c) win[j][c] = win[j + 1][c];
-        }
-    }
+    if (t0 >= H && t0 + kTileT <= L)
+        tile(std::integral_constant<bool, false>{});
+    else
+        tile(std::integral_constant<bool, true>{});
+
     if (state_out && t0 + kTileT >= L) {
 #pragma unroll
-        for (int c = 0; c < V; ++c)
+        for (int j = 0; j < H; ++j)
 #pragma unroll
-            for (int j = 0; j < H; ++j)
-                Elem<T>::store(state_out + (b * d_inner + d0 + c) * H + j, win[j][c]);
+            for (int p = 0; p < P; ++p) {
+                Elem<T>::store(state_out + (b * d_inner + d0 + 2 * p) * H + j, lo2(win[j][p]));
+                if (2 * p + 1 < V)
+                    Elem<T>::store(state_out + (b * d_inner + d0 + 2 * p + 1) * H + j,
+                                   hi2(win[j][p]));
+            }
     }
 }
 
@@ -169,7 +181,7 @@ conv1d_update_kernel(T* __restrict__ state, const T* __restrict__ x,
 #pragma unroll
     for (int k = 0; k < H; ++k) acc = fmaf(__ldg(w + d * KC + k), st[k], acc);
     acc = fmaf(__ldg(w + d * KC + H), cur, acc);
-    Elem<T>::store(out + i, silu_on ? silu(acc) : acc);
+    Elem<T>::store(out + i, silu_on ? silu_rcp(acc) : acc);  // same rounding as the prefill
 #pragma unroll
     for (int k = 0; k + 1 < H; ++k) Elem<T>::store(state + i * H + k, st[k + 1]);
     if (H > 0) Elem<T>::store(state + i * H + (H > 0 ? H - 1 : 0), cur);

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "msc_ptx.cuh"
+
 namespace msc {
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -78,6 +80,27 @@ __device__ __forceinline__ float zoh_gain(float x2, float dA, float delta, float
     const float small = delta * p;
     const float large = (dA - 1.0f) * iA;
     return fabsf(x2) < kZohSwitch ? small : large;
+}
+
+// 1/x on the MUFU pipe (PTX rcp.approx, flush-to-zero).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// silu with the reciprocal written out, z * (1 / (1 + e^-z)): the scalar
+// twin of silu2 (same operations per value), for kernels whose results must
+// match a paired evaluation bit for bit.
+__device__ __forceinline__ float silu_rcp(float z) {
+    return z * rcp_approx(ex2(-z * kLog2e) + 1.0f);
+}
+
+// silu of both halves of a pair: z / (1 + e^-z).
+__device__ __forceinline__ u64 silu2(u64 z2) {
+    const float z0 = lo2(z2), z1 = hi2(z2);
+    const u64 d = add2(pk2(ex2(-z0 * kLog2e), ex2(-z1 * kLog2e)), pk2(1.0f, 1.0f));
+    return mul2(z2, pk2(rcp_approx(lo2(d)), rcp_approx(hi2(d))));
 }
 
 // ---- typed element access -------------------------------------------------

@@ -84,12 +84,6 @@ template <> __device__ __forceinline__ float lds_elem<__nv_bfloat16>(const __nv_
                            << 16);
 }
 
-__device__ __forceinline__ float rcp_approx(float x) {
-    float y;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // softplus of both halves of a pair: max(x, 0) + log1p(e), e = e^-|x|,
 // log1p(e) = e * P(2e - 1) (the polynomial of log1p_unit, evaluated on pairs).
 __device__ __forceinline__ u64 softplus2(u64 x2) {
@@ -106,13 +100,6 @@ __device__ __forceinline__ u64 softplus2(u64 x2) {
     p = fma2(p, s, pk2(-0.14426334f, -0.14426334f));
     p = fma2(p, s, pk2(0.8109302f, 0.8109302f));
     return add2(pk2(fmaxf(x0, 0.0f), fmaxf(x1, 0.0f)), mul2(e, p));
-}
-
-// silu of both halves of a pair: z / (1 + e^-z).
-__device__ __forceinline__ u64 silu2(u64 z2) {
-    const float z0 = lo2(z2), z1 = hi2(z2);
-    const u64 d = add2(pk2(ex2(-z0 * kLog2e), ex2(-z1 * kLog2e)), pk2(1.0f, 1.0f));
-    return mul2(z2, pk2(rcp_approx(lo2(d)), rcp_approx(hi2(d))));
 }
 
 // Zero-order-hold input gain of a state pair: zoh_gain (msc_device.cuh) on
