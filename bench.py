@@ -616,21 +616,7 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
     def dstep(k):
         uu, dd, zz, BB, CC = pool[k % 8]
         msc.selective_state_update(state, uu, dd, A, BB, CC, Dv, zz, bias, out=out)
-    for k in range(10):
-        dstep(k)
-    torch.cuda.synchronize(dev)
-    msc.profile_read()
-    msc.profile_enable(True)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for k in range(steps):
-        dstep(k)
-    e1.record()
-    e1.synchronize()
-    msc.profile_enable(False)
-    _, kinds = msc.profile_read()
-    b2b_ms = e0.elapsed_time(e1) / steps
+    b2b_ms = back_to_back_ms(dstep, steps)   # no event pairs between the launches
     cold_ms = hook_cold_ms(dstep, "update")
     byt = 2 * Bb * Dd * Nn * 4 + 4 * Bb * Dd * 2 + 2 * Bb * Nn * 2 + Dd * Nn * 4 + 2 * Dd * 4
     upd = Bb * Dd * Nn
