@@ -75,6 +75,10 @@ class Oracle:
         lib.oracle_scan_fwd_segmented.restype = ctypes.c_int
         lib.oracle_scan_fwd_segmented.argtypes = ([dp] * 10 + [i64] * 5
                                                   + [ctypes.c_int])
+        lib.oracle_scan_fwd_trap.restype = ctypes.c_int
+        lib.oracle_scan_fwd_trap.argtypes = [dp] * 14 + [i64] * 4 + [ctypes.c_int]
+        lib.oracle_state_update_trap.restype = ctypes.c_int
+        lib.oracle_state_update_trap.argtypes = [dp] * 13 + [i64] * 3 + [ctypes.c_int]
         lib.oracle_causal_conv1d.restype = ctypes.c_int
         lib.oracle_causal_conv1d.argtypes = [dp] * 6 + [i64] * 4 + [ctypes.c_int] * 2
         lib.oracle_conv1d_update.restype = ctypes.c_int
@@ -147,6 +151,42 @@ class Oracle:
             d_state, int(bool(zoh)), int(nthreads))
         if rc != 0:
             raise ValueError("oracle_state_update rejected its sizes")
+        return st, out
+
+    def scan_fwd_trap(self, u, dt_raw, lam, A, B, C, D=None, z=None, dt_bias=None,
+                      h0=None, u_prev=None, B_prev=None, nthreads: int = 0):
+        """Exponential-trapezoid scan in fp64 -> (out, last_state).
+
+        lam: (batch, L, d_inner); u_prev: (batch, d_inner) and B_prev:
+        (batch, d_state) are the step before t = 0 (None: zero)."""
+        u, dt_raw, lam, A, B, C = map(_f64, (u, dt_raw, lam, A, B, C))
+        D, z, dt_bias, h0, u_prev, B_prev = map(_f64, (D, z, dt_bias, h0, u_prev, B_prev))
+        batch, L, d_inner, d_state = _dims(u, B)
+        out = np.zeros((batch, L, d_inner), dtype=np.float64)
+        last = np.zeros((batch, d_inner, d_state), dtype=np.float64)
+        rc = self.lib.oracle_scan_fwd_trap(
+            _ptr(u), _ptr(dt_raw), _ptr(lam), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+            _ptr(z), _ptr(dt_bias), _ptr(h0), _ptr(u_prev), _ptr(B_prev), _ptr(out),
+            _ptr(last), batch, L, d_inner, d_state, int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_scan_fwd_trap rejected its sizes")
+        return out, last
+
+    def state_update_trap(self, state, u_prev, B_prev, u, dt_raw, lam, A, B, C,
+                          D=None, z=None, dt_bias=None, nthreads: int = 0):
+        """One trapezoid decode token in fp64 -> (new_state, out)."""
+        st = np.array(state, dtype=np.float64, copy=True, order="C")
+        u_prev, B_prev, u, dt_raw, lam, A, B, C = map(
+            _f64, (u_prev, B_prev, u, dt_raw, lam, A, B, C))
+        D, z, dt_bias = map(_f64, (D, z, dt_bias))
+        batch, d_inner, d_state = st.shape
+        out = np.zeros((batch, d_inner), dtype=np.float64)
+        rc = self.lib.oracle_state_update_trap(
+            _ptr(st), _ptr(u_prev), _ptr(B_prev), _ptr(u), _ptr(dt_raw), _ptr(lam),
+            _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias), _ptr(out),
+            batch, d_inner, d_state, int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_state_update_trap rejected its sizes")
         return st, out
 
     def causal_conv1d(self, x, w, bias=None, state_in=None, silu: bool = True,
@@ -225,3 +265,11 @@ def causal_conv1d(*args, **kwargs):
 
 def conv1d_update(*args, **kwargs):
     return default().conv1d_update(*args, **kwargs)
+
+
+def scan_fwd_trap(*args, **kwargs):
+    return default().scan_fwd_trap(*args, **kwargs)
+
+
+def state_update_trap(*args, **kwargs):
+    return default().state_update_trap(*args, **kwargs)

@@ -33,7 +33,11 @@ different evaluation that the pages or plain mathematics fix:
     sections 3.2 and 5.2): against torch's own conv1d in fp64 (groups =
     channels, padding d_conv - 1, first L outputs), identity and pure-delay
     kernels, its conv state equal to convolving the concatenated sequence,
-    and decode steps equal to the prefill.
+    and decode steps equal to the prefill;
+  * the Mamba-3 exponential-trapezoid scan (Mamba series article, 2.1):
+    lambda = 1 is the Euler scan bit for bit, lambda = 0 is the Euler scan of
+    the inputs delayed one step, a constant-input closed form, split prefill
+    carrying the previous step's input, decode == scan.
 """
 from __future__ import annotations
 
@@ -438,6 +442,78 @@ def check_conv_decode_equals_prefill(orc):
     assert np.array_equal(st, st_ref)
 
 
+
+def check_trap_lambda_one_is_euler(orc):
+    x = _random_case(2, 30, 3, 4, seed=40)
+    lam = np.ones_like(x.u, dtype=np.float64)
+    y1, l1 = orc.scan_fwd_trap(x.u, x.dt_raw, lam, x.A, x.B, x.C, x.D, x.z, x.dt_bias)
+    y0, l0 = orc.scan_fwd(x.u, x.dt_raw, x.A, x.B, x.C, x.D, x.z, x.dt_bias)
+    assert np.array_equal(y1, y0) and np.array_equal(l1, l0)
+
+
+def check_trap_lambda_zero_is_delayed_euler(orc):
+    """lambda = 0 injects only B_{t-1} x_{t-1} with the step size of t: the
+    Euler scan of (u, B) delayed one step (the step before t = 0 given by
+    u_prev / B_prev), with delta and C not delayed (no skip, no gate)."""
+    x = _random_case(2, 25, 3, 4, seed=41, with_z=False)
+    rng = np.random.default_rng(42)
+    u_prev = rng.standard_normal((2, 3))
+    B_prev = rng.standard_normal((2, 4))
+    lam = np.zeros_like(x.u, dtype=np.float64)
+    y, last = orc.scan_fwd_trap(x.u, x.dt_raw, lam, x.A, x.B, x.C, None, None,
+                                x.dt_bias, u_prev=u_prev, B_prev=B_prev)
+    u_d = np.concatenate([u_prev[:, None, :], x.u[:, :-1]], axis=1)
+    B_d = np.concatenate([B_prev[:, None, :], x.B[:, :-1]], axis=1)
+    y0, l0 = orc.scan_fwd(u_d, x.dt_raw, x.A, B_d, x.C, None, None, x.dt_bias)
+    assert rel_l2(y, y0) < 1e-14 and rel_l2(last, l0) < 1e-14
+
+
+def check_trap_closed_form(orc):
+    """u = B = C = 1, N = 1, constant delta and lambda, nothing before t = 0:
+    h_0 = lambda*delta, h_t = a h_{t-1} + delta, so
+    h_t = a^t lambda delta + delta (1 - a^t) / (1 - a), a = exp(delta A)."""
+    batch, L, d_inner = 1, 40, 3
+    A = np.array([[-0.6], [-2.5], [-0.05]])
+    raw = np.array([0.2, -0.7, 1.1])
+    lamv = np.array([0.5, 0.3, 0.9])
+    u = np.ones((batch, L, d_inner))
+    dt_raw = np.broadcast_to(raw, (batch, L, d_inner)).copy()
+    lam = np.broadcast_to(lamv, (batch, L, d_inner)).copy()
+    ones = np.ones((batch, L, 1))
+    y, last = orc.scan_fwd_trap(u, dt_raw, lam, A, ones, ones, None, None, None)
+    dt = _softplus_np(raw)
+    a = np.exp(dt * A[:, 0])
+    t = np.arange(L, dtype=np.float64)[:, None]
+    h = a ** t * lamv * dt + dt * (1.0 - a ** t) / (1.0 - a)
+    assert rel_l2(y[0], h) < 1e-13, rel_l2(y[0], h)
+    assert rel_l2(last[0, :, 0], h[-1]) < 1e-13
+
+
+def check_trap_split_and_decode(orc):
+    """Two pieces (the second seeded with the first's last state and its last
+    step's u and B) equal one scan; decode tokens equal the scan."""
+    x = _random_case(2, 24, 3, 5, seed=43)
+    lam = np.random.default_rng(44).uniform(0.0, 1.0, x.u.shape)
+    y0, l0 = orc.scan_fwd_trap(x.u, x.dt_raw, lam, x.A, x.B, x.C, x.D, x.z, x.dt_bias)
+    k = 11
+    sl = lambda v, lo, hi: v[:, lo:hi]
+    ya, la = orc.scan_fwd_trap(sl(x.u, 0, k), sl(x.dt_raw, 0, k), sl(lam, 0, k), x.A,
+                               sl(x.B, 0, k), sl(x.C, 0, k), x.D, sl(x.z, 0, k), x.dt_bias)
+    yb, lb = orc.scan_fwd_trap(sl(x.u, k, 24), sl(x.dt_raw, k, 24), sl(lam, k, 24), x.A,
+                               sl(x.B, k, 24), sl(x.C, k, 24), x.D, sl(x.z, k, 24),
+                               x.dt_bias, h0=la, u_prev=x.u[:, k - 1], B_prev=x.B[:, k - 1])
+    assert rel_l2(np.concatenate([ya, yb], axis=1), y0) < 1e-14
+    assert rel_l2(lb, l0) < 1e-14
+    st = np.zeros_like(l0)
+    for t in range(24):
+        up = x.u[:, t - 1] if t else None
+        Bp = x.B[:, t - 1] if t else None
+        st, o = orc.state_update_trap(st, up, Bp, x.u[:, t], x.dt_raw[:, t], lam[:, t],
+                                      x.A, x.B[:, t], x.C[:, t], x.D, x.z[:, t], x.dt_bias)
+        assert np.array_equal(o, y0[:, t]), t
+    assert np.array_equal(st, l0)
+
+
 ALL_CHECKS = [
     check_softplus,
     check_silu,
@@ -457,4 +533,8 @@ ALL_CHECKS = [
     check_conv_special_kernels,
     check_conv_state,
     check_conv_decode_equals_prefill,
+    check_trap_lambda_one_is_euler,
+    check_trap_lambda_zero_is_delayed_euler,
+    check_trap_closed_form,
+    check_trap_split_and_decode,
 ]

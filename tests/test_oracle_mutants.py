@@ -62,6 +62,14 @@ MUTANTS = [
     ("conv_update_no_append", "if (H > 0) st[H - 1] = x[c];", ";"),
     ("conv_update_window_reversed", "acc += w[d * d_conv + k] * st[k];",
      "acc += w[d * d_conv + k] * st[H - 1 - k];"),
+    ("trap_no_previous_term", "(1.0 - lt) * delta * bx[n]", "0.0 * bx[n]"),
+    ("trap_weights_swapped", "(1.0 - lt) * delta * bx[n] + lt * delta * B[r + n] * ut",
+     "lt * delta * bx[n] + (1.0 - lt) * delta * B[r + n] * ut"),
+    ("trap_previous_not_advanced", "bx[n] = B[r + n] * ut;", ";"),
+    ("trap_previous_decayed", "(1.0 - lt) * delta * bx[n]", "(1.0 - lt) * delta * dA * bx[n]"),
+    ("trap_prev_input_ignored",
+     "bx[n] = (u_prev && B_prev) ? B_prev[b * d_state + n] * u_prev[c] : 0.0;\n        }",
+     "bx[n] = 0.0;\n        }"),
     ("segment_rerun_from_zero", "memcpy(hk, h, (size_t)d_state * sizeof(double));",
      "memset(hk, 0, (size_t)d_state * sizeof(double));"),
 ]
