@@ -217,6 +217,31 @@ msc_status msc_selective_scan_fwd_ex(
     msc_stream_t stream);
 
 /*
+ * The Mamba-3 exponential-trapezoid scan ("State space models and the Mamba
+ * series", section 2.1), in the S6 layout: the input term mixes the previous
+ * and the current step with a data-dependent lambda in [0, 1],
+ *     h_t = exp(delta_t*A) h_{t-1} + (1 - lambda_t)*delta_t * B_{t-1} u_{t-1}
+ *                                  + lambda_t*delta_t * B_t u_t
+ * (the formula as the page prints it: no decay on the t-1 term); the rest as
+ * msc_selective_scan_fwd (softplus step size, y = C.h + D*u, gate).
+ *   lam           : (batch, L, d_inner), `dtype`, values in [0, 1]; required
+ *   u_prev        : (batch, d_inner), `dtype`, nullable: u of the step before
+ *                   t = 0 (split prefill: the previous piece's last u)
+ *   B_prev        : (batch, d_state), `dtype`, nullable: its B; the t = 0
+ *                   previous-step term is zero unless both are given
+ *   h0, workspace : as msc_selective_scan_fwd_ex
+ * lambda = 1 everywhere gives the msc_selective_scan_fwd result bit for bit.
+ * Errors as msc_selective_scan_fwd; lam NULL is MSC_ERR_INVALID_ARG.
+ */
+msc_status msc_selective_scan_trap_fwd(
+    const void* u, const void* dt, const void* lam, const float* A,
+    const void* B, const void* C, const float* D, const void* z,
+    const float* dt_bias, const float* h0, const void* u_prev,
+    const void* B_prev, void* out, float* last_state, int64_t batch,
+    int64_t L, int64_t d_inner, int64_t d_state, msc_dtype dtype,
+    void* workspace, size_t workspace_bytes, msc_stream_t stream);
+
+/*
  * Single-token selective state update (decode).
  *   state         : (batch, d_inner, d_state) fp32, read and written in place
  *   u, dt, z, out : (batch, d_inner), `dtype`          z nullable: no gate
@@ -242,6 +267,19 @@ msc_status msc_selective_state_update_ex(
     const float* dt_bias, void* out, int64_t batch, int64_t d_inner,
     int64_t d_state, msc_dtype dtype, msc_discretization disc,
     msc_stream_t stream);
+
+/*
+ * One decode token of the exponential-trapezoid scan: u_prev / B_prev are
+ * the previous token's u (batch, d_inner) and B (batch, d_state) (nullable:
+ * zero term); lam (batch, d_inner).  Other arguments as
+ * msc_selective_state_update.
+ */
+msc_status msc_selective_state_update_trap(
+    float* state, const void* u_prev, const void* B_prev, const void* u,
+    const void* dt, const void* lam, const float* A, const void* B,
+    const void* C, const float* D, const void* z, const float* dt_bias,
+    void* out, int64_t batch, int64_t d_inner, int64_t d_state,
+    msc_dtype dtype, msc_stream_t stream);
 
 /*
  * Kernels never spin without bound: every wait for an asynchronous copy

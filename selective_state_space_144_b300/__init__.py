@@ -80,6 +80,11 @@ def load():
                                               + [st, st, vp, ctypes.c_size_t, vp])
     lib.msc_selective_state_update_ex.restype = st
     lib.msc_selective_state_update_ex.argtypes = [vp] * 10 + [i64] * 3 + [st, st, vp]
+    lib.msc_selective_scan_trap_fwd.restype = st
+    lib.msc_selective_scan_trap_fwd.argtypes = ([vp] * 14 + [i64] * 4
+                                                + [st, vp, ctypes.c_size_t, vp])
+    lib.msc_selective_state_update_trap.restype = st
+    lib.msc_selective_state_update_trap.argtypes = [vp] * 13 + [i64] * 3 + [st, vp]
     lib.msc_causal_conv1d_fwd.restype = st
     lib.msc_causal_conv1d_fwd.argtypes = [vp] * 6 + [i64] * 4 + [ctypes.c_int, st, vp]
     lib.msc_causal_conv1d_update.restype = st
@@ -288,6 +293,59 @@ def selective_state_update(state, u, dt, A, B, C, D=None, z=None,
         _ptr(out, "out", sdt, (batch, d_inner), dev),
         batch, d_inner, d_state, code, *extra, _stream(dev))
     _check(fn, st)
+    return out
+
+
+def selective_scan_trap_fwd(u, dt, lam, A, B, C, D=None, z=None, dt_bias=None,
+                            h0=None, u_prev=None, B_prev=None, out=None,
+                            last_state=None, workspace=None, return_last_state=True):
+    """Exponential-trapezoid scan on the GPU -> (out, last_state).
+
+    lam: (batch, L, d_inner) in u's dtype, values in [0, 1]; u_prev
+    (batch, d_inner) and B_prev (batch, d_state): the step before t = 0."""
+    lib = load()
+    p, out, last_state, dims, code, dev = _scan_args(
+        u, dt, A, B, C, D, z, dt_bias, out, last_state, return_last_state)
+    batch, L, d_inner, d_state = dims
+    sdt = u.dtype
+    wp = _ptr(workspace, "workspace", None, None, dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.msc_selective_scan_trap_fwd(
+        p["u"], p["dt"], _ptr(lam, "lam", sdt, (batch, L, d_inner), dev), p["A"], p["B"],
+        p["C"], p["D"], p["z"], p["dt_bias"],
+        _ptr(h0, "h0", _torch().float32, (batch, d_inner, d_state), dev),
+        _ptr(u_prev, "u_prev", sdt, (batch, d_inner), dev),
+        _ptr(B_prev, "B_prev", sdt, (batch, d_state), dev),
+        p["out"], p["last_state"], *dims, code, wp, wbytes, _stream(dev))
+    _check("msc_selective_scan_trap_fwd", st)
+    return out, last_state
+
+
+def selective_state_update_trap(state, u_prev, B_prev, u, dt, lam, A, B, C, D=None,
+                                z=None, dt_bias=None, out=None):
+    """One exponential-trapezoid decode token; updates ``state`` -> out."""
+    torch = _torch()
+    batch, d_inner, d_state = state.shape
+    dev, sdt, f32 = state.device, u.dtype, torch.float32
+    code = _dtype_code(u)
+    if out is None:
+        out = torch.empty((batch, d_inner), dtype=sdt, device=dev)
+    st = load().msc_selective_state_update_trap(
+        _ptr(state, "state", f32, (batch, d_inner, d_state), dev),
+        _ptr(u_prev, "u_prev", sdt, (batch, d_inner), dev),
+        _ptr(B_prev, "B_prev", sdt, (batch, d_state), dev),
+        _ptr(u, "u", sdt, (batch, d_inner), dev),
+        _ptr(dt, "dt", sdt, (batch, d_inner), dev),
+        _ptr(lam, "lam", sdt, (batch, d_inner), dev),
+        _ptr(A, "A", f32, (d_inner, d_state), dev),
+        _ptr(B, "B", sdt, (batch, d_state), dev),
+        _ptr(C, "C", sdt, (batch, d_state), dev),
+        _ptr(D, "D", f32, (d_inner,), dev),
+        _ptr(z, "z", sdt, (batch, d_inner), dev),
+        _ptr(dt_bias, "dt_bias", f32, (d_inner,), dev),
+        _ptr(out, "out", sdt, (batch, d_inner), dev),
+        batch, d_inner, d_state, code, _stream(dev))
+    _check("msc_selective_state_update_trap", st)
     return out
 
 

@@ -52,7 +52,8 @@ ScanCheck check_scan(const void* u, const void* dt, const float* A, const void* 
                      const void* C, const float* D, const void* z, const float* dt_bias,
                      void* out, float* last_state, int64_t batch, int64_t L,
                      int64_t d_inner, int64_t d_state, msc_dtype dtype,
-                     const float* h0 = nullptr) {
+                     const float* h0 = nullptr, const void* lam = nullptr,
+                     const void* u_prev = nullptr, const void* B_prev = nullptr) {
     ScanCheck r{};
     r.st = MSC_OK;
     if (dtype != MSC_F32 && dtype != MSC_BF16) {
@@ -84,7 +85,7 @@ ScanCheck check_scan(const void* u, const void* dt, const float* A, const void* 
         }
     }
     const size_t es = elem_size(dtype);
-    const void* typed[] = {u, dt, B, C, z, out};
+    const void* typed[] = {u, dt, B, C, z, out, lam, u_prev, B_prev};
     for (const void* p : typed)
         if (p && !aligned(p, es)) {
             r.st = MSC_ERR_ALIGNMENT;
@@ -96,7 +97,8 @@ ScanCheck check_scan(const void* u, const void* dt, const float* A, const void* 
             r.st = MSC_ERR_ALIGNMENT;
             return r;
         }
-    if (g_scan_path == 0 && L > 0 && msc::tma_scan_supported(d_state, d_inner, dtype, u, dt, z)) {
+    if (g_scan_path == 0 && L > 0 &&
+        msc::tma_scan_supported(d_state, d_inner, dtype, u, dt, z, lam)) {
         // fp32 B/C copies unless fp32 inputs already suit 16-byte TMA boxes
         const bool need_bc = dtype == MSC_BF16 || !aligned(B, 16) || !aligned(C, 16);
         r.plan = msc::make_tma_plan(batch, L, d_inner, d_state, sm_count(), g_force_chunks,
@@ -167,9 +169,10 @@ static msc_status run_scan(const void* u, const void* dt, const float* A, const 
                            const float* dt_bias, void* out, float* last_state, int64_t batch,
                            int64_t L, int64_t d_inner, int64_t d_state, msc_dtype dtype,
                            void* ws, size_t ws_bytes, bool own_ws, msc_stream_t stream,
-                           const float* h0 = nullptr, int zoh = 0) {
+                           const float* h0 = nullptr, int zoh = 0, const void* lam = nullptr,
+                           const void* u_prev = nullptr, const void* B_prev = nullptr) {
     ScanCheck c = check_scan(u, dt, A, B, C, D, z, dt_bias, out, last_state, batch, L, d_inner,
-                             d_state, dtype, h0);
+                             d_state, dtype, h0, lam, u_prev, B_prev);
     if (c.st != MSC_OK) return c.st;
     if (batch == 0 || d_inner == 0) return MSC_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -185,6 +188,7 @@ static msc_status run_scan(const void* u, const void* dt, const float* A, const 
     msc::ScanArgs a{};
     a.u = u; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.dt_bias = dt_bias;
     a.out = out; a.last_state = last_state; a.h0 = h0; a.zoh = zoh;
+    a.trap = lam != nullptr; a.lam = lam; a.u_prev = u_prev; a.B_prev = B_prev;
     const size_t half = c.plan.ws_carry / 2 / sizeof(float);
     a.ws_a = c.plan.ws_carry ? static_cast<float*>(w) : nullptr;
     a.ws_b = c.plan.ws_carry ? static_cast<float*>(w) + half : nullptr;
@@ -287,6 +291,20 @@ msc_status msc_selective_scan_fwd_ex(const void* u, const void* dt, const float*
                     disc == MSC_DISC_ZOH ? 1 : 0);
 }
 
+msc_status msc_selective_scan_trap_fwd(const void* u, const void* dt, const void* lam,
+                                       const float* A, const void* B, const void* C,
+                                       const float* D, const void* z, const float* dt_bias,
+                                       const float* h0, const void* u_prev, const void* B_prev,
+                                       void* out, float* last_state, int64_t batch, int64_t L,
+                                       int64_t d_inner, int64_t d_state, msc_dtype dtype,
+                                       void* workspace, size_t workspace_bytes,
+                                       msc_stream_t stream) {
+    if (!lam && batch > 0 && L > 0 && d_inner > 0) return MSC_ERR_INVALID_ARG;
+    return run_scan(u, dt, A, B, C, D, z, dt_bias, out, last_state, batch, L, d_inner, d_state,
+                    dtype, workspace, workspace_bytes, workspace == nullptr, stream, h0, 0,
+                    L > 0 ? lam : nullptr, u_prev, B_prev);
+}
+
 msc_status msc_selective_scan_workspace_size(int64_t batch, int64_t L, int64_t d_inner,
                                              int64_t d_state, msc_dtype dtype, size_t* bytes) {
     if (!bytes) return MSC_ERR_INVALID_ARG;
@@ -318,7 +336,9 @@ msc_status msc_selective_scan_workspace_size(int64_t batch, int64_t L, int64_t d
 static msc_status run_update(float* state, const void* u, const void* dt, const float* A,
                              const void* B, const void* C, const float* D, const void* z,
                              const float* dt_bias, void* out, int64_t batch, int64_t d_inner,
-                             int64_t d_state, msc_dtype dtype, int zoh, msc_stream_t stream) {
+                             int64_t d_state, msc_dtype dtype, int zoh, msc_stream_t stream,
+                             const void* lam = nullptr, const void* u_prev = nullptr,
+                             const void* B_prev = nullptr) {
     if (dtype != MSC_F32 && dtype != MSC_BF16) return MSC_ERR_INVALID_ARG;
     if (batch < 0 || d_inner < 0 || d_state < 0) return MSC_ERR_INVALID_ARG;
     if (d_state < 1 || d_state > 64) return MSC_ERR_UNSUPPORTED;
@@ -333,7 +353,7 @@ static msc_status run_update(float* state, const void* u, const void* dt, const 
         std::numeric_limits<int>::max())
         return MSC_ERR_UNSUPPORTED;
     const size_t es = elem_size(dtype);
-    const void* typed[] = {u, dt, B, C, z, out};
+    const void* typed[] = {u, dt, B, C, z, out, lam, u_prev, B_prev};
     for (const void* p : typed)
         if (p && !aligned(p, es)) return MSC_ERR_ALIGNMENT;
     const void* f32[] = {state, A, D, dt_bias};
@@ -344,6 +364,7 @@ static msc_status run_update(float* state, const void* u, const void* dt, const 
     a.dt_bias = dt_bias; a.out = out; a.batch = batch; a.d_inner = d_inner; a.N = d_state;
     a.vec = (d_state % 4 == 0) && aligned(state, 16) && aligned(B, 4 * es) && aligned(C, 4 * es);
     a.zoh = zoh;
+    a.trap = lam != nullptr; a.lam = lam; a.u_prev = u_prev; a.B_prev = B_prev;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     msc::ProfileMark m = msc::profile_begin(s, MSC_PROF_UPDATE);
     cudaError_t e = msc::launch_state_update(a, dtype, s);
@@ -370,6 +391,18 @@ msc_status msc_selective_state_update_ex(float* state, const void* u, const void
     if (disc != MSC_DISC_EULER && disc != MSC_DISC_ZOH) return MSC_ERR_INVALID_ARG;
     return run_update(state, u, dt, A, B, C, D, z, dt_bias, out, batch, d_inner, d_state, dtype,
                       disc == MSC_DISC_ZOH ? 1 : 0, stream);
+}
+
+msc_status msc_selective_state_update_trap(float* state, const void* u_prev, const void* B_prev,
+                                           const void* u, const void* dt, const void* lam,
+                                           const float* A, const void* B, const void* C,
+                                           const float* D, const void* z, const float* dt_bias,
+                                           void* out, int64_t batch, int64_t d_inner,
+                                           int64_t d_state, msc_dtype dtype,
+                                           msc_stream_t stream) {
+    if (!lam && batch > 0 && d_inner > 0) return MSC_ERR_INVALID_ARG;
+    return run_update(state, u, dt, A, B, C, D, z, dt_bias, out, batch, d_inner, d_state, dtype,
+                      0, stream, lam, u_prev, B_prev);
 }
 
 static msc_status run_conv(const void* x, const float* w, const float* bias,

@@ -24,6 +24,10 @@ struct ScanArgs {
     float* last_state;
     const float* h0;   // initial state (batch, d_inner, N) or nullptr for zero
     int zoh;           // 1: zero-order-hold input matrix, 0: delta*B
+    int trap;          // 1: exponential-trapezoid input (lam, u_prev, B_prev below)
+    const void* lam;   // trapezoid mixing coefficient (batch, L, d_inner), storage dtype
+    const void* u_prev;  // u of the step before t = 0 (batch, d_inner) or nullptr
+    const void* B_prev;  // B of the step before t = 0 (batch, N) or nullptr
     float* ws_a;       // chunk transfer coefficients, (batch, K-1, d_inner, N)
     float* ws_b;       // chunk end states from zero,   (batch, K-1, d_inner, N)
     int64_t batch, L, d_inner, N;
@@ -60,6 +64,10 @@ struct UpdateArgs {
     int64_t batch, d_inner, N;
     int vec;           // 1: state and B/C rows can be read 4 elements at a time
     int zoh;           // 1: zero-order-hold input matrix, 0: delta*B
+    int trap;          // 1: exponential-trapezoid input
+    const void* lam;   // (batch, d_inner) trapezoid mixing coefficient
+    const void* u_prev;  // previous token's u (batch, d_inner) or nullptr
+    const void* B_prev;  // previous token's B (batch, N) or nullptr
 };
 
 // The causal depthwise conv1d before the scan (conv1d.cu).  For the decode
@@ -106,7 +114,7 @@ cudaError_t launch_scan(const ScanArgs& a, const ScanPlan& p, msc_dtype dtype,
 // TMA path (scan_tma.cu): supported shapes, time-tile length, launch, and
 // the device word its bounded waits set when a copy never lands.
 bool tma_scan_supported(int64_t N, int64_t d_inner, msc_dtype dtype, const void* u,
-                        const void* dt, const void* z);
+                        const void* dt, const void* z, const void* lam = nullptr);
 int tma_scan_tile(int64_t N);
 cudaError_t launch_scan_tma(const ScanArgs& a, const ScanPlan& p, msc_dtype dtype, float* Bf,
                             float* Cf, cudaStream_t stream);

@@ -76,6 +76,24 @@ scan_chunk_kernel(ScanArgs a, int kgrid) {
     T* op = static_cast<T*>(a.out) + base;
     const T* Bp = static_cast<const T*>(a.B) + b * a.L * N;
     const T* Cp = static_cast<const T*>(a.C) + b * a.L * N;
+    const T* lamp = a.trap ? static_cast<const T*>(a.lam) + base : nullptr;
+
+    // exponential trapezoid: B*u of the step before the current one, seeded
+    // from the step before the chunk (or the caller's u_prev / B_prev)
+    float bx[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (a.trap && (t0 > 0 || (a.u_prev && a.B_prev))) {
+        float Bq[4];
+        float uq;
+        if (t0 > 0) {
+            uq = Elem<T>::load(up + (t0 - 1) * a.d_inner);
+            load_row4<T, false>(Bp + (t0 - 1) * N, n0, N, Bq);
+        } else {
+            uq = Elem<T>::load(static_cast<const T*>(a.u_prev) + b * a.d_inner + d);
+            load_row4<T, false>(static_cast<const T*>(a.B_prev) + b * N, n0, N, Bq);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) bx[j] = uq * Bq[j];
+    }
 
 #pragma unroll 2
     for (int64_t t = t0; t < t1; ++t) {
@@ -86,6 +104,22 @@ scan_chunk_kernel(ScanArgs a, int kgrid) {
         const float du = delta * uu;
         float Bv[4];
         load_row4<T, VEC>(Bp + t * N, n0, N, Bv);
+        // input term of state j: delta*B*u, the zero-order hold's gain*u*B,
+        // or the trapezoid's (1-lambda)*delta*(B*u)_{t-1} + (lambda*delta*u)*B
+        float tra = 0.0f, trc = 0.0f;
+        if (a.trap) {
+            const float lt = Elem<T>::load(lamp + off);
+            tra = (1.0f - lt) * delta;
+            trc = (lt * delta) * uu;
+        }
+        auto inject = [&](int j, float x2, float dA) {
+            if (a.trap) {
+                const float v = fmaf(tra, bx[j], trc * Bv[j]);
+                bx[j] = uu * Bv[j];
+                return v;
+            }
+            return a.zoh ? zoh_gain(x2, dA, delta, iA[j]) * uu * Bv[j] : du * Bv[j];
+        };
         if (OUTPUT) {
             float Cv[4];
             load_row4<T, VEC>(Cp + t * N, n0, N, Cv);
@@ -94,9 +128,7 @@ scan_chunk_kernel(ScanArgs a, int kgrid) {
             for (int j = 0; j < 4; ++j) {
                 const float x2 = delta * A2[j];
                 const float dA = ex2(x2);
-                const float inj = a.zoh ? zoh_gain(x2, dA, delta, iA[j]) * uu * Bv[j]
-                                        : du * Bv[j];
-                h[j] = fmaf(dA, h[j], inj);
+                h[j] = fmaf(dA, h[j], inject(j, x2, dA));
                 y = fmaf(Cv[j], h[j], y);
             }
 #pragma unroll
@@ -112,9 +144,7 @@ scan_chunk_kernel(ScanArgs a, int kgrid) {
             for (int j = 0; j < 4; ++j) {
                 const float x2 = delta * A2[j];
                 const float dA = ex2(x2);
-                const float inj = a.zoh ? zoh_gain(x2, dA, delta, iA[j]) * uu * Bv[j]
-                                        : du * Bv[j];
-                h[j] = fmaf(dA, h[j], inj);
+                h[j] = fmaf(dA, h[j], inject(j, x2, dA));
                 P[j] *= dA;
             }
         }

@@ -63,15 +63,22 @@ constexpr int kOct = 8;  // steps per iteration
 // channels and the core's 16-byte loads (2 steps) hit distinct banks.
 constexpr int kDUStride = 10;
 
-template <typename T, int G, int NS, int TT, int S>
+// Shared memory of one CTA: S stages of [u | dt | z | (lambda) | B | C]
+// tiles, the (delta, delta*u) buffers (trapezoid: two sets), the barriers.
+template <typename T, int G, int NS, int TT, int S, bool TRAP = false>
 struct TmaLayout {
     static constexpr int CPW = 32 / G;                  // channels per warp
     static constexpr int N = G * NS;
-    static constexpr int kX = TT * CPW * (int)sizeof(T); // one of u / dt / z per stage
+    static constexpr int NX = TRAP ? 4 : 3;             // [TT x CPW] tiles per stage
+    static constexpr int kX = TT * CPW * (int)sizeof(T); // one of u / dt / z / lambda
     static constexpr int kBC = TT * N * 4;              // one of B / C (fp32) per stage
-    static constexpr int kStage = 3 * kX + 2 * kBC;
+    static constexpr int kLam = 3 * kX;                 // lambda tile (trapezoid)
+    static constexpr int kBoff = NX * kX;               // B tile
+    static constexpr int kCoff = kBoff + kBC;           // C tile
+    static constexpr int kStage = NX * kX + 2 * kBC;
     static constexpr int kDU = S * kStage;              // float2 [2][CPW][kDUStride]
-    static constexpr int kBar = kDU + 2 * CPW * kDUStride * 8;
+    static constexpr int kDUsz = 2 * CPW * kDUStride * 8;
+    static constexpr int kBar = kDU + (TRAP ? 2 : 1) * kDUsz;
     static constexpr int kTotal = kBar + S * 8;
     static_assert(kX % 128 == 0 && kBC % 128 == 0, "TMA destinations must stay 128B aligned");
     static_assert(TT % kOct == 0, "tiles hold whole octets");
@@ -164,16 +171,17 @@ __device__ __forceinline__ void reduce_scatter(const float (&y)[kOct], int lane,
 }
 
 // Per-(step, channel) prologue of one octet: delta = softplus(dt + dt_bias)
-// and delta*u (ZOH: u, the gain being per state) for steps g + G*m
-// (m < 8/G) of the octet whose first row is `row0` of the tile at `stage`;
-// written to `dst` (the lane's channel row of one sDU buffer, indexed by
-// step) for the core.  The u of those steps is returned as pairs for the D*u
+// and delta*u (ZOH: u, the gain being per state; trapezoid: lambda*delta*u,
+// with ((1-lambda)*delta, u) in `dst2`) for steps g + G*m (m < 8/G) of the
+// octet whose first row is `row0` of the tile at `stage`; written to `dst`
+// (the lane's channel row of one sDU buffer, indexed by step) for the core.  The u of those steps is returned as pairs for the D*u
 // term.  MASK: steps at or past `nsteps` get delta = 0 and no input (the
 // state passes through).
-template <typename T, int G, int TT, bool MASK, bool ZOH>
+template <typename T, int G, int TT, bool MASK, int DISC>
 __device__ __forceinline__ void octet_prologue(const unsigned char* stage, int row0, int lane_x,
-                                               float2* dst, u64 bias2, int s0_first,
-                                               int nsteps, u64 (&uu)[kOct / G / 2]) {
+                                               float2* dst, float2* dst2, u64 bias2,
+                                               int s0_first, int nsteps,
+                                               u64 (&uu)[kOct / G / 2]) {
     constexpr int CPW = 32 / G;
     constexpr int PPL = kOct / G / 2;
     const T* sx = reinterpret_cast<const T*>(stage) + row0 * CPW + lane_x;
@@ -184,25 +192,69 @@ __device__ __forceinline__ void octet_prologue(const unsigned char* stage, int r
         const u64 x =
             add2(pk2(lds_elem<T>(sx + TT * CPW + r0), lds_elem<T>(sx + TT * CPW + r1)), bias2);
         const u64 dl = softplus2(x);
-        const u64 du = ZOH ? uu[p] : mul2(dl, uu[p]);
+        u64 du, tra = 0;
+        if constexpr (DISC == 2) {  // trapezoid: (lambda*delta)*u here, (1-lambda)*delta in dst2
+            const u64 lt =
+                pk2(lds_elem<T>(sx + 3 * TT * CPW + r0), lds_elem<T>(sx + 3 * TT * CPW + r1));
+            du = mul2(mul2(lt, dl), uu[p]);
+            tra = mul2(fma2(lt, pk2(-1.0f, -1.0f), pk2(1.0f, 1.0f)), dl);
+        } else if constexpr (DISC == 1) {
+            du = uu[p];
+        } else {
+            du = mul2(dl, uu[p]);
+        }
         if (MASK) {
             const int s0 = s0_first + G * (2 * p);
             const bool v0 = s0 < nsteps, v1 = s0 + G < nsteps;
             dst[(2 * p) * G] = make_float2(v0 ? lo2(dl) : 0.0f, v0 ? lo2(du) : 0.0f);
             dst[(2 * p + 1) * G] = make_float2(v1 ? hi2(dl) : 0.0f, v1 ? hi2(du) : 0.0f);
+            if constexpr (DISC == 2) {
+                dst2[(2 * p) * G] = make_float2(v0 ? lo2(tra) : 0.0f, v0 ? lo2(uu[p]) : 0.0f);
+                dst2[(2 * p + 1) * G] = make_float2(v1 ? hi2(tra) : 0.0f, v1 ? hi2(uu[p]) : 0.0f);
+            }
         } else {
             dst[(2 * p) * G] = make_float2(lo2(dl), lo2(du));
             dst[(2 * p + 1) * G] = make_float2(hi2(dl), hi2(du));
+            if constexpr (DISC == 2) {
+                dst2[(2 * p) * G] = make_float2(lo2(tra), lo2(uu[p]));
+                dst2[(2 * p + 1) * G] = make_float2(hi2(tra), hi2(uu[p]));
+            }
         }
     }
 }
 
-template <typename T, int G, int NS, int TT, int S, bool ZOH>
+// Exponential trapezoid: B*u of the step before a chunk for the lane's NS
+// states -- step tc0 - 1 of the caller's u and B, or, for the first chunk,
+// the caller's u_prev / B_prev (zero when absent).
+template <typename T, int NS>
+__device__ __forceinline__ void trap_seed(const ScanArgs& a, int b, int64_t d, int n0,
+                                          int64_t tc0, u64 (&bx)[NS / 2]) {
+    const T* ur;
+    const T* Br;
+    if (tc0 > 0) {
+        ur = static_cast<const T*>(a.u) + ((int64_t)b * a.L + tc0 - 1) * a.d_inner + d;
+        Br = static_cast<const T*>(a.B) + ((int64_t)b * a.L + tc0 - 1) * a.N + n0;
+    } else if (a.u_prev && a.B_prev) {
+        ur = static_cast<const T*>(a.u_prev) + (int64_t)b * a.d_inner + d;
+        Br = static_cast<const T*>(a.B_prev) + (int64_t)b * a.N + n0;
+    } else {
+        return;
+    }
+    const float uq = Elem<T>::load(ur);
+#pragma unroll
+    for (int i = 0; i < NS / 2; ++i)
+        bx[i] = pk2(uq * Elem<T>::load(Br + 2 * i), uq * Elem<T>::load(Br + 2 * i + 1));
+}
+
+template <typename T, int G, int NS, int TT, int S, int DISC>
 __global__ void __launch_bounds__(32)
 scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dt,
                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
-                const __grid_constant__ CUtensorMap tm_C, const ScanArgs a, const int kgrid) {
-    using Lay = TmaLayout<T, G, NS, TT, S>;
+                const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_lam,
+                const ScanArgs a, const int kgrid) {
+    constexpr bool ZOH = DISC == 1, TRAP = DISC == 2;
+    using Lay = TmaLayout<T, G, NS, TT, S, TRAP>;
+    constexpr int kD2 = Lay::kDUsz / 8;  // second (delta) buffer, trapezoid only
     constexpr int CPW = Lay::CPW;
     constexpr int N = Lay::N;
     constexpr int NP = NS / 2;         // state pairs per lane
@@ -226,7 +278,8 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const int nsteps = (int)min(a.chunk, a.L - tc0);
     const int ntiles = (nsteps + TT - 1) / TT;
     const bool has_z = a.z != nullptr;
-    const uint32_t tx_bytes = (uint32_t)((2 + (has_z ? 1 : 0)) * Lay::kX + 2 * Lay::kBC);
+    const uint32_t tx_bytes =
+        (uint32_t)((2 + (has_z ? 1 : 0) + (TRAP ? 1 : 0)) * Lay::kX + 2 * Lay::kBC);
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + Lay::kBar;
@@ -238,6 +291,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         prefetch_tensormap(&tm_B);
         prefetch_tensormap(&tm_C);
         if (has_z) prefetch_tensormap(&tm_z);
+        if (TRAP) prefetch_tensormap(&tm_lam);
     }
     __syncwarp();
 
@@ -249,8 +303,9 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         tma_load_3d(st, &tm_u, bar, d0, tt, b);
         tma_load_3d(st + Lay::kX, &tm_dt, bar, d0, tt, b);
         if (has_z) tma_load_3d(st + 2 * Lay::kX, &tm_z, bar, d0, tt, b);
-        tma_load_3d(st + 3 * Lay::kX, &tm_B, bar, 0, tt, b);
-        tma_load_3d(st + 3 * Lay::kX + Lay::kBC, &tm_C, bar, 0, tt, b);
+        if (TRAP) tma_load_3d(st + Lay::kLam, &tm_lam, bar, d0, tt, b);
+        tma_load_3d(st + Lay::kBoff, &tm_B, bar, 0, tt, b);
+        tma_load_3d(st + Lay::kCoff, &tm_C, bar, 0, tt, b);
     };
     int issued = min(S, ntiles);
     if (lane == 0)
@@ -277,6 +332,11 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             hp[i] = pk2(v.x, v.y);
         }
     }
+    // trapezoid: B*u of the step before the chunk (or the caller's u_prev, B_prev)
+    u64 bxp[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i) bxp[i] = pk2(0.0f, 0.0f);
+    if (TRAP) trap_seed<T, NS>(a, b, d, n0, tc0, bxp);
 
     float2* const sDU = reinterpret_cast<float2*>(smem + Lay::kDU);
     const u64 bias2 = pk2(bias, bias);
@@ -289,8 +349,9 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 #pragma unroll
     for (int p = 0; p < PPL; ++p) u_cur[p] = u_nxt[p] = pk2(0.0f, 0.0f);
     if (ok && ntiles > 0)
-        octet_prologue<T, G, TT, true, ZOH>(smem, 0, lane_x, sDU + ch * kDUStride + g, bias2, g,
-                                       nsteps, u_cur);
+        octet_prologue<T, G, TT, true, DISC>(smem, 0, lane_x, sDU + ch * kDUStride + g,
+                                             sDU + ch * kDUStride + g + kD2, bias2, g, nsteps,
+                                             u_cur);
     __syncwarp();
 
     const u64 D2 = pk2(Dd, Dd);
@@ -305,8 +366,8 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         constexpr bool FULL = decltype(full_tag)::value;
         const unsigned char* st = smem + st_idx * Lay::kStage;
         const int nxt_idx = st_idx + 1 == S ? 0 : st_idx + 1;
-        const float* sB0 = reinterpret_cast<const float*>(st + 3 * Lay::kX) + n0;
-        const float* sC0 = reinterpret_cast<const float*>(st + 3 * Lay::kX + Lay::kBC) + n0;
+        const float* sB0 = reinterpret_cast<const float*>(st + Lay::kBoff) + n0;
+        const float* sC0 = reinterpret_cast<const float*>(st + Lay::kCoff) + n0;
         const T* sz0 = reinterpret_cast<const T*>(st + 2 * Lay::kX) + lane_x;
 #pragma unroll
         for (int oo = 0; oo < OPT; ++oo) {
@@ -315,6 +376,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             // (1) the state updates of this octet
             const float4* sd =
                 reinterpret_cast<const float4*>(sDU + ((oo & 1) * CPW + ch) * kDUStride);
+            [[maybe_unused]] const float4* sd2 = sd + kD2 / 2;  // trapezoid: ((1-lambda)*delta, u)
             const float* sB = sB0 + kOct * oo * N;
             const float* sC = sC0 + kOct * oo * N;
             float yv[kOct];
@@ -323,6 +385,13 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 const float4 v2 = sd[j >> 1];  // steps j & ~1 and (j & ~1) + 1
                 const float vdl = (j & 1) ? v2.z : v2.x, vdu = (j & 1) ? v2.w : v2.y;
                 const u64 dl2 = pk2(vdl, vdl), du2 = pk2(vdu, vdu);
+                [[maybe_unused]] u64 tr2 = 0, ux2 = 0;
+                if constexpr (TRAP) {
+                    const float4 w2 = sd2[j >> 1];
+                    const float vtr = (j & 1) ? w2.z : w2.x, vux = (j & 1) ? w2.w : w2.y;
+                    tr2 = pk2(vtr, vtr);
+                    ux2 = pk2(vux, vux);
+                }
                 u64 Bp[NP], Cp[NP];
                 if constexpr (NP == 1) {  // 2 states: one 8-byte read each
                     Bp[0] = *reinterpret_cast<const u64*>(sB + j * N);
@@ -345,8 +414,14 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 for (int i2 = 0; i2 < NP; ++i2) {
                     const u64 x2 = mul2(dl2, A2[i2]);
                     const u64 dA = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
-                    hp[i2] = fma2(dA, hp[i2],
-                                  injection2<ZOH>(x2, dA, dl2, du2, iA2[i2], Bp[i2]));
+                    u64 inj;
+                    if constexpr (TRAP) {
+                        inj = fma2(tr2, bxp[i2], mul2(du2, Bp[i2]));
+                        bxp[i2] = mul2(ux2, Bp[i2]);
+                    } else {
+                        inj = injection2<ZOH>(x2, dA, dl2, du2, iA2[i2], Bp[i2]);
+                    }
+                    hp[i2] = fma2(dA, hp[i2], inj);
                     y2 = fma2(Cp[i2], hp[i2], y2);
                 }
                 yv[j] = lo2(y2) + hi2(y2);
@@ -355,7 +430,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             //     octet's (next tile: wait for it first)
             float2* const dnx = sDU + (((oo + 1) & 1) * CPW + ch) * kDUStride + g;
             if (oo + 1 < OPT) {
-                octet_prologue<T, G, TT, !FULL, ZOH>(st, kOct * (oo + 1), lane_x, dnx, bias2,
+                octet_prologue<T, G, TT, !FULL, DISC>(st, kOct * (oo + 1), lane_x, dnx, dnx + kD2, bias2,
                                                 sb + kOct + g, nsteps, u_nxt);
             } else if (i + 1 < ntiles) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * nxt_idx,
@@ -364,10 +439,10 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 waited = i + 2;
                 const unsigned char* stn = smem + nxt_idx * Lay::kStage;
                 if ((i + 2) * TT <= nsteps)
-                    octet_prologue<T, G, TT, false, ZOH>(stn, 0, lane_x, dnx, bias2, sb + kOct + g,
+                    octet_prologue<T, G, TT, false, DISC>(stn, 0, lane_x, dnx, dnx + kD2, bias2, sb + kOct + g,
                                                     nsteps, u_nxt);
                 else
-                    octet_prologue<T, G, TT, true, ZOH>(stn, 0, lane_x, dnx, bias2, sb + kOct + g,
+                    octet_prologue<T, G, TT, true, DISC>(stn, 0, lane_x, dnx, dnx + kD2, bias2, sb + kOct + g,
                                                    nsteps, u_nxt);
             }
             // (3) outputs of steps g + G*m of channel ch
@@ -441,12 +516,15 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 // prologue as scan_tma_kernel; only u, dt and B are loaded.
 constexpr float kSummaryCut = 9.094947e-13f;  // 2^-40
 
-template <typename T, int G, int NS, int TT, int S, bool ZOH>
+template <typename T, int G, int NS, int TT, int S, int DISC>
 __global__ void __launch_bounds__(32)
 scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
                     const __grid_constant__ CUtensorMap tm_dt,
-                    const __grid_constant__ CUtensorMap tm_B, const ScanArgs a, const int kgrid) {
-    using Lay = TmaLayout<T, G, NS, TT, S>;
+                    const __grid_constant__ CUtensorMap tm_B,
+                    const __grid_constant__ CUtensorMap tm_lam, const ScanArgs a, const int kgrid) {
+    constexpr bool ZOH = DISC == 1, TRAP = DISC == 2;
+    using Lay = TmaLayout<T, G, NS, TT, S, TRAP>;
+    constexpr int kD2 = Lay::kDUsz / 8;
     constexpr int CPW = Lay::CPW;
     constexpr int N = Lay::N;
     constexpr int NP = NS / 2;
@@ -467,7 +545,7 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
     const int64_t d = d0 + ch;
     const int64_t tc0 = (int64_t)k * a.chunk;
     const int ntiles = (int)(a.chunk / TT);  // summarised chunks are whole tiles
-    const uint32_t tx_bytes = (uint32_t)(2 * Lay::kX + Lay::kBC);
+    const uint32_t tx_bytes = (uint32_t)((TRAP ? 3 : 2) * Lay::kX + Lay::kBC);
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + Lay::kBar;
@@ -477,6 +555,7 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
         prefetch_tensormap(&tm_u);
         prefetch_tensormap(&tm_dt);
         prefetch_tensormap(&tm_B);
+        if (TRAP) prefetch_tensormap(&tm_lam);
     }
     __syncwarp();
     // r-th tile in walking order = tile ntiles-1-r of the chunk, stage r % S
@@ -487,7 +566,8 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
         mbar_expect_tx(bar, tx_bytes);
         tma_load_3d(st, &tm_u, bar, d0, tt, b);
         tma_load_3d(st + Lay::kX, &tm_dt, bar, d0, tt, b);
-        tma_load_3d(st + 3 * Lay::kX, &tm_B, bar, 0, tt, b);
+        if (TRAP) tma_load_3d(st + Lay::kLam, &tm_lam, bar, d0, tt, b);
+        tma_load_3d(st + Lay::kBoff, &tm_B, bar, 0, tt, b);
     };
     int issued = min(S, ntiles);
     if (lane == 0)
@@ -496,6 +576,7 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
     const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
     const u64 bias2 = pk2(bias, bias);
     u64 A2[NP], iA2[NP], Pp[NP], bp[NP];
+    u64 pend[NP];  // trapezoid: P * (1-lambda)*delta of the step after, awaiting B*u
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
         const float* Ar = a.A + d * N + n0 + 2 * i;
@@ -503,6 +584,7 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
         A2[i] = pk2(a0 * kLog2e, a1 * kLog2e);
         iA2[i] = ZOH ? pk2(1.0f / a0, 1.0f / a1) : pk2(0.0f, 0.0f);
         Pp[i] = pk2(1.0f, 1.0f);
+        pend[i] = pk2(0.0f, 0.0f);
         bp[i] = pk2(0.0f, 0.0f);
     }
     float2* const sDU = reinterpret_cast<float2*>(smem + Lay::kDU);
@@ -512,26 +594,35 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
     bool ok = ntiles == 0 || __all_sync(0xffffffffu, mbar_wait(bar0, 0, kWaitLimit));
     int waited = ntiles > 0 ? 1 : 0;
     if (ok && ntiles > 0)
-        octet_prologue<T, G, TT, false, ZOH>(smem, kOct * (OPT - 1), lane_x, sDU + ch * kDUStride + g,
-                                        bias2, 0, 0, uu);
+        octet_prologue<T, G, TT, false, DISC>(smem, kOct * (OPT - 1), lane_x,
+                                              sDU + ch * kDUStride + g,
+                                              sDU + ch * kDUStride + g + kD2, bias2, 0, 0, uu);
     __syncwarp();
 
     bool done = false;
     int c = 0;  // octets processed: sDU buffer c & 1
     for (int r = 0; ok && !done && r < ntiles; ++r) {
         const unsigned char* st = smem + (r % S) * Lay::kStage;
-        const float* sB0 = reinterpret_cast<const float*>(st + 3 * Lay::kX) + n0;
+        const float* sB0 = reinterpret_cast<const float*>(st + Lay::kBoff) + n0;
 #pragma unroll
         for (int oo = OPT - 1; oo >= 0; --oo, ++c) {
             // (1) the octet's steps, last to first
             const float4* sd =
                 reinterpret_cast<const float4*>(sDU + ((c & 1) * CPW + ch) * kDUStride);
+            [[maybe_unused]] const float4* sd2 = sd + kD2 / 2;
             const float* sB = sB0 + kOct * oo * N;
 #pragma unroll
             for (int j = kOct - 1; j >= 0; --j) {
                 const float4 v2 = sd[j >> 1];
                 const float vdl = (j & 1) ? v2.z : v2.x, vdu = (j & 1) ? v2.w : v2.y;
                 const u64 dl2 = pk2(vdl, vdl), du2 = pk2(vdu, vdu);
+                [[maybe_unused]] u64 tr2 = 0, ux2 = 0;
+                if constexpr (TRAP) {
+                    const float4 w2 = sd2[j >> 1];
+                    const float vtr = (j & 1) ? w2.z : w2.x, vux = (j & 1) ? w2.w : w2.y;
+                    tr2 = pk2(vtr, vtr);
+                    ux2 = pk2(vux, vux);
+                }
                 u64 Bp[NP];
                 if constexpr (NP == 1) {
                     Bp[0] = *reinterpret_cast<const u64*>(sB + j * N);
@@ -548,22 +639,30 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
                 for (int i2 = 0; i2 < NP; ++i2) {
                     const u64 x2 = mul2(dl2, A2[i2]);
                     const u64 dA = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
-                    bp[i2] = fma2(Pp[i2], injection2<ZOH>(x2, dA, dl2, du2, iA2[i2], Bp[i2]),
-                                  bp[i2]);
+                    if constexpr (TRAP) {
+                        // this step's B*u meets the later step's deferred weight,
+                        // and this step's own (lambda*delta*u)*B its weight P
+                        bp[i2] = fma2(pend[i2], mul2(ux2, Bp[i2]), bp[i2]);
+                        bp[i2] = fma2(Pp[i2], mul2(du2, Bp[i2]), bp[i2]);
+                        pend[i2] = mul2(Pp[i2], tr2);
+                    } else {
+                        bp[i2] = fma2(Pp[i2], injection2<ZOH>(x2, dA, dl2, du2, iA2[i2], Bp[i2]),
+                                      bp[i2]);
+                    }
                     Pp[i2] = mul2(Pp[i2], dA);
                 }
             }
             // (2) the previous octet's step sizes (previous tile: wait first)
             float2* const dnx = sDU + (((c + 1) & 1) * CPW + ch) * kDUStride + g;
             if (oo > 0) {
-                octet_prologue<T, G, TT, false, ZOH>(st, kOct * (oo - 1), lane_x, dnx, bias2, 0, 0, uu);
+                octet_prologue<T, G, TT, false, DISC>(st, kOct * (oo - 1), lane_x, dnx, dnx + kD2, bias2, 0, 0, uu);
             } else if (r + 1 < ntiles) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * ((r + 1) % S),
                                                        ((r + 1) / S) & 1, kWaitLimit));
                 if (!ok) break;
                 waited = r + 2;
-                octet_prologue<T, G, TT, false, ZOH>(smem + ((r + 1) % S) * Lay::kStage,
-                                                kOct * (OPT - 1), lane_x, dnx, bias2, 0, 0, uu);
+                octet_prologue<T, G, TT, false, DISC>(smem + ((r + 1) % S) * Lay::kStage,
+                                                kOct * (OPT - 1), lane_x, dnx, dnx + kD2, bias2, 0, 0, uu);
             }
             __syncwarp();
             // (3) stop once every later-decay product is below fp32 resolution
@@ -590,6 +689,14 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
     if (!ok) {
         if (lane == 0) atomicOr(&g_scan_error, 1u);
         return;
+    }
+    if (TRAP && !done) {  // the first step's (1-lambda)*delta term: B*u before the chunk
+        u64 bxq[NP];
+#pragma unroll
+        for (int i = 0; i < NP; ++i) bxq[i] = pk2(0.0f, 0.0f);
+        trap_seed<T, NS>(a, b, d, n0, tc0, bxq);
+#pragma unroll
+        for (int i = 0; i < NP; ++i) bp[i] = fma2(pend[i], bxq[i], bp[i]);
     }
     const int64_t w = ((int64_t)(b * (a.K - 1) + k) * a.d_inner + d) * N + n0;
 #pragma unroll
@@ -660,16 +767,43 @@ static bool make_map(CUtensorMap* m, CUtensorMapDataType t, int es, const void* 
 }
 
 bool tma_scan_supported(int64_t N, int64_t d_inner, msc_dtype dtype, const void* u,
-                        const void* dt, const void* z) {
+                        const void* dt, const void* z, const void* lam) {
     if (!(N == 8 || N == 16 || N == 32 || N == 64)) return false;
     if (d_inner % 8 != 0) return false;  // whole 8-channel boxes (16 B of bf16)
     auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-    if (!al(u) || !al(dt) || (z && !al(z))) return false;
+    if (!al(u) || !al(dt) || (z && !al(z)) || (lam && !al(lam))) return false;
     (void)dtype;
     return encode_fn() != nullptr;
 }
 
 int tma_scan_tile(int64_t N) { return N <= 16 ? 32 : 16; }
+
+template <typename T, int G, int NS, int TT, int S, int DISC>
+static cudaError_t launch_tma_d(const ScanArgs& a, const ScanPlan& p, const CUtensorMap& mu,
+                                const CUtensorMap& mdt, const CUtensorMap& mz,
+                                const CUtensorMap& mB, const CUtensorMap& mC,
+                                const CUtensorMap& ml, cudaStream_t s) {
+    using Lay = TmaLayout<T, G, NS, TT, S, DISC == 2>;
+    const size_t smem = Lay::kTotal;
+    if (p.K > 1) {
+        auto kern = scan_summary_kernel<T, G, NS, TT, S, DISC>;
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        const int64_t nb = a.batch * (int64_t)(p.K - 1) * p.ntile;
+        kern<<<(unsigned)nb, 32, smem, s>>>(mu, mdt, mB, ml, a, p.K - 1);
+        const cudaError_t e = launch_carry_prefix(a, s);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t nb = a.batch * (int64_t)p.K * p.ntile;
+    const ProfileMark m = profile_begin(s, MSC_PROF_SCAN);
+    auto kern = scan_tma_kernel<T, G, NS, TT, S, DISC>;
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<(unsigned)nb, 32, smem, s>>>(mu, mdt, mz, mB, mC, ml, a, p.K);
+    profile_end(m, s);
+    profile_count(p.K > 1 ? 3 : 1);
+    return cudaGetLastError();
+}
 
 template <typename T, int G, int NS, int TT, int S>
 static cudaError_t launch_tma_ns(const ScanArgs& a, const ScanPlan& p, const float* Bf,
@@ -678,34 +812,17 @@ static cudaError_t launch_tma_ns(const ScanArgs& a, const ScanPlan& p, const flo
     const CUtensorMapDataType tt =
         sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const int es = (int)sizeof(T);
-    CUtensorMap mu, mdt, mz, mB, mC;
+    CUtensorMap mu, mdt, mz, mB, mC, ml;
     if (!make_map(&mu, tt, es, a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
         !make_map(&mdt, tt, es, a.dt, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
         !make_map(&mz, tt, es, a.z ? a.z : a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_map(&ml, tt, es, a.trap ? a.lam : a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
         !make_map(&mB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Bf, a.N, a.L, a.batch, (int)a.N, TT) ||
         !make_map(&mC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Cf, a.N, a.L, a.batch, (int)a.N, TT))
         return cudaErrorInvalidValue;
-    const size_t smem = Lay::kTotal;
-    if (p.K > 1) {
-        auto kern = a.zoh ? scan_summary_kernel<T, G, NS, TT, S, true>
-                          : scan_summary_kernel<T, G, NS, TT, S, false>;
-        if (smem > 48 * 1024)
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        const int64_t nb = a.batch * (int64_t)(p.K - 1) * p.ntile;
-        kern<<<(unsigned)nb, 32, smem, s>>>(mu, mdt, mB, a, p.K - 1);
-        const cudaError_t e = launch_carry_prefix(a, s);
-        if (e != cudaSuccess) return e;
-    }
-    const int64_t nb = a.batch * (int64_t)p.K * p.ntile;
-    const ProfileMark m = profile_begin(s, MSC_PROF_SCAN);
-    auto kern = a.zoh ? scan_tma_kernel<T, G, NS, TT, S, true>
-                      : scan_tma_kernel<T, G, NS, TT, S, false>;
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<(unsigned)nb, 32, smem, s>>>(mu, mdt, mz, mB, mC, a, p.K);
-    profile_end(m, s);
-    profile_count(p.K > 1 ? 3 : 1);
-    return cudaGetLastError();
+    if (a.trap) return launch_tma_d<T, G, NS, TT, S, 2>(a, p, mu, mdt, mz, mB, mC, ml, s);
+    if (a.zoh) return launch_tma_d<T, G, NS, TT, S, 1>(a, p, mu, mdt, mz, mB, mC, ml, s);
+    return launch_tma_d<T, G, NS, TT, S, 0>(a, p, mu, mdt, mz, mB, mC, ml, s);
 }
 
 template <typename T>

@@ -56,15 +56,27 @@ state_update_kernel(UpdateArgs a) {
     const float uu = Elem<T>::load(static_cast<const T*>(a.u) + ch);
     const float delta = softplus(x);
     const float du = delta * uu;
-    float Bv[4], Cv[4];
+    float Bv[4], Cv[4], Bq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     load_row4<T, VEC>(static_cast<const T*>(a.B) + b * N, n0, N, Bv);
     load_row4<T, VEC>(static_cast<const T*>(a.C) + b * N, n0, N, Cv);
+    float tra = 0.0f, trc = 0.0f, uq = 0.0f;  // exponential trapezoid
+    if (a.trap) {
+        const float lt = Elem<T>::load(static_cast<const T*>(a.lam) + ch);
+        tra = (1.0f - lt) * delta;
+        trc = (lt * delta) * uu;
+        if (a.u_prev && a.B_prev) {
+            uq = Elem<T>::load(static_cast<const T*>(a.u_prev) + ch);
+            load_row4<T, false>(static_cast<const T*>(a.B_prev) + b * N, n0, N, Bq);
+        }
+    }
     float y = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const float x2 = delta * A2[j];
         const float dA = ex2(x2);
-        const float inj = a.zoh ? zoh_gain(x2, dA, delta, iA[j]) * uu * Bv[j] : du * Bv[j];
+        const float inj = a.trap  ? fmaf(tra, uq * Bq[j], trc * Bv[j])
+                          : a.zoh ? zoh_gain(x2, dA, delta, iA[j]) * uu * Bv[j]
+                                  : du * Bv[j];
         h[j] = fmaf(dA, h[j], inj);
         y = fmaf(Cv[j], h[j], y);
     }
@@ -97,7 +109,7 @@ state_update_kernel(UpdateArgs a) {
 template <typename T, int N>
 __global__ void __launch_bounds__(128)
 state_update_row_kernel(UpdateArgs a) {
-    __shared__ float sB[N], sC[N];
+    __shared__ float sB[N], sC[N], sBq[N];
     const int b = blockIdx.y;
     const int64_t d_raw = (int64_t)blockIdx.x * 128 + threadIdx.x;
     const bool valid = d_raw < a.d_inner;
@@ -118,15 +130,29 @@ state_update_row_kernel(UpdateArgs a) {
     const float x = Elem<T>::load(static_cast<const T*>(a.dt) + ch) + bias;
     const float uu = Elem<T>::load(static_cast<const T*>(a.u) + ch);
     const float zz = a.z ? Elem<T>::load(static_cast<const T*>(a.z) + ch) : 0.0f;
+    const bool prev = a.trap && a.u_prev && a.B_prev;
+    const float lt = a.trap ? Elem<T>::load(static_cast<const T*>(a.lam) + ch) : 0.0f;
+    const float uq = prev ? Elem<T>::load(static_cast<const T*>(a.u_prev) + ch) : 0.0f;
     if (threadIdx.x < N) {
         sB[threadIdx.x] = Elem<T>::load(static_cast<const T*>(a.B) + (int64_t)b * N + threadIdx.x);
         sC[threadIdx.x] = Elem<T>::load(static_cast<const T*>(a.C) + (int64_t)b * N + threadIdx.x);
+        sBq[threadIdx.x] =
+            prev ? Elem<T>::load(static_cast<const T*>(a.B_prev) + (int64_t)b * N + threadIdx.x)
+                 : 0.0f;
     }
     const float delta = softplus(x);
     const float du = delta * uu;
     __syncthreads();
     float y = 0.0f;
-    if (a.zoh) {
+    if (a.trap) {  // exponential trapezoid
+        const float tra = (1.0f - lt) * delta, trc = (lt * delta) * uu;
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+            const float dA = ex2(delta * (Av[n] * kLog2e));
+            h[n] = fmaf(dA, h[n], fmaf(tra, uq * sBq[n], trc * sB[n]));
+            y = fmaf(sC[n], h[n], y);
+        }
+    } else if (a.zoh) {
 #pragma unroll
         for (int n = 0; n < N; ++n) {
             const float x2 = delta * (Av[n] * kLog2e);
