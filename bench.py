@@ -550,24 +550,39 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
     }
     del xu, su, ou
 
-    # (workload, zero-order hold): the other two scan workloads, and the
-    # 8 x 2048 x 1536 x 16 layer once more with the ZOH input matrix
-    for name, zoh in (("long_seq_64k", False), ("mamba2p8b_layer", False),
-                      ("mamba130m_layer", True)):
+    # (workload, discretisation): the other two scan workloads, and the
+    # 8 x 2048 x 1536 x 16 layer once more with the ZOH input matrix and with
+    # the exponential-trapezoid input (lambda ~ U[0, 1])
+    for name, disc in (("long_seq_64k", "euler"), ("mamba2p8b_layer", "euler"),
+                       ("mamba130m_layer", "zoh"), ("mamba130m_layer", "trapezoid")):
+        zoh = disc == "zoh"
         w = synth.WORKLOADS[name]
         x = synth.workload_inputs(name)
         a = dict(u=dev_t(x.u, "bf16"), dt=dev_t(x.dt_raw, "bf16"),
                  A=dev_t(x.A, "f32"), B=dev_t(x.B, "bf16"), C=dev_t(x.C, "bf16"),
                  D=dev_t(x.D, "f32"), z=dev_t(x.z, "bf16"),
                  dt_bias=dev_t(x.dt_bias, "f32"))
+        lam = None
+        if disc == "trapezoid":
+            lam = dev_t(synth.round_bf16(np.random.default_rng(13).uniform(
+                0.0, 1.0, x.u.shape).astype(np.float32)), "bf16")
         del x
         B_, L_, D_, N_ = w["batch"], w["L"], w["d_inner"], w["d_state"]
         out = torch.empty_like(a["u"])
         last = torch.empty(B_, D_, N_, dtype=torch.float32, device=dev)
         nws = msc.scan_workspace_size(B_, L_, D_, N_, torch.bfloat16)
         wsp = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
+
+        def call():
+            if lam is not None:
+                msc.selective_scan_trap_fwd(a["u"], a["dt"], lam, a["A"], a["B"], a["C"],
+                                            a["D"], a["z"], a["dt_bias"], out=out,
+                                            last_state=last, workspace=wsp)
+            else:
+                msc.selective_scan_fwd_ws(**a, out=out, last_state=last, workspace=wsp,
+                                          zoh=zoh)
         for _ in range(3):
-            msc.selective_scan_fwd_ws(**a, out=out, last_state=last, workspace=wsp, zoh=zoh)
+            call()
         times, total = [], []
         for _ in range(7):
             flush()
@@ -577,7 +592,7 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
-            msc.selective_scan_fwd_ws(**a, out=out, last_state=last, workspace=wsp, zoh=zoh)
+            call()
             e1.record()
             e1.synchronize()
             msc.profile_enable(False)
@@ -587,8 +602,8 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
         upd, mufu, byt = algorithmic(B_, L_, D_, N_)
         ms = statistics.median(total)
         kms = statistics.median(times)
-        res[name + ("_zoh" if zoh else "")] = {
-            "shape": [B_, L_, D_, N_], "discretization": "zoh" if zoh else "euler",
+        res[name + ("" if disc == "euler" else "_" + disc)] = {
+            "shape": [B_, L_, D_, N_], "discretization": disc,
             "ms": ms,
             "updates_per_s": upd / (ms * 1e-3),
             "output_kernel_ms": kms,
@@ -596,7 +611,7 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
             "hbm_frac": (byt / (ms * 1e-3)) / (peaks["hbm_gbs"] * 1e9),
             "timing": "whole call (all kernels), L2 flushed by a 512 MiB read before each",
         }
-        del a, out, last, wsp
+        del a, out, last, wsp, lam
         torch.cuda.empty_cache()
 
     # decode: 256 x 5120 x 16, 1000 steps, state in place
