@@ -79,6 +79,8 @@ class Oracle:
         lib.oracle_scan_fwd_trap.argtypes = [dp] * 14 + [i64] * 4 + [ctypes.c_int]
         lib.oracle_state_update_trap.restype = ctypes.c_int
         lib.oracle_state_update_trap.argtypes = [dp] * 13 + [i64] * 3 + [ctypes.c_int]
+        lib.oracle_scan_bwd.restype = ctypes.c_int
+        lib.oracle_scan_bwd.argtypes = [dp] * 20 + [i64] * 4
         lib.oracle_causal_conv1d.restype = ctypes.c_int
         lib.oracle_causal_conv1d.argtypes = [dp] * 6 + [i64] * 4 + [ctypes.c_int] * 2
         lib.oracle_conv1d_update.restype = ctypes.c_int
@@ -189,6 +191,30 @@ class Oracle:
             raise ValueError("oracle_state_update_trap rejected its sizes")
         return st, out
 
+    def scan_bwd(self, u, dt_raw, A, B, C, D=None, z=None, dt_bias=None, h0=None,
+                 dout=None, dlast=None):
+        """Gradients of the scan in fp64 -> dict du, ddt, dA, dB, dC, dD, dz,
+        ddt_bias, dh0 (dz None without z)."""
+        u, dt_raw, A, B, C, dout = map(_f64, (u, dt_raw, A, B, C, dout))
+        D, z, dt_bias, h0, dlast = map(_f64, (D, z, dt_bias, h0, dlast))
+        batch, L, d_inner, d_state = _dims(u, B)
+        g = dict(du=np.zeros((batch, L, d_inner)), ddt=np.zeros((batch, L, d_inner)),
+                 dA=np.zeros((d_inner, d_state)), dB=np.zeros((batch, L, d_state)),
+                 dC=np.zeros((batch, L, d_state)), dD=np.zeros(d_inner),
+                 dz=np.zeros((batch, L, d_inner)), ddt_bias=np.zeros(d_inner),
+                 dh0=np.zeros((batch, d_inner, d_state)))
+        rc = self.lib.oracle_scan_bwd(
+            _ptr(u), _ptr(dt_raw), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+            _ptr(dt_bias), _ptr(h0), _ptr(dout), _ptr(dlast), _ptr(g["du"]),
+            _ptr(g["ddt"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
+            _ptr(g["dz"]), _ptr(g["ddt_bias"]), _ptr(g["dh0"]), batch, L, d_inner,
+            d_state)
+        if rc != 0:
+            raise ValueError("oracle_scan_bwd rejected its sizes")
+        if z is None:
+            g["dz"] = None
+        return g
+
     def causal_conv1d(self, x, w, bias=None, state_in=None, silu: bool = True,
                       nthreads: int = 0):
         """Causal depthwise conv1d (+ SiLU) in fp64 -> (out, state_out).
@@ -273,3 +299,7 @@ def scan_fwd_trap(*args, **kwargs):
 
 def state_update_trap(*args, **kwargs):
     return default().state_update_trap(*args, **kwargs)
+
+
+def scan_bwd(*args, **kwargs):
+    return default().scan_bwd(*args, **kwargs)

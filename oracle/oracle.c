@@ -393,3 +393,106 @@ int oracle_state_update_trap(double* state, const double* u_prev, const double* 
     }
     return 0;
 }
+
+/*
+ * Backward pass of the selective scan (Euler form): the gradients of a loss
+ * J(out, last_state) with respect to every input, given dout = dJ/dout and
+ * dlast = dJ/dlast_state (nullable: zero).  The pages say the backward
+ * recomputes the states rather than storing them (the chunk + recompute
+ * scheme of "Deep dive into Mamba" section 7.3; the Mamba series article,
+ * section 3: a custom kernel differentiates the scan); this oracle simply
+ * keeps every state of a channel and runs the adjoint recurrence backwards:
+ *     dy_t  = dout_t * silu(z_t)              (dout_t without the gate)
+ *     dh_t  = C_t dy_t + exp(delta_{t+1} A) dh_{t+1}      (dh_{L-1} += dlast)
+ *     with a_t = exp(delta_t A), from h_t = a_t h_{t-1} + delta_t B_t u_t:
+ *       dA      += dh_t h_{t-1} a_t delta_t
+ *       ddelta_t = sum_n dh_t h_{t-1} a_t A + dh_t B_t u_t
+ *       dB_t    += dh_t delta_t u_t        dC_t += dy_t h_t
+ *       du_t     = dy_t D + sum_n dh_t delta_t B_t
+ *     ddt_t = ddelta_t sigmoid(dt_t + dt_bias)  (softplus' = sigmoid)
+ *     dz_t  = dout_t y_t silu'(z_t),  silu'(z) = s (1 + z (1 - s)), s = sigmoid(z)
+ *     dD += dy_t u_t,  ddt_bias += ddt_t,  dh0 = a_0 dh_0.
+ * Shapes as the forward; dA: (d_inner, d_state); dB, dC: (batch, L,
+ * d_state); dD, ddt_bias: (d_inner); dh0: (batch, d_inner, d_state).  Every
+ * output is overwritten.  Sequential (the parameter gradients are sums over
+ * channels and steps).
+ */
+static double oracle_sigmoid(double x) {
+    if (x >= 0.0) return 1.0 / (1.0 + exp(-x));
+    const double e = exp(x);
+    return e / (1.0 + e);
+}
+
+int oracle_scan_bwd(const double* u, const double* dt_raw, const double* A,
+                    const double* B, const double* C, const double* D,
+                    const double* z, const double* dt_bias, const double* h0,
+                    const double* dout, const double* dlast, double* du,
+                    double* ddt, double* dA, double* dB, double* dC, double* dD,
+                    double* dz, double* ddt_bias, double* dh0, int64_t batch,
+                    int64_t L, int64_t d_inner, int64_t d_state) {
+    if (batch < 0 || L < 0 || d_inner < 0 || d_state < 1) return -1;
+    const int64_t N = d_state;
+    memset(dA, 0, (size_t)(d_inner * N) * sizeof(double));
+    memset(dB, 0, (size_t)(batch * L * N) * sizeof(double));
+    memset(dC, 0, (size_t)(batch * L * N) * sizeof(double));
+    memset(dD, 0, (size_t)d_inner * sizeof(double));
+    memset(ddt_bias, 0, (size_t)d_inner * sizeof(double));
+    double* hs = (double*)malloc((size_t)((L + 1) * N) * sizeof(double));
+    double* ys = (double*)malloc((size_t)(L + 1) * sizeof(double));
+    double* dh = (double*)malloc((size_t)N * sizeof(double));
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < d_inner; ++d) {
+            const int64_t c = b * d_inner + d;
+            const double bias = dt_bias ? dt_bias[d] : 0.0;
+            const double skip = D ? D[d] : 0.0;
+            /* forward, keeping h_{t} in hs[t + 1] and y_t (before the gate) */
+            for (int64_t n = 0; n < N; ++n) hs[n] = h0 ? h0[c * N + n] : 0.0;
+            for (int64_t t = 0; t < L; ++t) {
+                const int64_t i = (b * L + t) * d_inner + d, r = (b * L + t) * N;
+                const double delta = oracle_softplus(dt_raw[i] + bias);
+                double y = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    const double a = exp(delta * A[d * N + n]);
+                    hs[(t + 1) * N + n] = a * hs[t * N + n] + delta * B[r + n] * u[i];
+                    y += C[r + n] * hs[(t + 1) * N + n];
+                }
+                ys[t] = y + skip * u[i];
+            }
+            /* backward */
+            for (int64_t n = 0; n < N; ++n) dh[n] = dlast ? dlast[c * N + n] : 0.0;
+            for (int64_t t = L - 1; t >= 0; --t) {
+                const int64_t i = (b * L + t) * d_inner + d, r = (b * L + t) * N;
+                const double x = dt_raw[i] + bias;
+                const double delta = oracle_softplus(x);
+                double dy = dout[i];
+                if (z) {
+                    const double s = oracle_sigmoid(z[i]);
+                    dy = dout[i] * z[i] * s;
+                    dz[i] = dout[i] * ys[t] * s * (1.0 + z[i] * (1.0 - s));
+                }
+                dD[d] += dy * u[i];
+                double dui = dy * skip, ddelta = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    const double a = exp(delta * A[d * N + n]);
+                    dh[n] += C[r + n] * dy;
+                    dC[r + n] += dy * hs[(t + 1) * N + n];
+                    const double da = dh[n] * hs[t * N + n];
+                    dA[d * N + n] += da * a * delta;
+                    ddelta += da * a * A[d * N + n] + dh[n] * B[r + n] * u[i];
+                    dB[r + n] += dh[n] * delta * u[i];
+                    dui += dh[n] * delta * B[r + n];
+                    dh[n] *= a;
+                }
+                du[i] = dui;
+                ddt[i] = ddelta * oracle_sigmoid(x);
+                ddt_bias[d] += ddt[i];
+            }
+            if (dh0)
+                for (int64_t n = 0; n < N; ++n) dh0[c * N + n] = dh[n];
+        }
+    }
+    free(hs);
+    free(ys);
+    free(dh);
+    return 0;
+}

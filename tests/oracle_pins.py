@@ -37,7 +37,10 @@ different evaluation that the pages or plain mathematics fix:
   * the Mamba-3 exponential-trapezoid scan (Mamba series article, 2.1):
     lambda = 1 is the Euler scan bit for bit, lambda = 0 is the Euler scan of
     the inputs delayed one step, a constant-input closed form, split prefill
-    carrying the previous step's input, decode == scan.
+    carrying the previous step's input, decode == scan;
+  * the scan's backward pass: every gradient against central finite
+    differences of the (pinned) forward oracle, and against torch autograd
+    through an fp64 forward written here with tensor operations.
 """
 from __future__ import annotations
 
@@ -514,6 +517,77 @@ def check_trap_split_and_decode(orc):
     assert np.array_equal(st, l0)
 
 
+
+def _bwd_case(seed):
+    x = _random_case(2, 5, 2, 3, seed=seed)
+    rng = np.random.default_rng(seed + 1)
+    h0 = rng.standard_normal((2, 2, 3))
+    w_out = rng.standard_normal(x.u.shape)
+    w_last = rng.standard_normal((2, 2, 3))
+    return x, h0, w_out, w_last
+
+
+def _bwd_inputs(x, h0):
+    return dict(u=x.u, dt_raw=x.dt_raw, A=x.A, B=x.B, C=x.C, D=x.D, z=x.z,
+                dt_bias=x.dt_bias, h0=h0)
+
+
+def check_bwd_finite_differences(orc):
+    """J = sum(out * w_out) + sum(last * w_last); every input element's
+    gradient against a central difference of the forward oracle."""
+    x, h0, w_out, w_last = _bwd_case(50)
+    inp = {k: np.array(v, dtype=np.float64) for k, v in _bwd_inputs(x, h0).items()}
+    g = orc.scan_bwd(inp["u"], inp["dt_raw"], inp["A"], inp["B"], inp["C"], inp["D"],
+                     inp["z"], inp["dt_bias"], inp["h0"], dout=w_out, dlast=w_last)
+    names = dict(u="du", dt_raw="ddt", A="dA", B="dB", C="dC", D="dD", z="dz",
+                 dt_bias="ddt_bias", h0="dh0")
+
+    def J(v):
+        y, last = orc.scan_fwd(v["u"], v["dt_raw"], v["A"], v["B"], v["C"], v["D"],
+                               v["z"], v["dt_bias"], h0=v["h0"])
+        return float(np.sum(y * w_out) + np.sum(last * w_last))
+    eps = 1e-6
+    for key, gname in names.items():
+        arr = inp[key]
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + eps
+            jp = J(inp)
+            arr[idx] = old - eps
+            jm = J(inp)
+            arr[idx] = old
+            fd = (jp - jm) / (2 * eps)
+            got = g[gname][idx]
+            assert abs(got - fd) <= 1e-6 * (1.0 + abs(fd)), (key, idx, got, fd)
+
+
+def check_bwd_against_autograd(orc):
+    """The same gradients from torch autograd through an fp64 forward written
+    with tensor operations (softplus as log(1 + e^x), silu as z sigmoid z)."""
+    import torch
+    x, h0, w_out, w_last = _bwd_case(51)
+    t = {k: torch.tensor(np.asarray(v, dtype=np.float64), requires_grad=True)
+         for k, v in _bwd_inputs(x, h0).items()}
+    delta = torch.logaddexp(torch.zeros((), dtype=torch.float64), t["dt_raw"] + t["dt_bias"])
+    h = t["h0"]
+    outs = []
+    for s in range(x.u.shape[1]):
+        a = torch.exp(delta[:, s, :, None] * t["A"][None])
+        h = a * h + delta[:, s, :, None] * t["B"][:, s, None, :] * t["u"][:, s, :, None]
+        y = (h * t["C"][:, s, None, :]).sum(-1) + t["D"] * t["u"][:, s]
+        outs.append(y * t["z"][:, s] * torch.sigmoid(t["z"][:, s]))
+    J = (torch.stack(outs, 1) * torch.from_numpy(w_out)).sum() + \
+        (h * torch.from_numpy(w_last)).sum()
+    keys = list(t)
+    grads = torch.autograd.grad(J, [t[k] for k in keys])
+    g = orc.scan_bwd(x.u, x.dt_raw, x.A, x.B, x.C, x.D, x.z, x.dt_bias, h0,
+                     dout=w_out, dlast=w_last)
+    names = dict(u="du", dt_raw="ddt", A="dA", B="dB", C="dC", D="dD", z="dz",
+                 dt_bias="ddt_bias", h0="dh0")
+    for k, gr in zip(keys, grads):
+        assert rel_l2(g[names[k]], gr.numpy()) < 1e-12, k
+
+
 ALL_CHECKS = [
     check_softplus,
     check_silu,
@@ -537,4 +611,6 @@ ALL_CHECKS = [
     check_trap_lambda_zero_is_delayed_euler,
     check_trap_closed_form,
     check_trap_split_and_decode,
+    check_bwd_finite_differences,
+    check_bwd_against_autograd,
 ]

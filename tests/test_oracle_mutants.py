@@ -70,6 +70,20 @@ MUTANTS = [
     ("trap_prev_input_ignored",
      "bx[n] = (u_prev && B_prev) ? B_prev[b * d_state + n] * u_prev[c] : 0.0;\n        }",
      "bx[n] = 0.0;\n        }"),
+    ("bwd_no_carry", "dh[n] *= a;", ";"),
+    ("bwd_ddelta_sign", "ddelta += da * a * A[d * N + n] + dh[n] * B[r + n] * u[i];",
+     "ddelta += -da * a * A[d * N + n] + dh[n] * B[r + n] * u[i];"),
+    ("bwd_no_sigmoid", "ddt[i] = ddelta * oracle_sigmoid(x);", "ddt[i] = ddelta;"),
+    ("bwd_dC_previous_state", "dC[r + n] += dy * hs[(t + 1) * N + n];",
+     "dC[r + n] += dy * hs[t * N + n];"),
+    ("bwd_dB_no_delta", "dB[r + n] += dh[n] * delta * u[i];", "dB[r + n] += dh[n] * u[i];"),
+    ("bwd_dA_no_delta", "dA[d * N + n] += da * a * delta;", "dA[d * N + n] += da * a;"),
+    ("bwd_dz_no_silu_slope", "dz[i] = dout[i] * ys[t] * s * (1.0 + z[i] * (1.0 - s));",
+     "dz[i] = dout[i] * ys[t] * s;"),
+    ("bwd_dy_ungated", "dy = dout[i] * z[i] * s;", "dy = dout[i];"),
+    ("bwd_dlast_ignored", "dh[n] = dlast ? dlast[c * N + n] : 0.0;", "dh[n] = 0.0;"),
+    ("bwd_du_no_skip", "double dui = dy * skip, ddelta = 0.0;",
+     "double dui = 0.0, ddelta = 0.0;"),
     ("segment_rerun_from_zero", "memcpy(hk, h, (size_t)d_state * sizeof(double));",
      "memset(hk, 0, (size_t)d_state * sizeof(double));"),
 ]
