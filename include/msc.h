@@ -190,6 +190,36 @@ msc_status msc_causal_conv1d_update(
     int64_t batch, int64_t d_inner, int64_t d_conv, int silu, msc_dtype dtype,
     msc_stream_t stream);
 
+/*
+ * Backward pass of msc_selective_scan_fwd (the Euler form): the gradients of
+ * a loss J(out, last_state) given dout = dJ/dout and dlast_state =
+ * dJ/dlast_state.  The states are recomputed from checkpoints (one per 32
+ * steps), not read from the forward -- the pages' chunk + recompute scheme
+ * ("Deep dive into Mamba" section 7.3) -- and the adjoint
+ *     dh_t = C_t * dy_t + exp(delta_{t+1}*A) * dh_{t+1},  dy_t = dout_t * silu(z_t)
+ * runs backwards through the sequence.
+ *   forward inputs: as msc_selective_scan_fwd (h0 nullable: zero)
+ *   dout          : (batch, L, d_inner), `dtype`
+ *   dlast_state   : (batch, d_inner, d_state) fp32, nullable: zero
+ *   du, ddt, dz   : (batch, L, d_inner), `dtype` (ddt is d/d dt, before the
+ *                   softplus); dz nullable (not written), zeros when z is NULL
+ *   dA            : (d_inner, d_state) fp32
+ *   dB, dC        : (batch, L, d_state) fp32 (sums over the channels)
+ *   dD, ddt_bias  : (d_inner) fp32, nullable (not written)
+ *   dh0           : (batch, d_inner, d_state) fp32, nullable (not written)
+ * dA, dB, dC, dD, ddt_bias are accumulated with atomic adds after being
+ * zeroed by the call: their last bits depend on the order of the adds.
+ * Scratch: the checkpoints, batch * ceil(L/32) * d_inner * d_state * 4 bytes,
+ * taken stream-ordered.  batch <= 65535.  Errors as msc_selective_scan_fwd.
+ */
+msc_status msc_selective_scan_bwd(
+    const void* u, const void* dt, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* dt_bias, const float* h0,
+    const void* dout, const float* dlast_state, void* du, void* ddt, float* dA,
+    float* dB, float* dC, float* dD, void* dz, float* ddt_bias, float* dh0,
+    int64_t batch, int64_t L, int64_t d_inner, int64_t d_state, msc_dtype dtype,
+    msc_stream_t stream);
+
 /* Discretisation of the input matrix B (the _ex entry points). */
 typedef enum msc_discretization {
     MSC_DISC_EULER = 0,  /* delta * B                                    */
@@ -317,7 +347,8 @@ enum {
     MSC_PROF_UPDATE = 1,       /* decode state-update kernel         */
     MSC_PROF_CONV = 2,         /* causal conv1d prefill kernel       */
     MSC_PROF_CONV_UPDATE = 3,  /* causal conv1d decode-update kernel */
-    MSC_PROF_KINDS = 4
+    MSC_PROF_SCAN_BWD = 4,     /* scan backward (adjoint) kernel      */
+    MSC_PROF_KINDS = 5
 };
 msc_status msc_profile_enable(int on);
 msc_status msc_profile_read(int64_t* launches, int64_t* timed, double* total_ms);

@@ -85,6 +85,8 @@ def load():
                                                 + [st, vp, ctypes.c_size_t, vp])
     lib.msc_selective_state_update_trap.restype = st
     lib.msc_selective_state_update_trap.argtypes = [vp] * 13 + [i64] * 3 + [st, vp]
+    lib.msc_selective_scan_bwd.restype = st
+    lib.msc_selective_scan_bwd.argtypes = [vp] * 20 + [i64] * 4 + [st, vp]
     lib.msc_causal_conv1d_fwd.restype = st
     lib.msc_causal_conv1d_fwd.argtypes = [vp] * 6 + [i64] * 4 + [ctypes.c_int, st, vp]
     lib.msc_causal_conv1d_update.restype = st
@@ -349,6 +351,42 @@ def selective_state_update_trap(state, u_prev, B_prev, u, dt, lam, A, B, C, D=No
     return out
 
 
+def selective_scan_bwd(u, dt, A, B, C, D=None, z=None, dt_bias=None, h0=None,
+                       dout=None, dlast_state=None, want_dh0=False):
+    """Backward pass of selective_scan_fwd on the GPU -> dict of gradients:
+    du, ddt, dz (u's dtype), dA, dB, dC, dD, ddt_bias, dh0 (fp32; dz, dD,
+    ddt_bias None when z, D, dt_bias are None; dh0 only with want_dh0)."""
+    torch = _torch()
+    batch, L, d_inner = u.shape
+    d_state = B.shape[-1]
+    dev, sdt, f32 = u.device, u.dtype, torch.float32
+    code = _dtype_code(u)
+    g = dict(du=torch.empty_like(u), ddt=torch.empty_like(u),
+             dz=torch.empty_like(u) if z is not None else None,
+             dA=torch.empty(d_inner, d_state, dtype=f32, device=dev),
+             dB=torch.empty(batch, L, d_state, dtype=f32, device=dev),
+             dC=torch.empty(batch, L, d_state, dtype=f32, device=dev),
+             dD=torch.empty(d_inner, dtype=f32, device=dev) if D is not None else None,
+             ddt_bias=torch.empty(d_inner, dtype=f32, device=dev) if dt_bias is not None else None,
+             dh0=torch.empty(batch, d_inner, d_state, dtype=f32, device=dev) if want_dh0 else None)
+    P = lambda t, name, dt_=None, shape=None: _ptr(t, name, dt_, shape, dev)
+    st = load().msc_selective_scan_bwd(
+        P(u, "u", sdt, (batch, L, d_inner)), P(dt, "dt", sdt, (batch, L, d_inner)),
+        P(A, "A", f32, (d_inner, d_state)), P(B, "B", sdt, (batch, L, d_state)),
+        P(C, "C", sdt, (batch, L, d_state)), P(D, "D", f32, (d_inner,)),
+        P(z, "z", sdt, (batch, L, d_inner)), P(dt_bias, "dt_bias", f32, (d_inner,)),
+        P(h0, "h0", f32, (batch, d_inner, d_state)), P(dout, "dout", sdt, (batch, L, d_inner)),
+        P(dlast_state, "dlast_state", f32, (batch, d_inner, d_state)),
+        g["du"].data_ptr(), g["ddt"].data_ptr(), g["dA"].data_ptr(), g["dB"].data_ptr(),
+        g["dC"].data_ptr(), None if g["dD"] is None else g["dD"].data_ptr(),
+        None if g["dz"] is None else g["dz"].data_ptr(),
+        None if g["ddt_bias"] is None else g["ddt_bias"].data_ptr(),
+        None if g["dh0"] is None else g["dh0"].data_ptr(),
+        batch, L, d_inner, d_state, code, _stream(dev))
+    _check("msc_selective_scan_bwd", st)
+    return g
+
+
 def causal_conv1d_fwd(x, w, bias=None, state_in=None, out=None, state_out=None,
                       silu=True, return_state=True):
     """Causal depthwise conv1d (+ SiLU) on the GPU -> (out, state_out).
@@ -411,7 +449,7 @@ def profile_enable(on: bool = True):
     _check("msc_profile_enable", load().msc_profile_enable(int(on)))
 
 
-_PROF_KINDS = ("scan", "update", "conv", "conv_update")   # msc.h MSC_PROF_* order
+_PROF_KINDS = ("scan", "update", "conv", "conv_update", "scan_bwd")  # MSC_PROF_* order
 
 
 def profile_read():

@@ -26,7 +26,7 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
 
 LIBS = {
     "libmsc.so": ["msc_api.cu", "scan_fwd.cu", "scan_tma.cu", "state_update.cu",
-                  "conv1d.cu"],
+                  "conv1d.cu", "scan_bwd.cu"],
     "libmsc_peaks.so": ["peaks.cu"],
 }
 

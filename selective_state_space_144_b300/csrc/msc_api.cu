@@ -405,6 +405,59 @@ msc_status msc_selective_state_update_trap(float* state, const void* u_prev, con
                       0, stream, lam, u_prev, B_prev);
 }
 
+msc_status msc_selective_scan_bwd(const void* u, const void* dt, const float* A, const void* B,
+                                  const void* C, const float* D, const void* z,
+                                  const float* dt_bias, const float* h0, const void* dout,
+                                  const float* dlast, void* du, void* ddt, float* dA, float* dB,
+                                  float* dC, float* dD, void* dz, float* ddt_bias, float* dh0,
+                                  int64_t batch, int64_t L, int64_t d_inner, int64_t d_state,
+                                  msc_dtype dtype, msc_stream_t stream) {
+    if (dtype != MSC_F32 && dtype != MSC_BF16) return MSC_ERR_INVALID_ARG;
+    if (batch < 0 || L < 0 || d_inner < 0 || d_state < 0) return MSC_ERR_INVALID_ARG;
+    if (d_state < 1 || d_state > 64) return MSC_ERR_UNSUPPORTED;
+    int64_t bl, bld, bln, dn;
+    if (!mul_ok(batch, L, &bl) || !mul_ok(bl, d_inner, &bld) || !mul_ok(bl, d_state, &bln) ||
+        !mul_ok(d_inner, d_state, &dn) || bld > std::numeric_limits<int64_t>::max() / 8 ||
+        bln > std::numeric_limits<int64_t>::max() / 8)
+        return MSC_ERR_UNSUPPORTED;
+    if (batch == 0 || d_inner == 0) return MSC_OK;
+    if (!A || !dA || (L > 0 && (!u || !dt || !B || !C || !dout || !du || !ddt || !dB || !dC)))
+        return MSC_ERR_INVALID_ARG;
+    if (batch > 65535) return MSC_ERR_UNSUPPORTED;
+    const size_t es = elem_size(dtype);
+    const void* typed[] = {u, dt, B, C, z, dout, du, ddt, dz};
+    for (const void* p : typed)
+        if (p && !aligned(p, es)) return MSC_ERR_ALIGNMENT;
+    const void* f32[] = {A, D, dt_bias, h0, dlast, dA, dB, dC, dD, ddt_bias, dh0};
+    for (const void* p : f32)
+        if (p && !aligned(p, 4)) return MSC_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    msc::BwdArgs a{};
+    a.u = u; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.dt_bias = dt_bias;
+    a.h0 = h0; a.dout = dout; a.dlast = dlast; a.du = du; a.ddt = ddt; a.dA = dA; a.dB = dB;
+    a.dC = dC; a.dD = dD; a.dz = dz; a.ddt_bias = ddt_bias; a.dh0 = dh0;
+    a.batch = batch; a.L = L; a.d_inner = d_inner; a.N = d_state;
+    a.nseg = (L + msc::kBwdSegment - 1) / msc::kBwdSegment;
+    a.vec = (d_state % 4 == 0) && (!B || aligned(B, 4 * es)) && (!C || aligned(C, 4 * es));
+    // the accumulated gradients start from zero
+    cudaError_t e = cudaMemsetAsync(dA, 0, (size_t)dn * sizeof(float), s);
+    if (e == cudaSuccess && L > 0) e = cudaMemsetAsync(dB, 0, (size_t)bln * sizeof(float), s);
+    if (e == cudaSuccess && L > 0) e = cudaMemsetAsync(dC, 0, (size_t)bln * sizeof(float), s);
+    if (e == cudaSuccess && dD) e = cudaMemsetAsync(dD, 0, (size_t)d_inner * sizeof(float), s);
+    if (e == cudaSuccess && ddt_bias)
+        e = cudaMemsetAsync(ddt_bias, 0, (size_t)d_inner * sizeof(float), s);
+    if (e != cudaSuccess) return MSC_ERR_CUDA;
+    void* ck = nullptr;
+    if (cudaMallocAsync(&ck, msc::scan_bwd_ckpt_bytes(batch, L, d_inner, d_state), s) !=
+        cudaSuccess)
+        return MSC_ERR_CUDA;
+    a.ckpt = static_cast<float*>(ck);
+    e = msc::launch_scan_bwd(a, dtype, s);
+    const cudaError_t f = cudaFreeAsync(ck, s);
+    if (e == cudaSuccess) e = f;
+    return e == cudaSuccess ? MSC_OK : MSC_ERR_CUDA;
+}
+
 static msc_status run_conv(const void* x, const float* w, const float* bias,
                            const void* state_in, void* out, void* state, int64_t batch,
                            int64_t L, int64_t d_inner, int64_t d_conv, int silu,

@@ -86,6 +86,37 @@ struct ConvArgs {
 cudaError_t launch_causal_conv1d(const ConvArgs& a, msc_dtype dtype, cudaStream_t s);
 cudaError_t launch_conv1d_update(const ConvArgs& a, msc_dtype dtype, cudaStream_t s);
 
+// Backward pass of the scan (scan_bwd.cu).  ckpt: (batch, nseg, d_inner, N)
+// fp32 states entering each segment of the recompute.
+struct BwdArgs {
+    const void* u;
+    const void* dt;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* dt_bias;
+    const float* h0;
+    const void* dout;
+    const float* dlast;
+    void* du;
+    void* ddt;
+    float* dA;
+    float* dB;
+    float* dC;
+    float* dD;
+    void* dz;
+    float* ddt_bias;
+    float* dh0;
+    float* ckpt;
+    int64_t batch, L, d_inner, N, nseg;
+    int vec;           // 1: B/C rows can be read 4 elements at a time
+};
+cudaError_t launch_scan_bwd(const BwdArgs& a, msc_dtype dtype, cudaStream_t s);
+size_t scan_bwd_ckpt_bytes(int64_t batch, int64_t L, int64_t d_inner, int64_t N);
+constexpr int64_t kBwdSegment = 32;  // steps per recomputed segment
+
 // Measurement hook (msc_api.cu): while enabled, launchers count kernels and
 // bracket their main kernel with an event pair on the launch stream.
 struct ProfileMark {
