@@ -66,7 +66,8 @@ def parse():
     ap.add_argument("--profile", default=None, metavar="WORKLOAD",
                     help="profiling driver: run only the scan (or, for "
                          "decode_256x5120, the decode step; for conv1d_prefill "
-                         "/ conv1d_update, the conv) on WORKLOAD "
+                         "/ conv1d_update, the conv; for scan_bwd, the backward "
+                         "pass on the 130M layer) on WORKLOAD "
                          "--warmup + --steps times, print nothing else "
                          "(for ncu; see profiles/)")
     return ap.parse_args()
@@ -550,6 +551,53 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
     }
     del xu, su, ou
 
+    # backward pass of the scan on the 8 x 2048 x 1536 x 16 layer (bf16):
+    # checkpoint pass + adjoint pass, gradients of every input
+    xb = synth.workload_inputs("mamba130m_layer")
+    ab = dict(u=dev_t(xb.u, "bf16"), dt=dev_t(xb.dt_raw, "bf16"), A=dev_t(xb.A, "f32"),
+              B=dev_t(xb.B, "bf16"), C=dev_t(xb.C, "bf16"), D=dev_t(xb.D, "f32"),
+              z=dev_t(xb.z, "bf16"), dt_bias=dev_t(xb.dt_bias, "f32"))
+    gout = dev_t(synth.round_bf16(np.random.default_rng(14).standard_normal(
+        xb.u.shape).astype(np.float32)), "bf16")
+    Bb_, Lb_, Db_, Nb_ = xb.u.shape + (xb.B.shape[-1],)
+    del xb
+    bstep = lambda k: msc.selective_scan_bwd(**ab, dout=gout)
+    for k in range(2):
+        bstep(k)
+    tb, kb = [], []
+    for _ in range(5):
+        flush()
+        torch.cuda.synchronize(dev)
+        msc.profile_read()
+        msc.profile_enable(True)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        bstep(0)
+        e1.record()
+        e1.synchronize()
+        msc.profile_enable(False)
+        _, kinds = msc.profile_read()
+        kb.append(kinds["scan_bwd"][1])
+        tb.append(e0.elapsed_time(e1))
+    updb = Bb_ * Lb_ * Db_ * Nb_
+    bms, bkms = statistics.median(tb), statistics.median(kb)
+    # algorithmic work of a recompute backward: the forward exponential again
+    # and the adjoint's, 2 ex2 per update, plus softplus, sigmoid(dt), sigmoid(z)
+    # per (step, channel); HBM: u, dt, z, dout read, du, ddt, dz written (2 B
+    # each), B, C read and dB, dC written per (step, state)
+    b_mufu = updb * (2 + 6.0 / Nb_)
+    b_bytes = Bb_ * Lb_ * Db_ * 7 * 2 + Bb_ * Lb_ * Nb_ * (2 * 2 + 2 * 4) + Db_ * Nb_ * 8
+    res["scan_bwd_mamba130m_layer"] = {
+        "shape": [Bb_, Lb_, Db_, Nb_], "ms": bms, "adjoint_kernel_ms": bkms,
+        "updates_per_s": updb / (bms * 1e-3),
+        "mufu_frac": (b_mufu / (bms * 1e-3)) / ex2_peak,
+        "hbm_frac": (b_bytes / (bms * 1e-3)) / (peaks["hbm_gbs"] * 1e9),
+        "timing": "whole call (memsets, checkpoint and adjoint kernels, stream-ordered scratch)",
+    }
+    del ab, gout
+    torch.cuda.empty_cache()
+
     # (workload, discretisation): the other two scan workloads, and the
     # 8 x 2048 x 1536 x 16 layer once more with the ZOH input matrix and with
     # the exponential-trapezoid input (lambda ~ U[0, 1])
@@ -666,6 +714,21 @@ def run_profile(args):
             return torch.from_numpy(bits.copy()).to(dev).view(torch.bfloat16)
         return torch.from_numpy(np.ascontiguousarray(arr, np.float32)).to(dev)
 
+    if name == "scan_bwd":
+        # backward pass of the scan on the 8 x 2048 x 1536 x 16 layer, bf16
+        x = synth.workload_inputs("mamba130m_layer")
+        a = dict(u=dev_t(x.u, "bf16"), dt=dev_t(x.dt_raw, "bf16"), A=dev_t(x.A, "f32"),
+                 B=dev_t(x.B, "bf16"), C=dev_t(x.C, "bf16"), D=dev_t(x.D, "f32"),
+                 z=dev_t(x.z, "bf16"), dt_bias=dev_t(x.dt_bias, "f32"))
+        gout = dev_t(synth.round_bf16(np.random.default_rng(14).standard_normal(
+            x.u.shape).astype(np.float32)), "bf16")
+        del x
+        for _ in range(args.warmup + args.steps):
+            msc.selective_scan_bwd(**a, dout=gout)
+        torch.cuda.synchronize(dev)
+        msc.check_device_error()
+        print(f"profile run done: {name}, {args.warmup + args.steps} calls", flush=True)
+        return 0
     if name in ("conv1d_prefill", "conv1d_update"):
         # the conv before the scan: prefill on the 8 x 2048 x 1536 layer, or
         # the decode token on 256 x 5120; d_conv 4, bf16

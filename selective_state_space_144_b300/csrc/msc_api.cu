@@ -447,12 +447,43 @@ msc_status msc_selective_scan_bwd(const void* u, const void* dt, const float* A,
     if (e == cudaSuccess && ddt_bias)
         e = cudaMemsetAsync(ddt_bias, 0, (size_t)d_inner * sizeof(float), s);
     if (e != cudaSuccess) return MSC_ERR_CUDA;
+    // checkpoints: the forward's TMA chunk summaries + carry prefix with chunks
+    // of one recompute segment when the shape allows, else the element-load
+    // checkpoint kernel
+    msc::ScanPlan p{};
+    bool tma_ck = g_scan_path == 0 && a.nseg >= 2 &&
+                  msc::tma_scan_supported(d_state, d_inner, dtype, u, dt, nullptr);
+    if (tma_ck) {
+        const bool need_bc = dtype == MSC_BF16 || !aligned(B, 16) || !aligned(C, 16);
+        p = msc::make_tma_plan(batch, L, d_inner, d_state, sm_count(), a.nseg, g_min_chunk,
+                               need_bc, g_scan_lanes);
+        p.summaries_only = 1;
+        tma_ck = p.chunk == msc::kBwdSegment && p.K == a.nseg;
+    }
     void* ck = nullptr;
-    if (cudaMallocAsync(&ck, msc::scan_bwd_ckpt_bytes(batch, L, d_inner, d_state), s) !=
-        cudaSuccess)
-        return MSC_ERR_CUDA;
-    a.ckpt = static_cast<float*>(ck);
-    e = msc::launch_scan_bwd(a, dtype, s);
+    const size_t ck_bytes =
+        tma_ck ? p.ws_bytes : msc::scan_bwd_ckpt_bytes(batch, L, d_inner, d_state);
+    if (cudaMallocAsync(&ck, ck_bytes, s) != cudaSuccess) return MSC_ERR_CUDA;
+    if (tma_ck) {
+        msc::ScanArgs sa{};
+        sa.u = u; sa.dt = dt; sa.A = A; sa.B = B; sa.C = C; sa.dt_bias = dt_bias; sa.h0 = h0;
+        const size_t half = p.ws_carry / 2 / sizeof(float);
+        sa.ws_a = static_cast<float*>(ck);
+        sa.ws_b = static_cast<float*>(ck) + half;
+        sa.batch = batch; sa.L = L; sa.d_inner = d_inner; sa.N = d_state;
+        sa.chunk = p.chunk; sa.K = p.K; sa.ntile = p.ntile; sa.vec = a.vec;
+        float* Bf = nullptr;
+        float* Cf = nullptr;
+        if (p.ws_bc) {
+            Bf = reinterpret_cast<float*>(static_cast<char*>(ck) + p.ws_carry);
+            Cf = reinterpret_cast<float*>(static_cast<char*>(ck) + p.ws_carry + p.ws_bc / 2);
+        }
+        e = msc::launch_scan_tma(sa, p, dtype, Bf, Cf, s);
+        a.ckpt = sa.ws_b;
+    } else {
+        a.ckpt = static_cast<float*>(ck);
+    }
+    if (e == cudaSuccess) e = msc::launch_scan_bwd(a, dtype, !tma_ck, s);
     const cudaError_t f = cudaFreeAsync(ck, s);
     if (e == cudaSuccess) e = f;
     return e == cudaSuccess ? MSC_OK : MSC_ERR_CUDA;

@@ -48,6 +48,7 @@ struct ScanPlan {
     size_t ws_carry;   // bytes of chunk summaries (a then b), 0 when K == 1
     size_t ws_bc;      // bytes of fp32 copies of B then C for the TMA boxes
     size_t ws_bytes;   // total workspace (carry, then B/C copies, 256-aligned)
+    int summaries_only;  // 1: stop after the chunk summaries and carry prefix (no outputs)
 };
 
 struct UpdateArgs {
@@ -86,8 +87,10 @@ struct ConvArgs {
 cudaError_t launch_causal_conv1d(const ConvArgs& a, msc_dtype dtype, cudaStream_t s);
 cudaError_t launch_conv1d_update(const ConvArgs& a, msc_dtype dtype, cudaStream_t s);
 
-// Backward pass of the scan (scan_bwd.cu).  ckpt: (batch, nseg, d_inner, N)
-// fp32 states entering each segment of the recompute.
+// Backward pass of the scan (scan_bwd.cu).  ckpt: (batch, nseg - 1, d_inner,
+// N) fp32 states entering segments 1 .. nseg-1 of the recompute (the layout
+// of the forward's chunk carries after the carry prefix); segment 0 starts
+// from h0 (or zero).
 struct BwdArgs {
     const void* u;
     const void* dt;
@@ -113,7 +116,10 @@ struct BwdArgs {
     int64_t batch, L, d_inner, N, nseg;
     int vec;           // 1: B/C rows can be read 4 elements at a time
 };
-cudaError_t launch_scan_bwd(const BwdArgs& a, msc_dtype dtype, cudaStream_t s);
+// generic_ckpt: compute the checkpoints with the element-load kernel first
+// (otherwise a.ckpt already holds them).
+cudaError_t launch_scan_bwd(const BwdArgs& a, msc_dtype dtype, bool generic_ckpt,
+                            cudaStream_t s);
 size_t scan_bwd_ckpt_bytes(int64_t batch, int64_t L, int64_t d_inner, int64_t N);
 constexpr int64_t kBwdSegment = 32;  // steps per recomputed segment
 

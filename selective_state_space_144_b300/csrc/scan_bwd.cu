@@ -4,16 +4,19 @@
 // D, z, dt_bias and h0, given dout and dlast_state.  The pages' design
 // recomputes the states instead of storing them ("Deep dive into Mamba",
 // section 7.3: chunk + recompute; the Mamba series article, section 3); here:
-//   1. scan_bwd_ckpt_kernel runs the forward recurrence once and keeps only
-//      the state entering every segment of kSeg steps (batch x segments x
-//      d_inner x N fp32);
+//   1. the checkpoints: the state entering every segment of kSeg steps
+//      (batch x (segments - 1) x d_inner x N fp32, segment 0 starting from
+//      h0) -- from the forward's TMA chunk summaries and carry prefix with
+//      chunks of kSeg steps where the shape allows, else from
+//      scan_bwd_ckpt_kernel, which runs the recurrence once keeping them;
 //   2. scan_bwd_kernel walks the segments from last to first: it recomputes
 //      the segment's states from its checkpoint into shared memory, then
 //      runs the adjoint recurrence backwards,
 //          dy_t = dout_t silu(z_t),  dh_t = C_t dy_t + exp(delta_{t+1} A) dh_{t+1},
 //      forming per step du, ddt (through softplus' = sigmoid) and dz (through
 //      silu'), and accumulating dA, dD, ddt_bias in registers and dB, dC (sums
-//      over channels) through a per-CTA shared-memory reduction and one
+//      over channels) in per-segment shared-memory accumulators (warp sums
+//      added there atomically, no barrier per step), flushed with one global
 //      atomic add per (batch, step, state) and CTA.
 // Thread layout as the element-load forward kernels: G lanes per channel,
 // 4 states per lane, 128 threads per CTA, grid (channel tiles, batch).
@@ -51,21 +54,25 @@ scan_bwd_ckpt_kernel(BwdArgs a) {
     const T* up = static_cast<const T*>(a.u) + base;
     const T* dtp = static_cast<const T*>(a.dt) + base;
     const T* Bp = static_cast<const T*>(a.B) + b * a.L * N;
-    float* ck = a.ckpt + (b * a.nseg * a.d_inner + d) * N;  // segment 0 of (b, d)
-    for (int64_t t = 0; t < a.L; ++t) {
-        if (t % kSeg == 0 && dvalid) {
-            float* c = ck + (t / kSeg) * a.d_inner * N;
+    // segment sg + 1 enters with the state after step (sg + 1) * kSeg - 1,
+    // kept at index sg (the layout of the forward's chunk carries)
+    for (int64_t sg = 0; sg < a.nseg - 1; ++sg) {
+#pragma unroll 8
+        for (int t = 0; t < kSeg; ++t) {
+            const int64_t off = (sg * kSeg + t) * a.d_inner;
+            const float delta = softplus(Elem<T>::load(dtp + off) + bias);
+            const float du = delta * Elem<T>::load(up + off);
+            float Bv[4];
+            load_row4<T, VEC>(Bp + (sg * kSeg + t) * N, n0, N, Bv);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) h[j] = fmaf(ex2(delta * A2[j]), h[j], du * Bv[j]);
+        }
+        if (dvalid) {
+            float* c = a.ckpt + ((b * (a.nseg - 1) + sg) * a.d_inner + d) * N;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 if (n0 + j < N) c[n0 + j] = h[j];
         }
-        const int64_t off = t * a.d_inner;
-        const float delta = softplus(Elem<T>::load(dtp + off) + bias);
-        const float du = delta * Elem<T>::load(up + off);
-        float Bv[4];
-        load_row4<T, VEC>(Bp + t * N, n0, N, Bv);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) h[j] = fmaf(ex2(delta * A2[j]), h[j], du * Bv[j]);
     }
 }
 
@@ -73,11 +80,11 @@ template <typename T, int G, bool VEC>
 __global__ void __launch_bounds__(kBwdThreads)
 scan_bwd_kernel(BwdArgs a) {
     constexpr int CPB = kBwdThreads / G;
-    constexpr int NW = kBwdThreads / 32;
-    extern __shared__ float4 hbuf[];          // [kSeg][kBwdThreads] states after each step
-    __shared__ float red[NW][2][64];          // per-warp partial dB, dC of one step
+    extern __shared__ float4 hbuf[];  // [kSeg][kBwdThreads] states after each step, then
+                                      // float acc[2][kSeg][N]: the segment's dB, dC sums
+    float* const acc = reinterpret_cast<float*>(hbuf + kSeg * kBwdThreads);
     const int g = threadIdx.x % G;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int64_t d_raw = (int64_t)blockIdx.x * CPB + threadIdx.x / G;
     const int64_t b = blockIdx.y;
     const bool dvalid = d_raw < a.d_inner;
@@ -108,36 +115,71 @@ scan_bwd_kernel(BwdArgs a) {
     for (int64_t sgi = a.nseg - 1; sgi >= 0; --sgi) {
         const int64_t t0 = sgi * kSeg;
         const int64_t t1 = min(t0 + kSeg, a.L);
+        for (int i = threadIdx.x; i < 2 * kSeg * N; i += kBwdThreads) acc[i] = 0.0f;
+        __syncthreads();
         // (1) recompute the segment's states from its checkpoint
         float hs0[4], h[4];
-        const float* ck = a.ckpt + ((b * a.nseg + sgi) * a.d_inner + d) * N;
+        const float* ck = sgi > 0 ? a.ckpt + ((b * (a.nseg - 1) + sgi - 1) * a.d_inner + d) * N
+                                  : (a.h0 ? a.h0 + (b * a.d_inner + d) * N : nullptr);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) hs0[j] = h[j] = (n0 + j < N) ? ck[n0 + j] : 0.0f;
-        for (int64_t t = t0; t < t1; ++t) {
-            const int64_t off = t * a.d_inner;
-            const float delta = softplus(Elem<T>::load(dtp + off) + bias);
-            const float du = delta * Elem<T>::load(up + off);
-            float Bv[4];
-            load_row4<T, VEC>(Bp + t * N, n0, N, Bv);
+        for (int j = 0; j < 4; ++j) hs0[j] = h[j] = (ck && n0 + j < N) ? ck[n0 + j] : 0.0f;
+        const int nk = (int)(t1 - t0);
+        const int64_t ds = a.d_inner;
+        {
+            const T* pdt = dtp + t0 * ds;
+            const T* pu = up + t0 * ds;
+            const T* pB = Bp + t0 * N;
+#pragma unroll 8
+            for (int k = 0; k < nk; ++k, pdt += ds, pu += ds, pB += N) {
+                const float delta = softplus(Elem<T>::load(pdt) + bias);
+                const float du = delta * Elem<T>::load(pu);
+                float Bv[4];
+                load_row4<T, VEC>(pB, n0, N, Bv);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) h[j] = fmaf(ex2(delta * A2[j]), h[j], du * Bv[j]);
-            hbuf[(t - t0) * kBwdThreads + threadIdx.x] = make_float4(h[0], h[1], h[2], h[3]);
+                for (int j = 0; j < 4; ++j) h[j] = fmaf(ex2(delta * A2[j]), h[j], du * Bv[j]);
+                hbuf[k * kBwdThreads + threadIdx.x] = make_float4(h[0], h[1], h[2], h[3]);
+            }
         }
-        // (2) the adjoint, last step of the segment first
-        for (int64_t t = t1 - 1; t >= t0; --t) {
-            const int64_t off = t * a.d_inner;
-            const float x = Elem<T>::load(dtp + off) + bias;
+        // (2) the adjoint, last step of the segment first; each step's global
+        // inputs are loaded one step ahead (before the previous step's
+        // reduction barrier) so that their latency overlaps it
+        struct In {
+            float dt, u, z, go, B[4], C[4];
+        };
+        // running pointers at the step being loaded (k - 1 while k is computed)
+        int64_t off_ld = (t1 - 1) * ds;
+        const T* pB = Bp + (t1 - 1) * N;
+        const T* pC = Cp + (t1 - 1) * N;
+        auto load_in = [&](In& v) {
+            v.dt = Elem<T>::load(dtp + off_ld);
+            v.u = Elem<T>::load(up + off_ld);
+            v.z = zp ? Elem<T>::load(zp + off_ld) : 0.0f;
+            v.go = dvalid ? Elem<T>::load(gp + off_ld) : 0.0f;
+            load_row4<T, VEC>(pB, n0, N, v.B);
+            load_row4<T, VEC>(pC, n0, N, v.C);
+        };
+        In nxt;
+        load_in(nxt);
+        int64_t off = off_ld;
+        for (int k = nk - 1; k >= 0; --k, off -= ds) {
+            const In cur = nxt;
+            if (k > 0) {
+                off_ld -= ds;
+                pB -= N;
+                pC -= N;
+                load_in(nxt);
+            }
+            const float x = cur.dt + bias;
             const float delta = softplus(x);
-            const float uu = Elem<T>::load(up + off);
-            const float go = dvalid ? Elem<T>::load(gp + off) : 0.0f;
-            float Bv[4], Cv[4];
-            load_row4<T, VEC>(Bp + t * N, n0, N, Bv);
-            load_row4<T, VEC>(Cp + t * N, n0, N, Cv);
-            const float4 hv = hbuf[(t - t0) * kBwdThreads + threadIdx.x];
+            const float uu = cur.u;
+            const float go = cur.go;
+            const float* Bv = cur.B;
+            const float* Cv = cur.C;
+            const float4 hv = hbuf[k * kBwdThreads + threadIdx.x];
             const float ht[4] = {hv.x, hv.y, hv.z, hv.w};
             float hp[4];
-            if (t > t0) {
-                const float4 pv = hbuf[(t - 1 - t0) * kBwdThreads + threadIdx.x];
+            if (k > 0) {
+                const float4 pv = hbuf[(k - 1) * kBwdThreads + threadIdx.x];
                 hp[0] = pv.x; hp[1] = pv.y; hp[2] = pv.z; hp[3] = pv.w;
             } else {
 #pragma unroll
@@ -152,7 +194,7 @@ scan_bwd_kernel(BwdArgs a) {
             y = fmaf(Dd, uu, y);
             float dy = go, dz = 0.0f;
             if (zp) {
-                const float zz = Elem<T>::load(zp + off);
+                const float zz = cur.z;
                 const float s = sigmoid_f(zz);
                 dy = go * zz * s;
                 dz = go * y * s * fmaf(zz, 1.0f - s, 1.0f);
@@ -194,25 +236,26 @@ scan_bwd_kernel(BwdArgs a) {
                     dCp[j] += __shfl_xor_sync(0xffffffffu, dCp[j], o);
                 }
             }
-            if (lane < G) {
+            if (lane < G) {  // the warp's sums into the segment accumulators
+                float* ab = acc + k * N;
+                float* ac = acc + (kSeg + k) * N;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     if (n0 + j < N) {
-                        red[warp][0][n0 + j] = dBp[j];
-                        red[warp][1][n0 + j] = dCp[j];
+                        atomicAdd(ab + n0 + j, dBp[j]);
+                        atomicAdd(ac + n0 + j, dCp[j]);
                     }
                 }
             }
-            __syncthreads();
-            if (threadIdx.x < 2 * N) {
-                const int which = threadIdx.x / N, n = threadIdx.x % N;
-                float v = 0.0f;
-#pragma unroll
-                for (int w = 0; w < NW; ++w) v += red[w][which][n];
-                atomicAdd((which ? a.dC : a.dB) + obase + t * N + n, v);
-            }
-            __syncthreads();
         }
+        // (3) the segment's dB, dC: one global add per (step, state) and CTA
+        __syncthreads();
+        for (int i = threadIdx.x; i < 2 * kSeg * N; i += kBwdThreads) {
+            const int which = i / (kSeg * N), r = i % (kSeg * N);
+            const int64_t t = t0 + r / N;
+            if (t < t1) atomicAdd((which ? a.dC : a.dB) + obase + t * N + r % N, acc[i]);
+        }
+        __syncthreads();
     }
     if (!dvalid) return;
     if (a.dh0) {
@@ -231,41 +274,47 @@ scan_bwd_kernel(BwdArgs a) {
 
 size_t scan_bwd_ckpt_bytes(int64_t batch, int64_t L, int64_t d_inner, int64_t N) {
     const int64_t nseg = (L + kSeg - 1) / kSeg;
-    return (size_t)batch * (size_t)(nseg > 0 ? nseg : 1) * (size_t)d_inner * (size_t)N *
+    return (size_t)batch * (size_t)(nseg > 1 ? nseg - 1 : 1) * (size_t)d_inner * (size_t)N *
            sizeof(float);
 }
 
 template <typename T, int G, bool VEC>
-static cudaError_t launch_bwd_g(BwdArgs a, cudaStream_t s) {
+static cudaError_t launch_bwd_g(BwdArgs a, bool generic_ckpt, cudaStream_t s) {
     constexpr int CPB = kBwdThreads / G;
     const dim3 grid((unsigned)((a.d_inner + CPB - 1) / CPB), (unsigned)a.batch);
-    scan_bwd_ckpt_kernel<T, G, VEC><<<grid, kBwdThreads, 0, s>>>(a);
-    const size_t smem = (size_t)kSeg * kBwdThreads * sizeof(float4);
+    if (generic_ckpt && a.nseg > 1) {
+        scan_bwd_ckpt_kernel<T, G, VEC><<<grid, kBwdThreads, 0, s>>>(a);
+        profile_count(1);
+    }
+    const size_t smem = (size_t)kSeg * kBwdThreads * sizeof(float4) +
+                        2 * (size_t)kSeg * (size_t)a.N * sizeof(float);
     auto kern = scan_bwd_kernel<T, G, VEC>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     const ProfileMark m = profile_begin(s, MSC_PROF_SCAN_BWD);
     kern<<<grid, kBwdThreads, smem, s>>>(a);
     profile_end(m, s);
-    profile_count(2);
+    profile_count(1);
     return cudaGetLastError();
 }
 
 template <typename T, bool VEC>
-static cudaError_t launch_bwd_v(const BwdArgs& a, cudaStream_t s) {
+static cudaError_t launch_bwd_v(const BwdArgs& a, bool gc, cudaStream_t s) {
     switch (lanes_per_channel(a.N)) {
-        case 1: return launch_bwd_g<T, 1, VEC>(a, s);
-        case 2: return launch_bwd_g<T, 2, VEC>(a, s);
-        case 4: return launch_bwd_g<T, 4, VEC>(a, s);
-        case 8: return launch_bwd_g<T, 8, VEC>(a, s);
-        default: return launch_bwd_g<T, 16, VEC>(a, s);
+        case 1: return launch_bwd_g<T, 1, VEC>(a, gc, s);
+        case 2: return launch_bwd_g<T, 2, VEC>(a, gc, s);
+        case 4: return launch_bwd_g<T, 4, VEC>(a, gc, s);
+        case 8: return launch_bwd_g<T, 8, VEC>(a, gc, s);
+        default: return launch_bwd_g<T, 16, VEC>(a, gc, s);
     }
 }
 
-cudaError_t launch_scan_bwd(const BwdArgs& a, msc_dtype dtype, cudaStream_t s) {
+cudaError_t launch_scan_bwd(const BwdArgs& a, msc_dtype dtype, bool generic_ckpt,
+                            cudaStream_t s) {
     if (dtype == MSC_BF16)
-        return a.vec ? launch_bwd_v<__nv_bfloat16, true>(a, s)
-                     : launch_bwd_v<__nv_bfloat16, false>(a, s);
-    return a.vec ? launch_bwd_v<float, true>(a, s) : launch_bwd_v<float, false>(a, s);
+        return a.vec ? launch_bwd_v<__nv_bfloat16, true>(a, generic_ckpt, s)
+                     : launch_bwd_v<__nv_bfloat16, false>(a, generic_ckpt, s);
+    return a.vec ? launch_bwd_v<float, true>(a, generic_ckpt, s)
+                 : launch_bwd_v<float, false>(a, generic_ckpt, s);
 }
 
 }  // namespace msc
