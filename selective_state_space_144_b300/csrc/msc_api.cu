@@ -437,7 +437,13 @@ msc_status msc_selective_scan_bwd(const void* u, const void* dt, const float* A,
     a.h0 = h0; a.dout = dout; a.dlast = dlast; a.du = du; a.ddt = ddt; a.dA = dA; a.dB = dB;
     a.dC = dC; a.dD = dD; a.dz = dz; a.ddt_bias = ddt_bias; a.dh0 = dh0;
     a.batch = batch; a.L = L; a.d_inner = d_inner; a.N = d_state;
-    a.nseg = (L + msc::kBwdSegment - 1) / msc::kBwdSegment;
+    // the TMA adjoint (tiles of tma_scan_tile(N) steps) where the shape allows,
+    // else the element-load adjoint (segments of kBwdSegment steps)
+    const bool v2 = g_scan_path == 0 && L > 0 &&
+                    msc::tma_scan_supported(d_state, d_inner, dtype, u, dt, z) &&
+                    msc::bwd_tma_supported(d_state, d_inner, dout);
+    const int64_t seg = v2 ? msc::tma_scan_tile(d_state) : msc::kBwdSegment;
+    a.nseg = (L + seg - 1) / seg;
     a.vec = (d_state % 4 == 0) && (!B || aligned(B, 4 * es)) && (!C || aligned(C, 4 * es));
     // the accumulated gradients start from zero
     cudaError_t e = cudaMemsetAsync(dA, 0, (size_t)dn * sizeof(float), s);
@@ -451,18 +457,23 @@ msc_status msc_selective_scan_bwd(const void* u, const void* dt, const float* A,
     // of one recompute segment when the shape allows, else the element-load
     // checkpoint kernel
     msc::ScanPlan p{};
-    bool tma_ck = g_scan_path == 0 && a.nseg >= 2 &&
+    bool tma_ck = g_scan_path == 0 && (v2 || a.nseg >= 2) &&
                   msc::tma_scan_supported(d_state, d_inner, dtype, u, dt, nullptr);
     if (tma_ck) {
         const bool need_bc = dtype == MSC_BF16 || !aligned(B, 16) || !aligned(C, 16);
         p = msc::make_tma_plan(batch, L, d_inner, d_state, sm_count(), a.nseg, g_min_chunk,
                                need_bc, g_scan_lanes);
         p.summaries_only = 1;
-        tma_ck = p.chunk == msc::kBwdSegment && p.K == a.nseg;
+        tma_ck = (a.nseg < 2 || p.chunk == seg) && p.K == a.nseg;
+    }
+    const bool use_v2 = v2 && tma_ck;
+    if (v2 && !use_v2) {  // checkpoints cannot come in tiles: element-load adjoint
+        a.nseg = (L + msc::kBwdSegment - 1) / msc::kBwdSegment;
+        tma_ck = false;
     }
     void* ck = nullptr;
-    const size_t ck_bytes =
-        tma_ck ? p.ws_bytes : msc::scan_bwd_ckpt_bytes(batch, L, d_inner, d_state);
+    size_t ck_bytes = tma_ck ? p.ws_bytes : msc::scan_bwd_ckpt_bytes(batch, L, d_inner, d_state);
+    if (ck_bytes == 0) ck_bytes = 256;
     if (cudaMallocAsync(&ck, ck_bytes, s) != cudaSuccess) return MSC_ERR_CUDA;
     if (tma_ck) {
         msc::ScanArgs sa{};
@@ -480,10 +491,13 @@ msc_status msc_selective_scan_bwd(const void* u, const void* dt, const float* A,
         }
         e = msc::launch_scan_tma(sa, p, dtype, Bf, Cf, s);
         a.ckpt = sa.ws_b;
+        if (use_v2 && e == cudaSuccess)
+            e = msc::launch_scan_bwd_tma(a, dtype, Bf ? Bf : static_cast<const float*>(B),
+                                         Cf ? Cf : static_cast<const float*>(C), s);
     } else {
         a.ckpt = static_cast<float*>(ck);
     }
-    if (e == cudaSuccess) e = msc::launch_scan_bwd(a, dtype, !tma_ck, s);
+    if (!use_v2 && e == cudaSuccess) e = msc::launch_scan_bwd(a, dtype, !tma_ck, s);
     const cudaError_t f = cudaFreeAsync(ck, s);
     if (e == cudaSuccess) e = f;
     return e == cudaSuccess ? MSC_OK : MSC_ERR_CUDA;

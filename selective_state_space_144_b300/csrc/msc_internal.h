@@ -121,6 +121,12 @@ struct BwdArgs {
 cudaError_t launch_scan_bwd(const BwdArgs& a, msc_dtype dtype, bool generic_ckpt,
                             cudaStream_t s);
 size_t scan_bwd_ckpt_bytes(int64_t batch, int64_t L, int64_t d_inner, int64_t N);
+// The TMA adjoint (scan_tma.cu): N in {8, 16, 32, 64}, d_inner % 8 == 0, 16-byte
+// aligned u / dt / z / dout; a.nseg tiles of tma_scan_tile(N) steps, a.ckpt the
+// states entering tiles 1 .. nseg-1; Bf / Cf fp32 B and C rows.
+bool bwd_tma_supported(int64_t N, int64_t d_inner, const void* dout);
+cudaError_t launch_scan_bwd_tma(const BwdArgs& a, msc_dtype dtype, const float* Bf,
+                                const float* Cf, cudaStream_t s);
 constexpr int64_t kBwdSegment = 32;  // steps per recomputed segment
 
 // Measurement hook (msc_api.cu): while enabled, launchers count kernels and

@@ -706,6 +706,296 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
     }
 }
 
+// Backward adjoint on TMA tiles.  One warp per CTA on CPW = 32/G channels of
+// one batch row, lane (ch, g) holding states g*NS .. of channel ch as fp32
+// pairs (the forward's layout).  The CTA walks the sequence's tiles of TT
+// steps from last to first through a TMA ring of S stages holding u, dt, z,
+// dout ([TT x CPW]) and B, C (fp32 [TT x N]).  Per tile:
+//   1. the states of the tile are recomputed from its entering state (the
+//      checkpoints of the forward's chunk summaries with TT-step chunks) and
+//      kept in shared memory, [TT][32 lanes][NS];
+//   2. the adjoint runs from the tile's last step to its first:
+//        dy = dout * silu(z),  dh = C dy + dh,  then per state
+//        dA += dh h_{t-1} a delta,  ddelta += dh h_{t-1} a A + (dh B) u,
+//        dB = dh delta u,  du += (dh B) delta,  dC = dy h_t,  dh *= a,
+//      with a = exp(delta A); ddelta and du are summed over the G lanes of
+//      the channel, dB and dC over the warp's channels (lanes G apart... here
+//      the CPW lanes of one state group) and written once per (step, state)
+//      to a tile buffer;
+//   3. the tile's dB, dC are added to global memory (one atomic add per
+//      (step, state) and CTA) and the stage is refilled.
+// dA, dD, ddt_bias accumulate in registers and are added once at the end.
+template <typename T, int G, int NS, int TT, int S>
+struct BwdLayout {
+    static constexpr int CPW = 32 / G;
+    static constexpr int N = G * NS;
+    static constexpr int kX = TT * CPW * (int)sizeof(T);  // u / dt / z / dout tile
+    static constexpr int kBC = TT * N * 4;                // B / C (fp32) tile
+    static constexpr int kStage = 4 * kX + 2 * kBC;
+    static constexpr int kH = S * kStage;                 // float [TT][32][NS] states
+    static constexpr int kDBC = kH + TT * 32 * NS * 4;    // float [TT][2][N] dB, dC
+    static constexpr int kBar = kDBC + TT * 2 * N * 4;
+    static constexpr int kTotal = kBar + S * 8;
+    static_assert(kX % 128 == 0 && kBC % 128 == 0, "TMA destinations must stay 128B aligned");
+};
+
+template <typename T, int G, int NS, int TT, int S>
+__global__ void __launch_bounds__(32)
+scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
+                    const __grid_constant__ CUtensorMap tm_dt,
+                    const __grid_constant__ CUtensorMap tm_z,
+                    const __grid_constant__ CUtensorMap tm_g,
+                    const __grid_constant__ CUtensorMap tm_B,
+                    const __grid_constant__ CUtensorMap tm_C, const BwdArgs a, const int ntile) {
+    using Lay = BwdLayout<T, G, NS, TT, S>;
+    constexpr int CPW = Lay::CPW;
+    constexpr int N = Lay::N;
+    constexpr int NP = NS / 2;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int lane = threadIdx.x;
+    const int ch = lane % CPW;
+    const int g = lane / CPW;
+    const int n0 = g * NS;
+    const int tile = (int)(blockIdx.x % ntile);
+    const int b = (int)(blockIdx.x / ntile);
+    const int d0 = tile * CPW;
+    const int64_t d = d0 + ch;
+    const int ntiles = (int)a.nseg;
+    const bool has_z = a.z != nullptr;
+    const uint32_t tx_bytes = (uint32_t)((3 + (has_z ? 1 : 0)) * Lay::kX + 2 * Lay::kBC);
+
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + Lay::kBar;
+    if (lane == 0) {
+        for (int s2 = 0; s2 < S; ++s2) mbar_init(bar0 + 8 * s2, 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tm_u);
+        prefetch_tensormap(&tm_dt);
+        prefetch_tensormap(&tm_g);
+        prefetch_tensormap(&tm_B);
+        prefetch_tensormap(&tm_C);
+        if (has_z) prefetch_tensormap(&tm_z);
+    }
+    __syncwarp();
+    // r-th tile in walking order = time tile ntiles-1-r, stage r % S
+    auto issue = [&](int r) {
+        const uint32_t st = sbase + (r % S) * Lay::kStage;
+        const uint32_t bar = bar0 + 8 * (r % S);
+        const int32_t tt = (int32_t)((int64_t)(ntiles - 1 - r) * TT);
+        mbar_expect_tx(bar, tx_bytes);
+        tma_load_3d(st, &tm_u, bar, d0, tt, b);
+        tma_load_3d(st + Lay::kX, &tm_dt, bar, d0, tt, b);
+        if (has_z) tma_load_3d(st + 2 * Lay::kX, &tm_z, bar, d0, tt, b);
+        tma_load_3d(st + 3 * Lay::kX, &tm_g, bar, d0, tt, b);
+        tma_load_3d(st + 4 * Lay::kX, &tm_B, bar, 0, tt, b);
+        tma_load_3d(st + 4 * Lay::kX + Lay::kBC, &tm_C, bar, 0, tt, b);
+    };
+    int issued = min(S, ntiles);
+    if (lane == 0)
+        for (int r = 0; r < issued; ++r) issue(r);
+
+    u64 A2[NP], An[NP], dh[NP], dAacc[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+        const float* Ar = a.A + d * N + n0 + 2 * i;
+        const float a0 = __ldg(Ar), a1 = __ldg(Ar + 1);
+        An[i] = pk2(a0, a1);
+        A2[i] = pk2(a0 * kLog2e, a1 * kLog2e);
+        dAacc[i] = pk2(0.0f, 0.0f);
+        dh[i] = pk2(0.0f, 0.0f);
+        if (a.dlast) {
+            const float* q = a.dlast + ((int64_t)b * a.d_inner + d) * N + n0 + 2 * i;
+            dh[i] = pk2(q[0], q[1]);
+        }
+    }
+    const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
+    const float Dd = a.D ? __ldg(a.D + d) : 0.0f;
+    float dDacc = 0.0f, dbacc = 0.0f;
+    float* const hb = reinterpret_cast<float*>(smem + Lay::kH);
+    float* const dbc = reinterpret_cast<float*>(smem + Lay::kDBC);
+    const int64_t rowL = (int64_t)b * a.L;  // (b, 0) row of the (batch, L, .) arrays
+
+    bool ok = true;
+    int waited = 0;
+    for (int r = 0; r < ntiles; ++r) {
+        const int it = ntiles - 1 - r;
+        const int64_t t0 = (int64_t)it * TT;
+        const int nst = (int)min((int64_t)TT, a.L - t0);
+        ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (r % S), (r / S) & 1, kWaitLimit));
+        if (!ok) break;
+        waited = r + 1;
+        const unsigned char* st = smem + (r % S) * Lay::kStage;
+        const T* su = reinterpret_cast<const T*>(st) + ch;
+        const T* sdt = reinterpret_cast<const T*>(st + Lay::kX) + ch;
+        const T* sz = reinterpret_cast<const T*>(st + 2 * Lay::kX) + ch;
+        const T* sg = reinterpret_cast<const T*>(st + 3 * Lay::kX) + ch;
+        const float* sB = reinterpret_cast<const float*>(st + 4 * Lay::kX) + n0;
+        const float* sC = reinterpret_cast<const float*>(st + 4 * Lay::kX + Lay::kBC) + n0;
+
+        // (1) the tile's entering state
+        u64 hin[NP];
+#pragma unroll
+        for (int i = 0; i < NP; ++i) hin[i] = pk2(0.0f, 0.0f);
+        const float* ck = it > 0
+            ? a.ckpt + (((int64_t)b * (ntiles - 1) + it - 1) * a.d_inner + d) * N + n0
+            : (a.h0 ? a.h0 + ((int64_t)b * a.d_inner + d) * N + n0 : nullptr);
+        if (ck) {
+#pragma unroll
+            for (int i = 0; i < NP; ++i) hin[i] = pk2(ck[2 * i], ck[2 * i + 1]);
+        }
+        // one recurrence step j of the tile on h, stored to buffer row j
+        auto fwd = [&](int j, u64 (&h)[NP]) {
+            const float delta = softplus(lds_elem<T>(sdt + j * CPW) + bias);
+            const float du = delta * lds_elem<T>(su + j * CPW);
+            const u64 dl2 = pk2(delta, delta), du2 = pk2(du, du);
+            u64* hs = reinterpret_cast<u64*>(hb + (j * 32 + lane) * NS);
+#pragma unroll
+            for (int i = 0; i < NP; ++i) {
+                const u64 x2 = mul2(dl2, A2[i]);
+                const u64 dA = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
+                const u64 Bq = *reinterpret_cast<const u64*>(sB + j * N + 2 * i);
+                h[i] = fma2(dA, h[i], mul2(du2, Bq));
+                hs[i] = h[i];
+            }
+        };
+        // (2) the adjoint, last step of the tile first
+        auto adj = [&](int j) {
+            const float x = lds_elem<T>(sdt + j * CPW) + bias;
+            const float delta = softplus(x);
+            const float sx = __fdividef(1.0f, 1.0f + ex2(-x * kLog2e));  // softplus'
+            const float uu = lds_elem<T>(su + j * CPW);
+            const float go = lds_elem<T>(sg + j * CPW);
+            const u64* hs = reinterpret_cast<const u64*>(hb + (j * 32 + lane) * NS);
+            const u64* hq =  // the step before (row 0 reads itself; hin is used then)
+                reinterpret_cast<const u64*>(hb + ((j > 0 ? j - 1 : 0) * 32 + lane) * NS);
+            u64 ht[NP], hp[NP], Bq[NP], Cq[NP];
+            u64 y2 = pk2(0.0f, 0.0f);
+#pragma unroll
+            for (int i = 0; i < NP; ++i) {
+                ht[i] = hs[i];
+                hp[i] = j > 0 ? hq[i] : hin[i];
+                Bq[i] = *reinterpret_cast<const u64*>(sB + j * N + 2 * i);
+                Cq[i] = *reinterpret_cast<const u64*>(sC + j * N + 2 * i);
+                y2 = fma2(Cq[i], ht[i], y2);
+            }
+            float y = lo2(y2) + hi2(y2);
+#pragma unroll
+            for (int o = CPW; o < 32; o <<= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+            y = fmaf(Dd, uu, y);
+            float dy = go, dz = 0.0f;
+            if (has_z) {
+                const float zz = lds_elem<T>(sz + j * CPW);
+                const float s = __fdividef(1.0f, 1.0f + ex2(-zz * kLog2e));
+                dy = go * zz * s;
+                dz = go * y * s * fmaf(zz, 1.0f - s, 1.0f);
+            }
+            const u64 dy2 = pk2(dy, dy), dl2 = pk2(delta, delta), u2 = pk2(uu, uu);
+            const u64 du2 = pk2(delta * uu, delta * uu);
+            u64 ddp = pk2(0.0f, 0.0f), dsp = pk2(0.0f, 0.0f), dBp[NP], dCp[NP];
+#pragma unroll
+            for (int i = 0; i < NP; ++i) {
+                const u64 x2 = mul2(dl2, A2[i]);
+                const u64 ea = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
+                dh[i] = fma2(Cq[i], dy2, dh[i]);
+                dCp[i] = mul2(dy2, ht[i]);
+                const u64 dae = mul2(mul2(dh[i], hp[i]), ea);
+                dAacc[i] = fma2(dae, dl2, dAacc[i]);
+                ddp = fma2(dae, An[i], ddp);
+                const u64 dhB = mul2(dh[i], Bq[i]);
+                ddp = fma2(dhB, u2, ddp);
+                dsp = fma2(dhB, dl2, dsp);
+                dBp[i] = mul2(dh[i], du2);
+                dh[i] = mul2(dh[i], ea);
+            }
+            float ddel = lo2(ddp) + hi2(ddp), dus = lo2(dsp) + hi2(dsp);
+#pragma unroll
+            for (int o = CPW; o < 32; o <<= 1) {
+                ddel += __shfl_xor_sync(0xffffffffu, ddel, o);
+                dus += __shfl_xor_sync(0xffffffffu, dus, o);
+            }
+            const float ddt = ddel * sx;
+            if (g == 0) {
+                const int64_t o = (rowL + t0 + j) * a.d_inner + d;
+                Elem<T>::store(static_cast<T*>(a.du) + o, fmaf(dy, Dd, dus));
+                Elem<T>::store(static_cast<T*>(a.ddt) + o, ddt);
+                if (a.dz) Elem<T>::store(static_cast<T*>(a.dz) + o, dz);
+                dDacc = fmaf(dy, uu, dDacc);
+                dbacc += ddt;
+            }
+            // dB, dC of this step: sum over the warp's channels (lanes 1 .. CPW-1 apart)
+#pragma unroll
+            for (int o = 1; o < CPW; o <<= 1) {
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    dBp[i] = add2(dBp[i], __shfl_xor_sync(0xffffffffu, dBp[i], o));
+                    dCp[i] = add2(dCp[i], __shfl_xor_sync(0xffffffffu, dCp[i], o));
+                }
+            }
+            if (ch == 0) {
+                u64* wb = reinterpret_cast<u64*>(dbc + j * 2 * N + n0);
+                u64* wc = reinterpret_cast<u64*>(dbc + j * 2 * N + N + n0);
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    wb[i] = dBp[i];
+                    wc[i] = dCp[i];
+                }
+            }
+        };
+        // (2) recompute the tile's states, then walk the adjoint back
+        {
+            u64 h[NP];
+#pragma unroll
+            for (int i = 0; i < NP; ++i) h[i] = hin[i];
+            if (nst == TT) {  // full tile: unrolled, constant shared-memory offsets
+#pragma unroll 8
+                for (int j = 0; j < TT; ++j) fwd(j, h);
+#pragma unroll 8
+                for (int j = TT - 1; j >= 0; --j) adj(j);
+            } else {
+                for (int j = 0; j < nst; ++j) fwd(j, h);
+                for (int j = nst - 1; j >= 0; --j) adj(j);
+            }
+        }
+        __syncwarp();
+        // (3) the tile's dB, dC into global memory, then refill its stage
+        for (int q = lane; q < nst * 2 * N; q += 32) {
+            const int j = q / (2 * N), rem = q % (2 * N);
+            float* dst = (rem < N ? a.dB : a.dC) + (rowL + t0 + j) * N + (rem % N);
+            atomicAdd(dst, dbc[q]);
+        }
+        __syncwarp();
+        if (r + S < ntiles) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(r + S);
+            }
+            issued = r + S + 1;
+        }
+    }
+    // copies still in flight (after a failed wait) land before exit
+    for (int r = waited; r < issued; ++r) mbar_wait(bar0 + 8 * (r % S), (r / S) & 1, kWaitLimit);
+    if (!ok) {
+        if (lane == 0) atomicOr(&g_scan_error, 1u);
+        return;
+    }
+    if (a.dh0) {
+        float* q = a.dh0 + ((int64_t)b * a.d_inner + d) * N + n0;
+#pragma unroll
+        for (int i = 0; i < NP; ++i)
+            *reinterpret_cast<float2*>(q + 2 * i) = make_float2(lo2(dh[i]), hi2(dh[i]));
+    }
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+        atomicAdd(a.dA + d * N + n0 + 2 * i, lo2(dAacc[i]));
+        atomicAdd(a.dA + d * N + n0 + 2 * i + 1, hi2(dAacc[i]));
+    }
+    if (g == 0) {
+        if (a.dD) atomicAdd(a.dD + d, dDacc);
+        if (a.ddt_bias) atomicAdd(a.ddt_bias + d, dbacc);
+    }
+}
+
 // B and C as fp32 rows for the [TT x N] fp32 TMA boxes; 8 elements per
 // thread when the arrays allow 16-byte bf16 reads, element-wise otherwise.
 template <typename T>
@@ -880,6 +1170,58 @@ cudaError_t scan_error_word(unsigned int* value, bool clear) {
         e = cudaMemcpyToSymbol(g_scan_error, &zero, sizeof(unsigned int));
     }
     return e;
+}
+
+template <typename T, int NS, int TT>
+static cudaError_t launch_bwd_tma_n(const BwdArgs& a, const float* Bf, const float* Cf,
+                                    cudaStream_t s) {
+    constexpr int G = 4, S = 2;
+    using Lay = BwdLayout<T, G, NS, TT, S>;
+    const CUtensorMapDataType tt =
+        sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const int es = (int)sizeof(T);
+    CUtensorMap mu, mdt, mz, mg, mB, mC;
+    if (!make_map(&mu, tt, es, a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_map(&mdt, tt, es, a.dt, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_map(&mz, tt, es, a.z ? a.z : a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_map(&mg, tt, es, a.dout, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_map(&mB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Bf, a.N, a.L, a.batch, (int)a.N, TT) ||
+        !make_map(&mC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Cf, a.N, a.L, a.batch, (int)a.N, TT))
+        return cudaErrorInvalidValue;
+    auto kern = scan_bwd_tma_kernel<T, G, NS, TT, S>;
+    const size_t smem = Lay::kTotal;
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const int ntile = (int)(a.d_inner / Lay::CPW);
+    const ProfileMark m = profile_begin(s, MSC_PROF_SCAN_BWD);
+    kern<<<(unsigned)(a.batch * ntile), 32, smem, s>>>(mu, mdt, mz, mg, mB, mC, a, ntile);
+    profile_end(m, s);
+    profile_count(1);
+    return cudaGetLastError();
+}
+
+bool bwd_tma_supported(int64_t N, int64_t d_inner, const void* dout) {
+    return (N == 8 || N == 16 || N == 32 || N == 64) && d_inner % 8 == 0 &&
+           (reinterpret_cast<uintptr_t>(dout) & 15) == 0 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_scan_bwd_tma(const BwdArgs& a, msc_dtype dtype, const float* Bf,
+                                const float* Cf, cudaStream_t s) {
+    const bool bf = dtype == MSC_BF16;
+    switch (a.N) {
+        case 8:
+            return bf ? launch_bwd_tma_n<__nv_bfloat16, 2, 32>(a, Bf, Cf, s)
+                      : launch_bwd_tma_n<float, 2, 32>(a, Bf, Cf, s);
+        case 16:
+            return bf ? launch_bwd_tma_n<__nv_bfloat16, 4, 32>(a, Bf, Cf, s)
+                      : launch_bwd_tma_n<float, 4, 32>(a, Bf, Cf, s);
+        case 32:
+            return bf ? launch_bwd_tma_n<__nv_bfloat16, 8, 16>(a, Bf, Cf, s)
+                      : launch_bwd_tma_n<float, 8, 16>(a, Bf, Cf, s);
+        default:
+            return bf ? launch_bwd_tma_n<__nv_bfloat16, 16, 16>(a, Bf, Cf, s)
+                      : launch_bwd_tma_n<float, 16, 16>(a, Bf, Cf, s);
+    }
 }
 
 }  // namespace msc
