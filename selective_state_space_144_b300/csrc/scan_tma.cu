@@ -722,8 +722,8 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
 //      the channel, dB and dC over the warp's channels (lanes G apart... here
 //      the CPW lanes of one state group) and written once per (step, state)
 //      to a tile buffer;
-//   3. the tile's dB, dC are added to global memory (one atomic add per
-//      (step, state) and CTA) and the stage is refilled.
+//   3. the tile's dB, dC are added to global memory (16-byte vector atomic
+//      adds, one per 4 states of a step and CTA) and the stage is refilled.
 // dA, dD, ddt_bias accumulate in registers and are added once at the end.
 template <typename T, int G, int NS, int TT, int S>
 struct BwdLayout {
@@ -959,10 +959,11 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
         }
         __syncwarp();
         // (3) the tile's dB, dC into global memory, then refill its stage
-        for (int q = lane; q < nst * 2 * N; q += 32) {
-            const int j = q / (2 * N), rem = q % (2 * N);
+        for (int q = lane; q < nst * 2 * N / 4; q += 32) {  // 4 states per vector add
+            const int e = q * 4;
+            const int j = e / (2 * N), rem = e % (2 * N);
             float* dst = (rem < N ? a.dB : a.dC) + (rowL + t0 + j) * N + (rem % N);
-            atomicAdd(dst, dbc[q]);
+            red_add_v4(dst, *reinterpret_cast<const float4*>(dbc + e));
         }
         __syncwarp();
         if (r + S < ntiles) {
