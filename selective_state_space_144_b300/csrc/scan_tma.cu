@@ -1132,7 +1132,8 @@ static cudaError_t launch_tma_t(const ScanArgs& a, const ScanPlan& p, const floa
     }
     switch (a.N) {
         case 8: return launch_tma_ns<T, 4, 2, 32, 3>(a, p, Bf, Cf, s);
-        case 16: return launch_tma_ns<T, 4, 4, 32, 3>(a, p, Bf, Cf, s);
+        case 16: return launch_tma_ns<T, 4, 4, 32, 2>(a, p, Bf, Cf, s);  // 2 stages: measured
+                                                                          // equal or faster
         case 32: return launch_tma_ns<T, 4, 8, 16, 3>(a, p, Bf, Cf, s);
         default: return launch_tma_ns<T, 4, 16, 16, 2>(a, p, Bf, Cf, s);
     }
