@@ -209,8 +209,10 @@ msc_status msc_causal_conv1d_update(
  *   dh0           : (batch, d_inner, d_state) fp32, nullable (not written)
  * dA, dB, dC, dD, ddt_bias are accumulated with atomic adds after being
  * zeroed by the call: their last bits depend on the order of the adds.
- * Scratch: the checkpoints, batch * ceil(L/32) * d_inner * d_state * 4 bytes,
- * taken stream-ordered.  batch <= 65535.  Errors as msc_selective_scan_fwd.
+ * Scratch, taken stream-ordered: the checkpoints, batch * d_inner * d_state
+ * * 4 bytes per 16 steps (d_state <= 16 on the TMA path) or 8 steps
+ * (d_state 32, 64) or 32 steps (element-load path), plus fp32 copies of B
+ * and C for bf16 storage.  batch <= 65535.  Errors as msc_selective_scan_fwd.
  */
 msc_status msc_selective_scan_bwd(
     const void* u, const void* dt, const float* A, const void* B, const void* C,
@@ -320,6 +322,17 @@ msc_status msc_selective_state_update_trap(
  * otherwise; a nonzero `clear` resets it.  MSC_ERR_CUDA if the read fails.
  */
 msc_status msc_check_device_error(int clear);
+
+/*
+ * Calls that take scratch stream-ordered (msc_selective_scan_fwd,
+ * msc_selective_scan_fwd_ex without a workspace, the trapezoid scan and
+ * msc_selective_scan_bwd) draw it from a memory pool that the library keeps
+ * on each device and that holds on to the memory it has reserved, so that
+ * repeated calls do not map memory again.  This returns the pools' unused
+ * memory to the device (cudaMemPoolTrimTo); memory of calls still in flight
+ * on some stream stays reserved.  MSC_ERR_CUDA if a trim fails.
+ */
+msc_status msc_scratch_release(void);
 
 /*
  * Plan overrides, for measurement and tuning.  Keys:

@@ -23,7 +23,7 @@ import os
 __all__ = [
     "MscError", "selective_scan_fwd", "selective_scan_fwd_ws",
     "selective_state_update", "scan_workspace_size", "tuning_set",
-    "check_device_error", "profile_enable", "profile_read",
+    "check_device_error", "scratch_release", "profile_enable", "profile_read",
     "library_path", "load",
 ]
 
@@ -104,6 +104,8 @@ def load():
     lib.msc_version.argtypes = []
     lib.msc_check_device_error.restype = st
     lib.msc_check_device_error.argtypes = [ctypes.c_int]
+    lib.msc_scratch_release.restype = st
+    lib.msc_scratch_release.argtypes = []
     lib.msc_profile_enable.restype = st
     lib.msc_profile_enable.argtypes = [ctypes.c_int]
     lib.msc_profile_read.restype = st
@@ -442,6 +444,11 @@ def check_device_error(clear: bool = True):
     """Raise MscError(MSC_ERR_TIMEOUT) if a kernel's bounded wait gave up.
     Synchronise the streams used first."""
     _check("msc_check_device_error", load().msc_check_device_error(int(clear)))
+
+
+def scratch_release():
+    """Return the memory the library's scratch pools hold unused to the device."""
+    _check("msc_scratch_release", load().msc_scratch_release())
 
 
 def profile_enable(on: bool = True):

@@ -42,6 +42,40 @@ int sm_count() {
     return n;
 }
 
+// Stream-ordered scratch comes from a memory pool of the library's own on
+// each device, which keeps the memory it has reserved between calls (release
+// threshold at the maximum): with the device's default pool, whose threshold
+// is zero, every synchronisation returns the memory and the next call maps it
+// afresh (about 0.2 ms for the 100 MB of a backward call).  The memory stays
+// reserved for the process until msc_scratch_release.
+constexpr int kMaxDevices = 64;
+std::mutex g_pool_mu;
+cudaMemPool_t g_pools[kMaxDevices] = {};
+
+cudaMemPool_t scratch_pool() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    if (!g_pools[dev]) {
+        cudaMemPoolProps props{};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        if (cudaMemPoolCreate(&p, &props) != cudaSuccess) return nullptr;
+        uint64_t keep = std::numeric_limits<uint64_t>::max();
+        cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+        g_pools[dev] = p;
+    }
+    return g_pools[dev];
+}
+
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s) {
+    cudaMemPool_t pool = scratch_pool();
+    return pool ? cudaMallocFromPoolAsync(p, bytes, pool, s) : cudaMallocAsync(p, bytes, s);
+}
+
 struct ScanCheck {
     msc_status st;
     msc::ScanPlan plan;
@@ -180,7 +214,7 @@ static msc_status run_scan(const void* u, const void* dt, const float* A, const 
     void* w = ws;
     if (need > 0) {
         if (own_ws) {
-            if (cudaMallocAsync(&w, need, s) != cudaSuccess) return MSC_ERR_CUDA;
+            if (scratch_alloc(&w, need, s) != cudaSuccess) return MSC_ERR_CUDA;
         } else if (!ws || ws_bytes < need || !aligned(ws, 256)) {
             return MSC_ERR_WORKSPACE;
         }
@@ -437,13 +471,11 @@ msc_status msc_selective_scan_bwd(const void* u, const void* dt, const float* A,
     a.h0 = h0; a.dout = dout; a.dlast = dlast; a.du = du; a.ddt = ddt; a.dA = dA; a.dB = dB;
     a.dC = dC; a.dD = dD; a.dz = dz; a.ddt_bias = ddt_bias; a.dh0 = dh0;
     a.batch = batch; a.L = L; a.d_inner = d_inner; a.N = d_state;
-    // the TMA adjoint (tiles of tma_scan_tile(N) steps) where the shape allows,
-    // else the element-load adjoint (segments of kBwdSegment steps)
+    // the TMA backward (checkpoints and adjoint in one kernel) where the shape
+    // allows, else the element-load checkpoint and adjoint kernels
     const bool v2 = g_scan_path == 0 && L > 0 &&
-                    msc::tma_scan_supported(d_state, d_inner, dtype, u, dt, z) &&
-                    msc::bwd_tma_supported(d_state, d_inner, dout);
-    const int64_t seg = v2 ? msc::tma_scan_tile(d_state) : msc::kBwdSegment;
-    a.nseg = (L + seg - 1) / seg;
+                    msc::bwd_tma_supported(d_state, d_inner, u, dt, z, dout, dB, dC);
+    a.nseg = (L + msc::kBwdSegment - 1) / msc::kBwdSegment;
     a.vec = (d_state % 4 == 0) && (!B || aligned(B, 4 * es)) && (!C || aligned(C, 4 * es));
     // the accumulated gradients start from zero
     cudaError_t e = cudaMemsetAsync(dA, 0, (size_t)dn * sizeof(float), s);
@@ -453,51 +485,17 @@ msc_status msc_selective_scan_bwd(const void* u, const void* dt, const float* A,
     if (e == cudaSuccess && ddt_bias)
         e = cudaMemsetAsync(ddt_bias, 0, (size_t)d_inner * sizeof(float), s);
     if (e != cudaSuccess) return MSC_ERR_CUDA;
-    // checkpoints: the forward's TMA chunk summaries + carry prefix with chunks
-    // of one recompute segment when the shape allows, else the element-load
-    // checkpoint kernel
-    msc::ScanPlan p{};
-    bool tma_ck = g_scan_path == 0 && (v2 || a.nseg >= 2) &&
-                  msc::tma_scan_supported(d_state, d_inner, dtype, u, dt, nullptr);
-    if (tma_ck) {
-        const bool need_bc = dtype == MSC_BF16 || !aligned(B, 16) || !aligned(C, 16);
-        p = msc::make_tma_plan(batch, L, d_inner, d_state, sm_count(), a.nseg, g_min_chunk,
-                               need_bc, g_scan_lanes);
-        p.summaries_only = 1;
-        tma_ck = (a.nseg < 2 || p.chunk == seg) && p.K == a.nseg;
-    }
-    const bool use_v2 = v2 && tma_ck;
-    if (v2 && !use_v2) {  // checkpoints cannot come in tiles: element-load adjoint
-        a.nseg = (L + msc::kBwdSegment - 1) / msc::kBwdSegment;
-        tma_ck = false;
-    }
     void* ck = nullptr;
-    size_t ck_bytes = tma_ck ? p.ws_bytes : msc::scan_bwd_ckpt_bytes(batch, L, d_inner, d_state);
+    size_t ck_bytes = v2 ? msc::scan_bwd_tma_scratch(a, dtype)
+                         : msc::scan_bwd_ckpt_bytes(batch, L, d_inner, d_state);
     if (ck_bytes == 0) ck_bytes = 256;
-    if (cudaMallocAsync(&ck, ck_bytes, s) != cudaSuccess) return MSC_ERR_CUDA;
-    if (tma_ck) {
-        msc::ScanArgs sa{};
-        sa.u = u; sa.dt = dt; sa.A = A; sa.B = B; sa.C = C; sa.dt_bias = dt_bias; sa.h0 = h0;
-        const size_t half = p.ws_carry / 2 / sizeof(float);
-        sa.ws_a = static_cast<float*>(ck);
-        sa.ws_b = static_cast<float*>(ck) + half;
-        sa.batch = batch; sa.L = L; sa.d_inner = d_inner; sa.N = d_state;
-        sa.chunk = p.chunk; sa.K = p.K; sa.ntile = p.ntile; sa.vec = a.vec;
-        float* Bf = nullptr;
-        float* Cf = nullptr;
-        if (p.ws_bc) {
-            Bf = reinterpret_cast<float*>(static_cast<char*>(ck) + p.ws_carry);
-            Cf = reinterpret_cast<float*>(static_cast<char*>(ck) + p.ws_carry + p.ws_bc / 2);
-        }
-        e = msc::launch_scan_tma(sa, p, dtype, Bf, Cf, s);
-        a.ckpt = sa.ws_b;
-        if (use_v2 && e == cudaSuccess)
-            e = msc::launch_scan_bwd_tma(a, dtype, Bf ? Bf : static_cast<const float*>(B),
-                                         Cf ? Cf : static_cast<const float*>(C), s);
+    if (scratch_alloc(&ck, ck_bytes, s) != cudaSuccess) return MSC_ERR_CUDA;
+    if (v2) {
+        e = msc::launch_scan_bwd_tma(a, dtype, ck, s);
     } else {
         a.ckpt = static_cast<float*>(ck);
+        e = msc::launch_scan_bwd(a, dtype, true, s);
     }
-    if (!use_v2 && e == cudaSuccess) e = msc::launch_scan_bwd(a, dtype, !tma_ck, s);
     const cudaError_t f = cudaFreeAsync(ck, s);
     if (e == cudaSuccess) e = f;
     return e == cudaSuccess ? MSC_OK : MSC_ERR_CUDA;
@@ -612,6 +610,13 @@ msc_status msc_check_device_error(int clear) {
     unsigned int v = 0;
     if (msc::scan_error_word(&v, clear != 0) != cudaSuccess) return MSC_ERR_CUDA;
     return v ? MSC_ERR_TIMEOUT : MSC_OK;
+}
+
+msc_status msc_scratch_release(void) {
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    for (cudaMemPool_t p : g_pools)
+        if (p && cudaMemPoolTrimTo(p, 0) != cudaSuccess) return MSC_ERR_CUDA;
+    return MSC_OK;
 }
 
 const char* msc_status_string(msc_status s) {

@@ -109,6 +109,12 @@ template <typename T> struct Elem;
 template <> struct Elem<float> {
     static __device__ __forceinline__ float load(const float* p) { return __ldg(p); }
     static __device__ __forceinline__ void store(float* p, float v) { *p = v; }
+    // store under a predicate, without a branch
+    static __device__ __forceinline__ void store_if(bool pred, float* p, float v) {
+        asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+                     "@q st.global.f32 [%0], %1;\n\t}" ::"l"(p), "f"(v), "r"((int)pred)
+                     : "memory");
+    }
     // 4 consecutive elements, p 16-byte aligned
     static __device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
         const float4 q = __ldg(reinterpret_cast<const float4*>(p));
@@ -126,6 +132,12 @@ template <> struct Elem<__nv_bfloat16> {
     }
     static __device__ __forceinline__ void store(__nv_bfloat16* p, float v) {
         *p = __float2bfloat16_rn(v);
+    }
+    static __device__ __forceinline__ void store_if(bool pred, __nv_bfloat16* p, float v) {
+        const unsigned short b = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+                     "@q st.global.b16 [%0], %1;\n\t}" ::"l"(p), "h"(b), "r"((int)pred)
+                     : "memory");
     }
     // 4 consecutive elements, p 8-byte aligned
     static __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {

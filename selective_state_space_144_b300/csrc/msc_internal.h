@@ -87,10 +87,10 @@ struct ConvArgs {
 cudaError_t launch_causal_conv1d(const ConvArgs& a, msc_dtype dtype, cudaStream_t s);
 cudaError_t launch_conv1d_update(const ConvArgs& a, msc_dtype dtype, cudaStream_t s);
 
-// Backward pass of the scan (scan_bwd.cu).  ckpt: (batch, nseg - 1, d_inner,
-// N) fp32 states entering segments 1 .. nseg-1 of the recompute (the layout
-// of the forward's chunk carries after the carry prefix); segment 0 starts
-// from h0 (or zero).
+// Backward pass of the scan.  Element-load path (scan_bwd.cu): ckpt is
+// (batch, nseg - 1, d_inner, N) fp32, the states entering segments
+// 1 .. nseg-1 of the recompute; segment 0 starts from h0 (or zero).  TMA path
+// (scan_tma.cu): ckpt is the kernel's own scratch, nseg its tile count.
 struct BwdArgs {
     const void* u;
     const void* dt;
@@ -121,12 +121,15 @@ struct BwdArgs {
 cudaError_t launch_scan_bwd(const BwdArgs& a, msc_dtype dtype, bool generic_ckpt,
                             cudaStream_t s);
 size_t scan_bwd_ckpt_bytes(int64_t batch, int64_t L, int64_t d_inner, int64_t N);
-// The TMA adjoint (scan_tma.cu): N in {8, 16, 32, 64}, d_inner % 8 == 0, 16-byte
-// aligned u / dt / z / dout; a.nseg tiles of tma_scan_tile(N) steps, a.ckpt the
-// states entering tiles 1 .. nseg-1; Bf / Cf fp32 B and C rows.
-bool bwd_tma_supported(int64_t N, int64_t d_inner, const void* dout);
-cudaError_t launch_scan_bwd_tma(const BwdArgs& a, msc_dtype dtype, const float* Bf,
-                                const float* Cf, cudaStream_t s);
+// The TMA backward (scan_tma.cu): N in {8, 16, 32, 64}, d_inner % 8 == 0,
+// 16-byte aligned u / dt / z / dout / dB / dC.  One kernel walks each
+// channel group forward (checkpoints every bwd_tma_tile(N) steps) and back;
+// `scratch` holds scan_bwd_tma_scratch() bytes (checkpoints, fp32 B / C).
+int bwd_tma_tile(int64_t N);
+bool bwd_tma_supported(int64_t N, int64_t d_inner, const void* u, const void* dt, const void* z,
+                       const void* dout, const void* dB, const void* dC);
+size_t scan_bwd_tma_scratch(const BwdArgs& a, msc_dtype dtype);
+cudaError_t launch_scan_bwd_tma(BwdArgs a, msc_dtype dtype, void* scratch, cudaStream_t s);
 constexpr int64_t kBwdSegment = 32;  // steps per recomputed segment
 
 // Measurement hook (msc_api.cu): while enabled, launchers count kernels and

@@ -67,6 +67,29 @@ __device__ __forceinline__ void red_add_v4(float* p, float4 v) {
                  : "memory");
 }
 
+// Atomic add of 2 consecutive floats (8-byte aligned) in global memory.
+__device__ __forceinline__ void red_add_v2(float* p, float2 v) {
+    asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(v.x), "f"(v.y)
+                 : "memory");
+}
+
+// The two atomic adds above under a predicate instead of a branch, so that
+// a loop that issues them stays one basic block.
+__device__ __forceinline__ void red_add_v4_if(bool pred, float* p, float4 v) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n\t}" ::"l"(p),
+        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"((int)pred)
+        : "memory");
+}
+__device__ __forceinline__ void red_add_v2_if(bool pred, float* p, float2 v) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %3, 0;\n\t"
+        "@q red.global.add.v2.f32 [%0], {%1, %2};\n\t}" ::"l"(p),
+        "f"(v.x), "f"(v.y), "r"((int)pred)
+        : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(

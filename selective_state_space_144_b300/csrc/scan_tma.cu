@@ -706,51 +706,122 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
     }
 }
 
-// Backward adjoint on TMA tiles.  One warp per CTA on CPW = 32/G channels of
-// one batch row, lane (ch, g) holding states g*NS .. of channel ch as fp32
-// pairs (the forward's layout).  The CTA walks the sequence's tiles of TT
-// steps from last to first through a TMA ring of S stages holding u, dt, z,
-// dout ([TT x CPW]) and B, C (fp32 [TT x N]).  Per tile:
-//   1. the states of the tile are recomputed from its entering state (the
-//      checkpoints of the forward's chunk summaries with TT-step chunks) and
-//      kept in shared memory, [TT][32 lanes][NS];
-//   2. the adjoint runs from the tile's last step to its first:
-//        dy = dout * silu(z),  dh = C dy + dh,  then per state
-//        dA += dh h_{t-1} a delta,  ddelta += dh h_{t-1} a A + (dh B) u,
-//        dB = dh delta u,  du += (dh B) delta,  dC = dy h_t,  dh *= a,
-//      with a = exp(delta A); ddelta and du are summed over the G lanes of
-//      the channel, dB and dC over the warp's channels (lanes G apart... here
-//      the CPW lanes of one state group) and written once per (step, state)
-//      to a tile buffer;
-//   3. the tile's dB, dC are added to global memory (16-byte vector atomic
-//      adds, one per 4 states of a step and CTA) and the stage is refilled.
-// dA, dD, ddt_bias accumulate in registers and are added once at the end.
-template <typename T, int G, int NS, int TT, int S>
+// Backward of the Euler scan on TMA tiles, checkpoints included.  One warp
+// per CTA on CPW = 8 channels of one batch row, lane (ch, g) = (l % 8, l / 8)
+// holding states g*NS .. g*NS+NS-1 of channel ch as fp32 pairs (the
+// forward's lane layout).  The sequence is cut into tiles of TT steps, and
+// the CTA makes one pass of 2*nt - 1 rounds over them through a TMA ring of
+// S stages:
+//   * forward rounds, tiles 0 .. nt-2 (u, dt, B loaded): the recurrence from
+//     h0 (or zero), the state entering each next tile stored to the CTA's
+//     own checkpoint rows in global memory (they stay in L2);
+//   * reverse rounds, tiles nt-1 .. 0 (u, dt, z, dout, B, C loaded):
+//       1. a tile prologue: every lane computes the per-(step, channel)
+//          scalars for TT/4 of the tile's (step, channel) pairs -- delta,
+//          delta*u, dy = dout*silu(z), u, softplus'(x) = sigmoid(x) and the
+//          gate's slope for dz -- once, into a table in shared memory;
+//       2. the tile's states recomputed from its entering state (the
+//          forward's registers for the last tile, a checkpoint otherwise)
+//          into a per-lane buffer, [TT][32 lanes][NS];
+//       3. the adjoint from the tile's last step to its first, per state:
+//            dh += C dy;  dC = dy h_t;  dae = dh h_{t-1} a   (a = e^{delta A})
+//            dA += dae delta;  ddelta += dae A;  S += dh B;  dB = dh delta u;
+//            dh *= a
+//          then ddelta += u S and du = dy D + delta S over the channel's
+//          states: (y, ddelta, S) are reduce-scattered over the 4 lanes of
+//          the channel, so that lane g = 0, 1, 2 ends with one of them and
+//          writes dz, ddt or du -- one store per lane and step; dB and dC
+//          are reduce-scattered over the 8 channels (lane bit 2 picks dB or
+//          dC) and added to global memory with one vector atomic add per
+//          lane with ch % 4 == 0.
+// dA, dD, ddt_bias accumulate in registers and are added once at the end;
+// dh after tile 0 is dh0.  Steps past L in the last tile get delta = 0,
+// dy = 0 (the state and the adjoint pass through) and store nothing.
+template <typename T, int NS, int TT, int S>
 struct BwdLayout {
+    static constexpr int G = 4;
     static constexpr int CPW = 32 / G;
     static constexpr int N = G * NS;
     static constexpr int kX = TT * CPW * (int)sizeof(T);  // u / dt / z / dout tile
     static constexpr int kBC = TT * N * 4;                // B / C (fp32) tile
+    static constexpr int kBoff = 4 * kX;
+    static constexpr int kCoff = kBoff + kBC;
     static constexpr int kStage = 4 * kX + 2 * kBC;
-    static constexpr int kH = S * kStage;                 // float [TT][32][NS] states
-    static constexpr int kDBC = kH + TT * 32 * NS * 4;    // float [TT][2][N] dB, dC
-    static constexpr int kBar = kDBC + TT * 2 * N * 4;
+    static constexpr int kTab = S * kStage;               // float4 [TT][CPW]: delta, delta*u, dy, u
+    static constexpr int kTab2 = kTab + TT * CPW * 16;    // float2 [TT][CPW]: sigmoid(x), dz slope
+    static constexpr int kH = kTab2 + TT * CPW * 8;       // float [TT][NS/HV][32][HV] states
+    static constexpr int kBar = kH + TT * 32 * NS * 4;
     static constexpr int kTotal = kBar + S * 8;
+    static constexpr int HV = NS >= 4 ? 4 : 2;            // floats per state-buffer vector
     static_assert(kX % 128 == 0 && kBC % 128 == 0, "TMA destinations must stay 128B aligned");
+    static_assert(TT % G == 0 && NS % 2 == 0, "tile and state split");
 };
 
-template <typename T, int G, int NS, int TT, int S>
-__global__ void __launch_bounds__(32)
+// NP = NS/2 state pairs at p (16-byte aligned when NP is even).
+template <int NP>
+__device__ __forceinline__ void ld_pairs(const float* p, u64 (&v)[NP]) {
+    if constexpr (NP % 2 == 0) {
+#pragma unroll
+        for (int c = 0; c < NP / 2; ++c) {
+            const ulonglong2 q = reinterpret_cast<const ulonglong2*>(p)[c];
+            v[2 * c] = q.x;
+            v[2 * c + 1] = q.y;
+        }
+    } else {
+        v[0] = *reinterpret_cast<const u64*>(p);
+    }
+}
+template <int NP>
+__device__ __forceinline__ void st_pairs(float* p, const u64 (&v)[NP]) {
+    if constexpr (NP % 2 == 0) {
+#pragma unroll
+        for (int c = 0; c < NP / 2; ++c)
+            reinterpret_cast<ulonglong2*>(p)[c] = make_ulonglong2(v[2 * c], v[2 * c + 1]);
+    } else {
+        *reinterpret_cast<u64*>(p) = v[0];
+    }
+}
+
+// The lane's states of step j in the state buffer: NS/HV vectors of HV
+// floats, 32 lanes apart, so that a warp's vector access is contiguous.
+template <int NS, int HV>
+__device__ __forceinline__ void hbuf_st(float* hb, int j, int lane, const u64 (&h)[NS / 2]) {
+    constexpr int NC = NS / HV, PV = HV / 2;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        u64 v[PV];
+#pragma unroll
+        for (int k = 0; k < PV; ++k) v[k] = h[c * PV + k];
+        st_pairs<PV>(hb + ((j * NC + c) * 32 + lane) * HV, v);
+    }
+}
+template <int NS, int HV>
+__device__ __forceinline__ void hbuf_ld(const float* hb, int j, int lane, u64 (&h)[NS / 2]) {
+    constexpr int NC = NS / HV, PV = HV / 2;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        u64 v[PV];
+        ld_pairs<PV>(hb + ((j * NC + c) * 32 + lane) * HV, v);
+#pragma unroll
+        for (int k = 0; k < PV; ++k) h[c * PV + k] = v[k];
+    }
+}
+
+template <typename T, int NS, int TT, int S>
+__global__ void __launch_bounds__(32, NS >= 16 ? 8 : 11)  // the grid's CTAs per SM
 scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
                     const __grid_constant__ CUtensorMap tm_dt,
                     const __grid_constant__ CUtensorMap tm_z,
                     const __grid_constant__ CUtensorMap tm_g,
                     const __grid_constant__ CUtensorMap tm_B,
                     const __grid_constant__ CUtensorMap tm_C, const BwdArgs a, const int ntile) {
-    using Lay = BwdLayout<T, G, NS, TT, S>;
+    using Lay = BwdLayout<T, NS, TT, S>;
+    constexpr int G = Lay::G;
     constexpr int CPW = Lay::CPW;
     constexpr int N = Lay::N;
     constexpr int NP = NS / 2;
+    constexpr int HV = Lay::HV;
+    constexpr int PQ = TT / G;  // prologue (step, channel) pairs per lane and tile
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int lane = threadIdx.x;
@@ -761,9 +832,11 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
     const int b = (int)(blockIdx.x / ntile);
     const int d0 = tile * CPW;
     const int64_t d = d0 + ch;
-    const int ntiles = (int)a.nseg;
+    const int nt = (int)a.nseg;
+    const int rounds = 2 * nt - 1;
     const bool has_z = a.z != nullptr;
-    const uint32_t tx_bytes = (uint32_t)((3 + (has_z ? 1 : 0)) * Lay::kX + 2 * Lay::kBC);
+    const uint32_t tx_fwd = (uint32_t)(2 * Lay::kX + Lay::kBC);
+    const uint32_t tx_rev = (uint32_t)((3 + (has_z ? 1 : 0)) * Lay::kX + 2 * Lay::kBC);
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + Lay::kBar;
@@ -772,30 +845,35 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
         fence_mbar_init();
         prefetch_tensormap(&tm_u);
         prefetch_tensormap(&tm_dt);
-        prefetch_tensormap(&tm_g);
         prefetch_tensormap(&tm_B);
-        prefetch_tensormap(&tm_C);
-        if (has_z) prefetch_tensormap(&tm_z);
+        if (rounds > 0) {
+            prefetch_tensormap(&tm_g);
+            prefetch_tensormap(&tm_C);
+            if (has_z) prefetch_tensormap(&tm_z);
+        }
     }
     __syncwarp();
-    // r-th tile in walking order = time tile ntiles-1-r, stage r % S
+    // round r: forward tile r (r < nt-1), else reverse tile 2nt-2-r; stage r % S
     auto issue = [&](int r) {
         const uint32_t st = sbase + (r % S) * Lay::kStage;
         const uint32_t bar = bar0 + 8 * (r % S);
-        const int32_t tt = (int32_t)((int64_t)(ntiles - 1 - r) * TT);
-        mbar_expect_tx(bar, tx_bytes);
+        const bool fwd = r < nt - 1;
+        const int32_t tt = (int32_t)((int64_t)(fwd ? r : 2 * nt - 2 - r) * TT);
+        mbar_expect_tx(bar, fwd ? tx_fwd : tx_rev);
         tma_load_3d(st, &tm_u, bar, d0, tt, b);
         tma_load_3d(st + Lay::kX, &tm_dt, bar, d0, tt, b);
-        if (has_z) tma_load_3d(st + 2 * Lay::kX, &tm_z, bar, d0, tt, b);
-        tma_load_3d(st + 3 * Lay::kX, &tm_g, bar, d0, tt, b);
-        tma_load_3d(st + 4 * Lay::kX, &tm_B, bar, 0, tt, b);
-        tma_load_3d(st + 4 * Lay::kX + Lay::kBC, &tm_C, bar, 0, tt, b);
+        tma_load_3d(st + Lay::kBoff, &tm_B, bar, 0, tt, b);
+        if (!fwd) {
+            if (has_z) tma_load_3d(st + 2 * Lay::kX, &tm_z, bar, d0, tt, b);
+            tma_load_3d(st + 3 * Lay::kX, &tm_g, bar, d0, tt, b);
+            tma_load_3d(st + Lay::kCoff, &tm_C, bar, 0, tt, b);
+        }
     };
-    int issued = min(S, ntiles);
+    int issued = min(S, rounds);
     if (lane == 0)
         for (int r = 0; r < issued; ++r) issue(r);
 
-    u64 A2[NP], An[NP], dh[NP], dAacc[NP];
+    u64 A2[NP], An[NP], h[NP], dh[NP], dAacc[NP];
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
         const float* Ar = a.A + d * N + n0 + 2 * i;
@@ -804,169 +882,196 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
         A2[i] = pk2(a0 * kLog2e, a1 * kLog2e);
         dAacc[i] = pk2(0.0f, 0.0f);
         dh[i] = pk2(0.0f, 0.0f);
-        if (a.dlast) {
-            const float* q = a.dlast + ((int64_t)b * a.d_inner + d) * N + n0 + 2 * i;
-            dh[i] = pk2(q[0], q[1]);
-        }
+        h[i] = pk2(0.0f, 0.0f);
     }
+    if (a.dlast) ld_pairs<NP>(a.dlast + ((int64_t)b * a.d_inner + d) * N + n0, dh);
+    const float* h0row = a.h0 ? a.h0 + ((int64_t)b * a.d_inner + d) * N + n0 : nullptr;
+    if (h0row) ld_pairs<NP>(h0row, h);
     const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
     const float Dd = a.D ? __ldg(a.D + d) : 0.0f;
     float dDacc = 0.0f, dbacc = 0.0f;
+    float4* const tab = reinterpret_cast<float4*>(smem + Lay::kTab);
+    float2* const tab2 = reinterpret_cast<float2*>(smem + Lay::kTab2);
     float* const hb = reinterpret_cast<float*>(smem + Lay::kH);
-    float* const dbc = reinterpret_cast<float*>(smem + Lay::kDBC);
-    const int64_t rowL = (int64_t)b * a.L;  // (b, 0) row of the (batch, L, .) arrays
+    // the CTA's checkpoint rows: entering state of tile k at ck + k * 32*NS
+    float* const ck = a.ckpt + (int64_t)blockIdx.x * nt * (32 * NS) + lane * NS;
+    // per-lane output of the reverse rounds: g = 0 dz, 1 ddt, 2 du, 3 none
+    T* outp = static_cast<T*>(a.du);  // also the (unwritten) address of g = 3
+    bool has_out = g < 3;
+    if (g == 0) {
+        if (a.dz) outp = static_cast<T*>(a.dz);
+        else has_out = false;
+    }
+    if (g == 1) outp = static_cast<T*>(a.ddt);
+    outp += (int64_t)b * a.L * a.d_inner + d;
+    const bool bsel = (ch & 4) != 0;  // dB / dC half of the channel reduction
+    float* const dbc = (bsel ? a.dC : a.dB) + (int64_t)b * a.L * N + n0;
+    const bool gb1 = (g & 2) != 0, gb0 = (g & 1) != 0;
 
     bool ok = true;
     int waited = 0;
-    for (int r = 0; r < ntiles; ++r) {
-        const int it = ntiles - 1 - r;
-        const int64_t t0 = (int64_t)it * TT;
-        const int nst = (int)min((int64_t)TT, a.L - t0);
+    u64 hin[NP];
+    for (int r = 0; r < rounds; ++r) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (r % S), (r / S) & 1, kWaitLimit));
         if (!ok) break;
         waited = r + 1;
         const unsigned char* st = smem + (r % S) * Lay::kStage;
-        const T* su = reinterpret_cast<const T*>(st) + ch;
-        const T* sdt = reinterpret_cast<const T*>(st + Lay::kX) + ch;
-        const T* sz = reinterpret_cast<const T*>(st + 2 * Lay::kX) + ch;
-        const T* sg = reinterpret_cast<const T*>(st + 3 * Lay::kX) + ch;
-        const float* sB = reinterpret_cast<const float*>(st + 4 * Lay::kX) + n0;
-        const float* sC = reinterpret_cast<const float*>(st + 4 * Lay::kX + Lay::kBC) + n0;
-
-        // (1) the tile's entering state
-        u64 hin[NP];
-#pragma unroll
-        for (int i = 0; i < NP; ++i) hin[i] = pk2(0.0f, 0.0f);
-        const float* ck = it > 0
-            ? a.ckpt + (((int64_t)b * (ntiles - 1) + it - 1) * a.d_inner + d) * N + n0
-            : (a.h0 ? a.h0 + ((int64_t)b * a.d_inner + d) * N + n0 : nullptr);
-        if (ck) {
-#pragma unroll
-            for (int i = 0; i < NP; ++i) hin[i] = pk2(ck[2 * i], ck[2 * i + 1]);
-        }
-        // one recurrence step j of the tile on h, stored to buffer row j
-        auto fwd = [&](int j, u64 (&h)[NP]) {
-            const float delta = softplus(lds_elem<T>(sdt + j * CPW) + bias);
-            const float du = delta * lds_elem<T>(su + j * CPW);
-            const u64 dl2 = pk2(delta, delta), du2 = pk2(du, du);
-            u64* hs = reinterpret_cast<u64*>(hb + (j * 32 + lane) * NS);
-#pragma unroll
-            for (int i = 0; i < NP; ++i) {
-                const u64 x2 = mul2(dl2, A2[i]);
-                const u64 dA = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
-                const u64 Bq = *reinterpret_cast<const u64*>(sB + j * N + 2 * i);
-                h[i] = fma2(dA, h[i], mul2(du2, Bq));
-                hs[i] = h[i];
-            }
-        };
-        // (2) the adjoint, last step of the tile first
-        auto adj = [&](int j) {
-            const float x = lds_elem<T>(sdt + j * CPW) + bias;
-            const float delta = softplus(x);
-            const float sx = __fdividef(1.0f, 1.0f + ex2(-x * kLog2e));  // softplus'
-            const float uu = lds_elem<T>(su + j * CPW);
-            const float go = lds_elem<T>(sg + j * CPW);
-            const u64* hs = reinterpret_cast<const u64*>(hb + (j * 32 + lane) * NS);
-            const u64* hq =  // the step before (row 0 reads itself; hin is used then)
-                reinterpret_cast<const u64*>(hb + ((j > 0 ? j - 1 : 0) * 32 + lane) * NS);
-            u64 ht[NP], hp[NP], Bq[NP], Cq[NP];
-            u64 y2 = pk2(0.0f, 0.0f);
-#pragma unroll
-            for (int i = 0; i < NP; ++i) {
-                ht[i] = hs[i];
-                hp[i] = j > 0 ? hq[i] : hin[i];
-                Bq[i] = *reinterpret_cast<const u64*>(sB + j * N + 2 * i);
-                Cq[i] = *reinterpret_cast<const u64*>(sC + j * N + 2 * i);
-                y2 = fma2(Cq[i], ht[i], y2);
-            }
-            float y = lo2(y2) + hi2(y2);
-#pragma unroll
-            for (int o = CPW; o < 32; o <<= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
-            y = fmaf(Dd, uu, y);
-            float dy = go, dz = 0.0f;
-            if (has_z) {
-                const float zz = lds_elem<T>(sz + j * CPW);
-                const float s = __fdividef(1.0f, 1.0f + ex2(-zz * kLog2e));
-                dy = go * zz * s;
-                dz = go * y * s * fmaf(zz, 1.0f - s, 1.0f);
-            }
-            const u64 dy2 = pk2(dy, dy), dl2 = pk2(delta, delta), u2 = pk2(uu, uu);
-            const u64 du2 = pk2(delta * uu, delta * uu);
-            u64 ddp = pk2(0.0f, 0.0f), dsp = pk2(0.0f, 0.0f), dBp[NP], dCp[NP];
+        const T* su = reinterpret_cast<const T*>(st);
+        const T* sdt = reinterpret_cast<const T*>(st + Lay::kX);
+        const T* sz = reinterpret_cast<const T*>(st + 2 * Lay::kX);
+        const T* sg = reinterpret_cast<const T*>(st + 3 * Lay::kX);
+        const float* sB = reinterpret_cast<const float*>(st + Lay::kBoff) + n0;
+        const float* sC = reinterpret_cast<const float*>(st + Lay::kCoff) + n0;
+        // one recurrence step j of the tile on the state x
+        auto step = [&](int j, u64 (&x)[NP]) {
+            const float2 t = *reinterpret_cast<const float2*>(tab + j * CPW + ch);
+            const u64 dl2 = pk2(t.x, t.x), du2 = pk2(t.y, t.y);
+            u64 Bq[NP];
+            ld_pairs<NP>(sB + j * N, Bq);
 #pragma unroll
             for (int i = 0; i < NP; ++i) {
                 const u64 x2 = mul2(dl2, A2[i]);
                 const u64 ea = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
-                dh[i] = fma2(Cq[i], dy2, dh[i]);
-                dCp[i] = mul2(dy2, ht[i]);
-                const u64 dae = mul2(mul2(dh[i], hp[i]), ea);
-                dAacc[i] = fma2(dae, dl2, dAacc[i]);
-                ddp = fma2(dae, An[i], ddp);
-                const u64 dhB = mul2(dh[i], Bq[i]);
-                ddp = fma2(dhB, u2, ddp);
-                dsp = fma2(dhB, dl2, dsp);
-                dBp[i] = mul2(dh[i], du2);
-                dh[i] = mul2(dh[i], ea);
-            }
-            float ddel = lo2(ddp) + hi2(ddp), dus = lo2(dsp) + hi2(dsp);
-#pragma unroll
-            for (int o = CPW; o < 32; o <<= 1) {
-                ddel += __shfl_xor_sync(0xffffffffu, ddel, o);
-                dus += __shfl_xor_sync(0xffffffffu, dus, o);
-            }
-            const float ddt = ddel * sx;
-            if (g == 0) {
-                const int64_t o = (rowL + t0 + j) * a.d_inner + d;
-                Elem<T>::store(static_cast<T*>(a.du) + o, fmaf(dy, Dd, dus));
-                Elem<T>::store(static_cast<T*>(a.ddt) + o, ddt);
-                if (a.dz) Elem<T>::store(static_cast<T*>(a.dz) + o, dz);
-                dDacc = fmaf(dy, uu, dDacc);
-                dbacc += ddt;
-            }
-            // dB, dC of this step: sum over the warp's channels (lanes 1 .. CPW-1 apart)
-#pragma unroll
-            for (int o = 1; o < CPW; o <<= 1) {
-#pragma unroll
-                for (int i = 0; i < NP; ++i) {
-                    dBp[i] = add2(dBp[i], __shfl_xor_sync(0xffffffffu, dBp[i], o));
-                    dCp[i] = add2(dCp[i], __shfl_xor_sync(0xffffffffu, dCp[i], o));
-                }
-            }
-            if (ch == 0) {
-                u64* wb = reinterpret_cast<u64*>(dbc + j * 2 * N + n0);
-                u64* wc = reinterpret_cast<u64*>(dbc + j * 2 * N + N + n0);
-#pragma unroll
-                for (int i = 0; i < NP; ++i) {
-                    wb[i] = dBp[i];
-                    wc[i] = dCp[i];
-                }
+                x[i] = fma2(ea, x[i], mul2(du2, Bq[i]));
             }
         };
-        // (2) recompute the tile's states, then walk the adjoint back
-        {
-            u64 h[NP];
+        if (r < nt - 1) {
+            // ---- forward round: tile r is whole (only the last tile can be short)
 #pragma unroll
-            for (int i = 0; i < NP; ++i) h[i] = hin[i];
-            if (nst == TT) {  // full tile: unrolled, constant shared-memory offsets
-#pragma unroll 8
-                for (int j = 0; j < TT; ++j) fwd(j, h);
-#pragma unroll 8
-                for (int j = TT - 1; j >= 0; --j) adj(j);
-            } else {
-                for (int j = 0; j < nst; ++j) fwd(j, h);
-                for (int j = nst - 1; j >= 0; --j) adj(j);
+            for (int q = 0; q < PQ; ++q) {
+                const int e = lane + 32 * q;  // step g + 4q of channel ch
+                const float dl = softplus(lds_elem<T>(sdt + e) + bias);
+                *reinterpret_cast<float2*>(tab + e) = make_float2(dl, dl * lds_elem<T>(su + e));
             }
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < TT; ++j) step(j, h);
+            st_pairs<NP>(ck + (int64_t)(r + 1) * (32 * NS), h);
+        } else {
+            // ---- reverse round
+            const int it = 2 * nt - 2 - r;
+            const int64_t t0 = (int64_t)it * TT;
+            const int nst = (int)min((int64_t)TT, a.L - t0);
+            if (r == nt - 1) {
+#pragma unroll
+                for (int i = 0; i < NP; ++i) hin[i] = h[i];  // the forward's last state
+            }
+            // the entering state of the next (earlier) tile, loaded ahead
+            u64 hnext[NP];
+#pragma unroll
+            for (int i = 0; i < NP; ++i) hnext[i] = pk2(0.0f, 0.0f);
+            if (it >= 2) ld_pairs<NP>(ck + (int64_t)(it - 1) * (32 * NS), hnext);
+            else if (it == 1 && h0row) ld_pairs<NP>(h0row, hnext);
+            // (1) per-(step, channel) scalars of the tile
+#pragma unroll
+            for (int q = 0; q < PQ; ++q) {
+                const int e = lane + 32 * q;
+                const int j = g + G * q;
+                const float x = lds_elem<T>(sdt + e) + bias;
+                const float uu = lds_elem<T>(su + e);
+                const float go = lds_elem<T>(sg + e);
+                const bool in = j < nst;  // past L: zero-filled inputs; pass through
+                const float dl = in ? softplus(x) : 0.0f;
+                const float sx = in ? rcp_approx(1.0f + ex2(-x * kLog2e)) : 0.0f;
+                // without z the tile holds stale data: read, then not used
+                const float zz = lds_elem<T>(sz + e);
+                const float s = rcp_approx(1.0f + ex2(-zz * kLog2e));
+                const float dy = has_z ? go * zz * s : go;
+                const float dzc = has_z ? go * s * fmaf(zz, 1.0f - s, 1.0f) : 0.0f;
+                tab[e] = make_float4(dl, dl * uu, dy, uu);
+                tab2[e] = make_float2(sx, dzc);
+                dDacc = fmaf(dy, uu, dDacc);
+            }
+            __syncwarp();
+            // (2) the tile's states
+            {
+                u64 x[NP];
+#pragma unroll
+                for (int i = 0; i < NP; ++i) x[i] = hin[i];
+#pragma unroll
+                for (int j = 0; j < TT; ++j) {
+                    step(j, x);
+                    hbuf_st<NS, HV>(hb, j, lane, x);
+                }
+            }
+            // (3) the adjoint, last step first
+            T* const orow = outp + t0 * a.d_inner;
+            float* const brow = dbc + t0 * N;
+#pragma unroll
+            for (int j = TT - 1; j >= 0; --j) {
+                const float4 ta = tab[j * CPW + ch];
+                const float2 tb = tab2[j * CPW + ch];
+                u64 ht[NP], hp[NP], Bq[NP], Cq[NP];
+                hbuf_ld<NS, HV>(hb, j, lane, ht);
+                if (j > 0) {
+                    hbuf_ld<NS, HV>(hb, j - 1, lane, hp);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) hp[i] = hin[i];
+                }
+                ld_pairs<NP>(sB + j * N, Bq);
+                ld_pairs<NP>(sC + j * N, Cq);
+                const u64 dl2 = pk2(ta.x, ta.x), du2 = pk2(ta.y, ta.y), dy2 = pk2(ta.z, ta.z);
+                u64 y2 = pk2(0.0f, 0.0f), ddp = pk2(0.0f, 0.0f), sp = pk2(0.0f, 0.0f);
+                u64 dB[NP], dC[NP];
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    y2 = fma2(Cq[i], ht[i], y2);
+                    const u64 x2 = mul2(dl2, A2[i]);
+                    const u64 ea = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
+                    dh[i] = fma2(Cq[i], dy2, dh[i]);
+                    dC[i] = mul2(dy2, ht[i]);
+                    const u64 dae = mul2(mul2(dh[i], hp[i]), ea);
+                    dAacc[i] = fma2(dae, dl2, dAacc[i]);
+                    ddp = fma2(dae, An[i], ddp);
+                    const u64 dhB = mul2(dh[i], Bq[i]);
+                    sp = add2(sp, dhB);
+                    dB[i] = mul2(dh[i], du2);
+                    dh[i] = mul2(dh[i], ea);
+                }
+                const float ssum = lo2(sp) + hi2(sp);
+                const float yp = lo2(y2) + hi2(y2);
+                const float dd = fmaf(ta.w, ssum, lo2(ddp) + hi2(ddp));
+                // (y, ddelta, S) over the channel's 4 lanes: g keeps one of them
+                float k0 = gb1 ? ssum : yp, k1 = gb1 ? 0.0f : dd;
+                const float s0 = gb1 ? yp : ssum, s1 = gb1 ? dd : 0.0f;
+                k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+                k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+                float v = gb0 ? k1 : k0;
+                v += __shfl_xor_sync(0xffffffffu, gb0 ? k0 : k1, 8);
+                const float o = g == 0 ? (v + Dd * ta.w) * tb.y
+                                       : (g == 1 ? v * tb.x : fmaf(ta.x, v, ta.z * Dd));
+                dbacc += g == 1 ? o : 0.0f;
+                Elem<T>::store_if(has_out && j < nst, orow + j * a.d_inner, o);
+                // dB (ch bit 2 clear) or dC (set) over the warp's 8 channels
+                u64 kq[NP];
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    kq[i] = bsel ? dC[i] : dB[i];
+                    kq[i] = add2(kq[i], __shfl_xor_sync(0xffffffffu, bsel ? dB[i] : dC[i], 4));
+                }
+#pragma unroll
+                for (int o2 = 2; o2 >= 1; o2 >>= 1)
+#pragma unroll
+                    for (int i = 0; i < NP; ++i)
+                        kq[i] = add2(kq[i], __shfl_xor_sync(0xffffffffu, kq[i], o2));
+                const bool lead = (ch & 3) == 0 && j < nst;
+                float* p = brow + j * N;
+                if constexpr (NP == 1) {
+                    red_add_v2_if(lead, p, make_float2(lo2(kq[0]), hi2(kq[0])));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < NP / 2; ++c)
+                        red_add_v4_if(lead, p + 4 * c,
+                                      make_float4(lo2(kq[2 * c]), hi2(kq[2 * c]),
+                                                  lo2(kq[2 * c + 1]), hi2(kq[2 * c + 1])));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < NP; ++i) hin[i] = hnext[i];
         }
         __syncwarp();
-        // (3) the tile's dB, dC into global memory, then refill its stage
-        for (int q = lane; q < nst * 2 * N / 4; q += 32) {  // 4 states per vector add
-            const int e = q * 4;
-            const int j = e / (2 * N), rem = e % (2 * N);
-            float* dst = (rem < N ? a.dB : a.dC) + (rowL + t0 + j) * N + (rem % N);
-            red_add_v4(dst, *reinterpret_cast<const float4*>(dbc + e));
-        }
-        __syncwarp();
-        if (r + S < ntiles) {
+        if (r + S < rounds) {
             if (lane == 0) {
                 fence_proxy_async_smem();
                 issue(r + S);
@@ -980,21 +1085,16 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
         if (lane == 0) atomicOr(&g_scan_error, 1u);
         return;
     }
-    if (a.dh0) {
-        float* q = a.dh0 + ((int64_t)b * a.d_inner + d) * N + n0;
-#pragma unroll
-        for (int i = 0; i < NP; ++i)
-            *reinterpret_cast<float2*>(q + 2 * i) = make_float2(lo2(dh[i]), hi2(dh[i]));
-    }
+    if (a.dh0) st_pairs<NP>(a.dh0 + ((int64_t)b * a.d_inner + d) * N + n0, dh);
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
         atomicAdd(a.dA + d * N + n0 + 2 * i, lo2(dAacc[i]));
         atomicAdd(a.dA + d * N + n0 + 2 * i + 1, hi2(dAacc[i]));
     }
-    if (g == 0) {
-        if (a.dD) atomicAdd(a.dD + d, dDacc);
-        if (a.ddt_bias) atomicAdd(a.ddt_bias + d, dbacc);
-    }
+    dDacc += __shfl_xor_sync(0xffffffffu, dDacc, 8);
+    dDacc += __shfl_xor_sync(0xffffffffu, dDacc, 16);
+    if (g == 0 && a.dD) atomicAdd(a.dD + d, dDacc);
+    if (g == 1 && a.ddt_bias) atomicAdd(a.ddt_bias + d, dbacc);
 }
 
 // B and C as fp32 rows for the [TT x N] fp32 TMA boxes; 8 elements per
@@ -1139,27 +1239,35 @@ static cudaError_t launch_tma_t(const ScanArgs& a, const ScanPlan& p, const floa
     }
 }
 
+// B and C rows as fp32 (converted, or realigned copies) for the TMA boxes.
+static void convert_bc(const void* B, const void* C, msc_dtype dtype, float* Bf, float* Cf,
+                       int64_t n, cudaStream_t s) {
+    if (n <= 0) return;
+    const int vec8 = dtype == MSC_BF16 && (n % 8 == 0) &&
+                     (reinterpret_cast<uintptr_t>(B) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(C) % 16 == 0);
+    const int64_t work = vec8 ? n / 8 : n;
+    const int64_t nb = (work + 255) / 256;
+    const int blocks = (int)(nb < 4096 ? nb : 4096);
+    if (dtype == MSC_BF16)
+        bc_to_f32_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), Bf, Cf,
+            n, vec8);
+    else
+        bc_to_f32_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(B),
+                                                       static_cast<const float*>(C), Bf, Cf, n,
+                                                       0);
+    profile_count(1);
+}
+
 cudaError_t launch_scan_tma(const ScanArgs& a, const ScanPlan& p, msc_dtype dtype, float* Bf,
                             float* Cf, cudaStream_t s) {
     const float* Bsrc = static_cast<const float*>(a.B);
     const float* Csrc = static_cast<const float*>(a.C);
-    const int64_t n = a.batch * a.L * a.N;
-    if (Bf && n > 0) {  // rows converted (or realigned) to fp32 for the TMA boxes
-        const int vec8 = dtype == MSC_BF16 && (n % 8 == 0) &&
-                         (reinterpret_cast<uintptr_t>(a.B) % 16 == 0) &&
-                         (reinterpret_cast<uintptr_t>(a.C) % 16 == 0);
-        const int64_t work = vec8 ? n / 8 : n;
-        const int64_t nb = (work + 255) / 256;
-        const int blocks = (int)(nb < 4096 ? nb : 4096);
-        if (dtype == MSC_BF16)
-            bc_to_f32_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
-                static_cast<const __nv_bfloat16*>(a.B), static_cast<const __nv_bfloat16*>(a.C),
-                Bf, Cf, n, vec8);
-        else
-            bc_to_f32_kernel<float><<<blocks, 256, 0, s>>>(Bsrc, Csrc, Bf, Cf, n, 0);
+    if (Bf && a.batch * a.L * a.N > 0) {
+        convert_bc(a.B, a.C, dtype, Bf, Cf, a.batch * a.L * a.N, s);
         Bsrc = Bf;
         Csrc = Cf;
-        profile_count(1);
     }
     if (dtype == MSC_BF16) return launch_tma_t<__nv_bfloat16>(a, p, Bsrc, Csrc, s);
     return launch_tma_t<float>(a, p, Bsrc, Csrc, s);
@@ -1177,8 +1285,8 @@ cudaError_t scan_error_word(unsigned int* value, bool clear) {
 template <typename T, int NS, int TT>
 static cudaError_t launch_bwd_tma_n(const BwdArgs& a, const float* Bf, const float* Cf,
                                     cudaStream_t s) {
-    constexpr int G = 4, S = 2;
-    using Lay = BwdLayout<T, G, NS, TT, S>;
+    constexpr int S = 2;
+    using Lay = BwdLayout<T, NS, TT, S>;
     const CUtensorMapDataType tt =
         sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const int es = (int)sizeof(T);
@@ -1190,7 +1298,7 @@ static cudaError_t launch_bwd_tma_n(const BwdArgs& a, const float* Bf, const flo
         !make_map(&mB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Bf, a.N, a.L, a.batch, (int)a.N, TT) ||
         !make_map(&mC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Cf, a.N, a.L, a.batch, (int)a.N, TT))
         return cudaErrorInvalidValue;
-    auto kern = scan_bwd_tma_kernel<T, G, NS, TT, S>;
+    auto kern = scan_bwd_tma_kernel<T, NS, TT, S>;
     const size_t smem = Lay::kTotal;
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1202,27 +1310,56 @@ static cudaError_t launch_bwd_tma_n(const BwdArgs& a, const float* Bf, const flo
     return cudaGetLastError();
 }
 
-bool bwd_tma_supported(int64_t N, int64_t d_inner, const void* dout) {
-    return (N == 8 || N == 16 || N == 32 || N == 64) && d_inner % 8 == 0 &&
-           (reinterpret_cast<uintptr_t>(dout) & 15) == 0 && encode_fn() != nullptr;
+int bwd_tma_tile(int64_t N) { return N <= 16 ? 16 : 8; }
+
+bool bwd_tma_supported(int64_t N, int64_t d_inner, const void* u, const void* dt, const void* z,
+                       const void* dout, const void* dB, const void* dC) {
+    auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    return (N == 8 || N == 16 || N == 32 || N == 64) && d_inner % 8 == 0 && al(u) && al(dt) &&
+           (!z || al(z)) && al(dout) && al(dB) && al(dC) && encode_fn() != nullptr;
 }
 
-cudaError_t launch_scan_bwd_tma(const BwdArgs& a, msc_dtype dtype, const float* Bf,
-                                const float* Cf, cudaStream_t s) {
+static bool bwd_needs_bc(const BwdArgs& a, msc_dtype dtype) {
+    auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    return dtype == MSC_BF16 || !al(a.B) || !al(a.C);
+}
+
+size_t scan_bwd_tma_scratch(const BwdArgs& a, msc_dtype dtype) {
+    const int64_t TT = bwd_tma_tile(a.N);
+    const int64_t nt = (a.L + TT - 1) / TT;
+    const size_t ck = ((size_t)(a.batch * a.d_inner * a.N * nt) * 4 + 255) / 256 * 256;
+    const size_t bc = bwd_needs_bc(a, dtype) ? 2 * (size_t)(a.batch * a.L * a.N) * 4 : 0;
+    return ck + bc;
+}
+
+cudaError_t launch_scan_bwd_tma(BwdArgs a, msc_dtype dtype, void* scratch, cudaStream_t s) {
+    const int64_t TT = bwd_tma_tile(a.N);
+    a.nseg = (a.L + TT - 1) / TT;
+    a.ckpt = static_cast<float*>(scratch);
+    const size_t ck = ((size_t)(a.batch * a.d_inner * a.N * a.nseg) * 4 + 255) / 256 * 256;
+    const float* Bf = static_cast<const float*>(a.B);
+    const float* Cf = static_cast<const float*>(a.C);
+    if (bwd_needs_bc(a, dtype)) {
+        float* Bc = reinterpret_cast<float*>(static_cast<char*>(scratch) + ck);
+        float* Cc = Bc + a.batch * a.L * a.N;
+        convert_bc(a.B, a.C, dtype, Bc, Cc, a.batch * a.L * a.N, s);
+        Bf = Bc;
+        Cf = Cc;
+    }
     const bool bf = dtype == MSC_BF16;
     switch (a.N) {
         case 8:
-            return bf ? launch_bwd_tma_n<__nv_bfloat16, 2, 32>(a, Bf, Cf, s)
-                      : launch_bwd_tma_n<float, 2, 32>(a, Bf, Cf, s);
+            return bf ? launch_bwd_tma_n<__nv_bfloat16, 2, 16>(a, Bf, Cf, s)
+                      : launch_bwd_tma_n<float, 2, 16>(a, Bf, Cf, s);
         case 16:
-            return bf ? launch_bwd_tma_n<__nv_bfloat16, 4, 32>(a, Bf, Cf, s)
-                      : launch_bwd_tma_n<float, 4, 32>(a, Bf, Cf, s);
+            return bf ? launch_bwd_tma_n<__nv_bfloat16, 4, 16>(a, Bf, Cf, s)
+                      : launch_bwd_tma_n<float, 4, 16>(a, Bf, Cf, s);
         case 32:
-            return bf ? launch_bwd_tma_n<__nv_bfloat16, 8, 16>(a, Bf, Cf, s)
-                      : launch_bwd_tma_n<float, 8, 16>(a, Bf, Cf, s);
+            return bf ? launch_bwd_tma_n<__nv_bfloat16, 8, 8>(a, Bf, Cf, s)
+                      : launch_bwd_tma_n<float, 8, 8>(a, Bf, Cf, s);
         default:
-            return bf ? launch_bwd_tma_n<__nv_bfloat16, 16, 16>(a, Bf, Cf, s)
-                      : launch_bwd_tma_n<float, 16, 16>(a, Bf, Cf, s);
+            return bf ? launch_bwd_tma_n<__nv_bfloat16, 16, 8>(a, Bf, Cf, s)
+                      : launch_bwd_tma_n<float, 16, 8>(a, Bf, Cf, s);
     }
 }
 

@@ -102,3 +102,24 @@ def test_bwd_mid_size():
     """Many channel tiles and segments: 2 x 512 x 512 x 16, bf16."""
     x = synth.scan_inputs(2, 512, 512, 16, dtype="bf16", seed=870, D="normal")
     check(x, seed=9, want_dh0=False)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d_state", [8, 16, 32, 64])
+@pytest.mark.parametrize("L", [1, 8, 16, 17, 40])
+def test_bwd_tma_tiles(dtype, d_state, L):
+    """Shapes the TMA backward takes (d_inner % 8 == 0, N in {8, 16, 32, 64}):
+    tiles of 16 steps (N <= 16) or 8 steps (N > 16), one tile or several,
+    whole or ragged, with h0 so that the first tile's entering state is used."""
+    x = synth.scan_inputs(2, L, 48, d_state, dtype=dtype, seed=900 + d_state + L,
+                          D="normal", A_kind="random")
+    h0 = np.random.default_rng(L).standard_normal((2, 48, d_state)).astype(np.float32)
+    check(x, h0=h0, seed=11)
+
+
+def test_bwd_after_scratch_release():
+    """The scratch pool gives its memory back and the next call takes it again."""
+    x = synth.scan_inputs(2, 40, 64, 16, dtype="bf16", seed=960, D="normal")
+    check(x, seed=12)
+    msc.scratch_release()
+    check(x, seed=12)
