@@ -192,9 +192,11 @@ static cudaError_t launch_conv_v(const ConvArgs& a, cudaStream_t s) {
     const int64_t groups = (a.d_inner + (int64_t)kConvThreads * V - 1) / ((int64_t)kConvThreads * V);
     const int64_t tiles = a.L > 0 ? (a.L + kTileT - 1) / kTileT : 1;
     const dim3 grid((unsigned)groups, (unsigned)tiles, (unsigned)a.batch);
+    const ProfileMark m = profile_begin(s, MSC_PROF_CONV);
     causal_conv1d_kernel<T, V, KC><<<grid, kConvThreads, 0, s>>>(
         static_cast<const T*>(a.x), a.w, a.bias, static_cast<const T*>(a.state_in),
         static_cast<T*>(a.out), static_cast<T*>(a.state_out), a.L, a.d_inner, a.silu);
+    profile_end(m, s);
     return cudaGetLastError();
 }
 
@@ -208,9 +210,11 @@ static cudaError_t launch_conv_k(const ConvArgs& a, cudaStream_t s) {
 template <typename T, int KC>
 static cudaError_t launch_update_k(const ConvArgs& a, cudaStream_t s) {
     const int64_t n = a.batch * a.d_inner;
+    const ProfileMark m = profile_begin(s, MSC_PROF_CONV_UPDATE);
     conv1d_update_kernel<T, KC><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
         static_cast<T*>(a.state_out), static_cast<const T*>(a.x), a.w, a.bias,
         static_cast<T*>(a.out), n, a.d_inner, a.silu);
+    profile_end(m, s);
     return cudaGetLastError();
 }
 

@@ -32,13 +32,17 @@ bool mul_ok(int64_t a, int64_t b, int64_t* r) {
     return true;
 }
 
+// Multiprocessor count of the current device, queried once per device.
 int sm_count() {
+    static int counts[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < 64 && counts[dev] > 0) return counts[dev];
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         n <= 0)
         return 148;
+    if (dev >= 0 && dev < 64) counts[dev] = n;
     return n;
 }
 
@@ -530,10 +534,8 @@ static msc_status run_conv(const void* x, const float* w, const float* bias,
     a.vec = !update && (d_inner % (int64_t)(8 / es) == 0) && (!x || aligned(x, 8)) &&
             (!out || aligned(out, 8));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    msc::ProfileMark m = msc::profile_begin(s, update ? MSC_PROF_CONV_UPDATE : MSC_PROF_CONV);
     cudaError_t e = update ? msc::launch_conv1d_update(a, dtype, s)
                            : msc::launch_causal_conv1d(a, dtype, s);
-    msc::profile_end(m, s);
     msc::profile_count(1);
     return e == cudaSuccess ? MSC_OK : MSC_ERR_CUDA;
 }

@@ -110,10 +110,10 @@ template <> struct Elem<float> {
     static __device__ __forceinline__ float load(const float* p) { return __ldg(p); }
     static __device__ __forceinline__ void store(float* p, float v) { *p = v; }
     // store under a predicate, without a branch
+    // (no memory clobber: for outputs the storing kernel does not read back)
     static __device__ __forceinline__ void store_if(bool pred, float* p, float v) {
         asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
-                     "@q st.global.f32 [%0], %1;\n\t}" ::"l"(p), "f"(v), "r"((int)pred)
-                     : "memory");
+                     "@q st.global.f32 [%0], %1;\n\t}" ::"l"(p), "f"(v), "r"((int)pred));
     }
     // 4 consecutive elements, p 16-byte aligned
     static __device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
@@ -136,8 +136,7 @@ template <> struct Elem<__nv_bfloat16> {
     static __device__ __forceinline__ void store_if(bool pred, __nv_bfloat16* p, float v) {
         const unsigned short b = __bfloat16_as_ushort(__float2bfloat16_rn(v));
         asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
-                     "@q st.global.b16 [%0], %1;\n\t}" ::"l"(p), "h"(b), "r"((int)pred)
-                     : "memory");
+                     "@q st.global.b16 [%0], %1;\n\t}" ::"l"(p), "h"(b), "r"((int)pred));
     }
     // 4 consecutive elements, p 8-byte aligned
     static __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {

@@ -73,21 +73,26 @@ __device__ __forceinline__ void red_add_v2(float* p, float2 v) {
                  : "memory");
 }
 
-// The two atomic adds above under a predicate instead of a branch, so that
-// a loop that issues them stays one basic block.
+// Atomic adds (1, 2, 4 floats) under a predicate instead of a branch, so
+// that a loop that issues them stays one basic block.  No memory clobber: for
+// results the issuing kernel never reads back, so that the compiler may keep
+// shared-memory values in registers across them.
+__device__ __forceinline__ void red_add_if(bool pred, float* p, float v) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+        "@q red.global.add.f32 [%0], %1;\n\t}" ::"l"(p), "f"(v), "r"((int)pred));
+}
 __device__ __forceinline__ void red_add_v4_if(bool pred, float* p, float4 v) {
     asm volatile(
         "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
         "@q red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n\t}" ::"l"(p),
-        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"((int)pred)
-        : "memory");
+        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"((int)pred));
 }
 __device__ __forceinline__ void red_add_v2_if(bool pred, float* p, float2 v) {
     asm volatile(
         "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %3, 0;\n\t"
         "@q red.global.add.v2.f32 [%0], {%1, %2};\n\t}" ::"l"(p),
-        "f"(v.x), "f"(v.y), "r"((int)pred)
-        : "memory");
+        "f"(v.x), "f"(v.y), "r"((int)pred));
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {

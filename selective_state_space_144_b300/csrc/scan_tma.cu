@@ -730,10 +730,10 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
 //          then ddelta += u S and du = dy D + delta S over the channel's
 //          states: (y, ddelta, S) are reduce-scattered over the 4 lanes of
 //          the channel, so that lane g = 0, 1, 2 ends with one of them and
-//          writes dz, ddt or du -- one store per lane and step; dB and dC
-//          are reduce-scattered over the 8 channels (lane bit 2 picks dB or
-//          dC) and added to global memory with one vector atomic add per
-//          lane with ch % 4 == 0.
+//          writes dz, ddt or du -- one store per lane and step; the lane's
+//          2*NS values [dB | dC] are reduce-scattered over the 8 channels, and
+//          each lane adds its slice of the sums to global memory with one
+//          (vector) atomic add.
 // dA, dD, ddt_bias accumulate in registers and are added once at the end;
 // dh after tile 0 is dh0.  Steps past L in the last tile get delta = 0,
 // dy = 0 (the state and the adjoint pass through) and store nothing.
@@ -805,6 +805,39 @@ __device__ __forceinline__ void hbuf_ld(const float* hb, int j, int lane, u64 (&
 #pragma unroll
         for (int k = 0; k < PV; ++k) h[c * PV + k] = v[k];
     }
+}
+
+// Sum of v over the 8 lanes (xor 4, 2, 1) that share lane / 8, scattered:
+// at each of the three levels the lane keeps the half of its values that
+// the lane bit selects and adds its partner's copy of that half, so that
+// it ends with max(F/8, 1) consecutive sums in v[0..], the first of them
+// sum number rs8_first<F>(ch) (F < 8: lanes that differ only in the low
+// bits end with the same sums).
+template <int F>
+__device__ __forceinline__ void reduce_scatter8(float (&v)[F], int ch) {
+#pragma unroll
+    for (int lv = 0; lv < 3; ++lv) {
+        const int o = 4 >> lv;
+        const int m = F >> lv;  // values still held
+        const bool bit = (ch & o) != 0;
+        if (m >= 2) {
+#pragma unroll
+            for (int e = 0; e < m / 2; ++e) {
+                const float keep = bit ? v[e + m / 2] : v[e];
+                const float send = bit ? v[e] : v[e + m / 2];
+                v[e] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        }
+    }
+}
+template <int F>
+__host__ __device__ constexpr int rs8_first(int ch) {
+    int e0 = 0;
+    for (int lv = 0; lv < 3; ++lv)
+        if ((F >> lv) >= 2 && (ch & (4 >> lv))) e0 += (F >> lv) / 2;
+    return e0;
 }
 
 template <typename T, int NS, int TT, int S>
@@ -904,8 +937,11 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
     }
     if (g == 1) outp = static_cast<T*>(a.ddt);
     outp += (int64_t)b * a.L * a.d_inner + d;
-    const bool bsel = (ch & 4) != 0;  // dB / dC half of the channel reduction
-    float* const dbc = (bsel ? a.dC : a.dB) + (int64_t)b * a.L * N + n0;
+    // the dB / dC sums this lane adds: [dB | dC] values rs8_first .. of its states
+    constexpr int MF = 2 * NS >= 8 ? 2 * NS / 8 : 1;
+    const int e0 = rs8_first<2 * NS>(ch);
+    float* const dbc = (e0 < NS ? a.dB + e0 : a.dC + (e0 - NS)) + (int64_t)b * a.L * N + n0;
+    const bool bc_lead = 2 * NS >= 8 || (ch & 1) == 0;
     const bool gb1 = (g & 2) != 0, gb0 = (g & 1) != 0;
 
     bool ok = true;
@@ -997,12 +1033,13 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
             // (3) the adjoint, last step first
             T* const orow = outp + t0 * a.d_inner;
             float* const brow = dbc + t0 * N;
+            u64 ht[NP];  // h of step j; h of step j-1 is loaded once and carried
+            hbuf_ld<NS, HV>(hb, TT - 1, lane, ht);
 #pragma unroll
             for (int j = TT - 1; j >= 0; --j) {
                 const float4 ta = tab[j * CPW + ch];
                 const float2 tb = tab2[j * CPW + ch];
-                u64 ht[NP], hp[NP], Bq[NP], Cq[NP];
-                hbuf_ld<NS, HV>(hb, j, lane, ht);
+                u64 hp[NP], Bq[NP], Cq[NP];
                 if (j > 0) {
                     hbuf_ld<NS, HV>(hb, j - 1, lane, hp);
                 } else {
@@ -1043,29 +1080,25 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
                                        : (g == 1 ? v * tb.x : fmaf(ta.x, v, ta.z * Dd));
                 dbacc += g == 1 ? o : 0.0f;
                 Elem<T>::store_if(has_out && j < nst, orow + j * a.d_inner, o);
-                // dB (ch bit 2 clear) or dC (set) over the warp's 8 channels
-                u64 kq[NP];
+                // dB and dC over the warp's 8 channels: reduce-scatter of the
+                // lane's 2*NS values [dB | dC], lane ch keeping a slice
+                float bc[2 * NS];
 #pragma unroll
                 for (int i = 0; i < NP; ++i) {
-                    kq[i] = bsel ? dC[i] : dB[i];
-                    kq[i] = add2(kq[i], __shfl_xor_sync(0xffffffffu, bsel ? dB[i] : dC[i], 4));
+                    bc[2 * i] = lo2(dB[i]);
+                    bc[2 * i + 1] = hi2(dB[i]);
+                    bc[NS + 2 * i] = lo2(dC[i]);
+                    bc[NS + 2 * i + 1] = hi2(dC[i]);
                 }
+                reduce_scatter8<2 * NS>(bc, ch);
+                float* const p = brow + j * N;
+                const bool lead = bc_lead && j < nst;
+                if constexpr (MF == 1) red_add_if(lead, p, bc[0]);
+                if constexpr (MF == 2) red_add_v2_if(lead, p, make_float2(bc[0], bc[1]));
+                if constexpr (MF == 4)
+                    red_add_v4_if(lead, p, make_float4(bc[0], bc[1], bc[2], bc[3]));
 #pragma unroll
-                for (int o2 = 2; o2 >= 1; o2 >>= 1)
-#pragma unroll
-                    for (int i = 0; i < NP; ++i)
-                        kq[i] = add2(kq[i], __shfl_xor_sync(0xffffffffu, kq[i], o2));
-                const bool lead = (ch & 3) == 0 && j < nst;
-                float* p = brow + j * N;
-                if constexpr (NP == 1) {
-                    red_add_v2_if(lead, p, make_float2(lo2(kq[0]), hi2(kq[0])));
-                } else {
-#pragma unroll
-                    for (int c = 0; c < NP / 2; ++c)
-                        red_add_v4_if(lead, p + 4 * c,
-                                      make_float4(lo2(kq[2 * c]), hi2(kq[2 * c]),
-                                                  lo2(kq[2 * c + 1]), hi2(kq[2 * c + 1])));
-                }
+                for (int i = 0; i < NP; ++i) ht[i] = hp[i];
             }
 #pragma unroll
             for (int i = 0; i < NP; ++i) hin[i] = hnext[i];
