@@ -728,9 +728,11 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
 //            dA += dae delta;  ddelta += dae A;  S += dh B;  dB = dh delta u;
 //            dh *= a
 //          then ddelta += u S and du = dy D + delta S over the channel's
-//          states: (y, ddelta, S) are reduce-scattered over the 4 lanes of
-//          the channel, so that lane g = 0, 1, 2 ends with one of them and
-//          writes dz, ddt or du -- one store per lane and step; the lane's
+//          states: the lane writes its partial (y, ddelta, S) over row j of
+//          the state buffer (consumed by then), and after the tile every lane
+//          sums the 4 partials of TT/4 (step, channel) pairs and stores dz,
+//          ddt, du for them (with 2 states per lane, N = 8, the partials are
+//          reduce-scattered over the channel's lanes every step instead); the lane's
 //          2*NS values [dB | dC] are reduce-scattered over the 8 channels, and
 //          each lane adds its slice of the sums to global memory with one
 //          (vector) atomic add.
@@ -1031,14 +1033,13 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
                 }
             }
             // (3) the adjoint, last step first
-            T* const orow = outp + t0 * a.d_inner;
+            [[maybe_unused]] T* const orow = outp + t0 * a.d_inner;
             float* const brow = dbc + t0 * N;
             u64 ht[NP];  // h of step j; h of step j-1 is loaded once and carried
             hbuf_ld<NS, HV>(hb, TT - 1, lane, ht);
 #pragma unroll
             for (int j = TT - 1; j >= 0; --j) {
                 const float4 ta = tab[j * CPW + ch];
-                const float2 tb = tab2[j * CPW + ch];
                 u64 hp[NP], Bq[NP], Cq[NP];
                 if (j > 0) {
                     hbuf_ld<NS, HV>(hb, j - 1, lane, hp);
@@ -1069,17 +1070,26 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
                 const float ssum = lo2(sp) + hi2(sp);
                 const float yp = lo2(y2) + hi2(y2);
                 const float dd = fmaf(ta.w, ssum, lo2(ddp) + hi2(ddp));
-                // (y, ddelta, S) over the channel's 4 lanes: g keeps one of them
-                float k0 = gb1 ? ssum : yp, k1 = gb1 ? 0.0f : dd;
-                const float s0 = gb1 ? yp : ssum, s1 = gb1 ? dd : 0.0f;
-                k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
-                k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
-                float v = gb0 ? k1 : k0;
-                v += __shfl_xor_sync(0xffffffffu, gb0 ? k0 : k1, 8);
-                const float o = g == 0 ? (v + Dd * ta.w) * tb.y
-                                       : (g == 1 ? v * tb.x : fmaf(ta.x, v, ta.z * Dd));
-                dbacc += g == 1 ? o : 0.0f;
-                Elem<T>::store_if(has_out && j < nst, orow + j * a.d_inner, o);
+                if constexpr (HV == 4) {
+                    // the lane's partial (y, ddelta, S) into its row j of the state
+                    // buffer, whose states were consumed above; summed per
+                    // (step, channel) after the tile
+                    *reinterpret_cast<float4*>(hb + (j * (NS / HV) * 32 + lane) * HV) =
+                        make_float4(yp, dd, ssum, 0.0f);
+                } else {
+                    const float2 tb = tab2[j * CPW + ch];
+                    // (y, ddelta, S) over the channel's 4 lanes: g keeps one of them
+                    float k0 = gb1 ? ssum : yp, k1 = gb1 ? 0.0f : dd;
+                    const float s0 = gb1 ? yp : ssum, s1 = gb1 ? dd : 0.0f;
+                    k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+                    k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+                    float v = gb0 ? k1 : k0;
+                    v += __shfl_xor_sync(0xffffffffu, gb0 ? k0 : k1, 8);
+                    const float o = g == 0 ? (v + Dd * ta.w) * tb.y
+                                           : (g == 1 ? v * tb.x : fmaf(ta.x, v, ta.z * Dd));
+                    dbacc += g == 1 ? o : 0.0f;
+                    Elem<T>::store_if(has_out && j < nst, orow + j * a.d_inner, o);
+                }
                 // dB and dC over the warp's 8 channels: reduce-scatter of the
                 // lane's 2*NS values [dB | dC], lane ch keeping a slice
                 float bc[2 * NS];
@@ -1099,6 +1109,38 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
                     red_add_v4_if(lead, p, make_float4(bc[0], bc[1], bc[2], bc[3]));
 #pragma unroll
                 for (int i = 0; i < NP; ++i) ht[i] = hp[i];
+            }
+            if constexpr (HV == 4) {
+                // (4) per (step, channel) of the tile, as in the prologue: the
+                // channel's four partials summed, then dz, ddt, du stored
+                __syncwarp();
+                const int64_t o0 = ((int64_t)b * a.L + t0) * a.d_inner + d;
+                T* const orow_dz = static_cast<T*>(a.dz ? a.dz : a.du) + o0;
+                T* const orow_dt = static_cast<T*>(a.ddt) + o0;
+                T* const orow_du = static_cast<T*>(a.du) + o0;
+#pragma unroll
+                for (int q = 0; q < PQ; ++q) {
+                    const int e = lane + 32 * q;
+                    const int j = g + G * q;
+                    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+                    for (int g2 = 0; g2 < G; ++g2) {
+                        const float4 v = *reinterpret_cast<const float4*>(
+                            hb + (j * (NS / HV) * 32 + g2 * CPW + ch) * HV);
+                        acc.x += v.x;
+                        acc.y += v.y;
+                        acc.z += v.z;
+                    }
+                    const float4 ta = tab[e];
+                    const float2 tb = tab2[e];
+                    const float ddt = acc.y * tb.x;
+                    dbacc += ddt;  // zero past L (sigmoid entry zero)
+                    const bool in = j < nst;
+                    const int64_t off = (int64_t)j * a.d_inner;
+                    Elem<T>::store_if(in, orow_dt + off, ddt);
+                    Elem<T>::store_if(in, orow_du + off, fmaf(ta.x, acc.z, ta.z * Dd));
+                    Elem<T>::store_if(in && a.dz, orow_dz + off, (acc.x + Dd * ta.w) * tb.y);
+                }
             }
 #pragma unroll
             for (int i = 0; i < NP; ++i) hin[i] = hnext[i];
@@ -1127,7 +1169,13 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
     dDacc += __shfl_xor_sync(0xffffffffu, dDacc, 8);
     dDacc += __shfl_xor_sync(0xffffffffu, dDacc, 16);
     if (g == 0 && a.dD) atomicAdd(a.dD + d, dDacc);
-    if (g == 1 && a.ddt_bias) atomicAdd(a.ddt_bias + d, dbacc);
+    if constexpr (HV == 4) {  // per-lane sums of the epilogue's steps
+        dbacc += __shfl_xor_sync(0xffffffffu, dbacc, 8);
+        dbacc += __shfl_xor_sync(0xffffffffu, dbacc, 16);
+        if (g == 0 && a.ddt_bias) atomicAdd(a.ddt_bias + d, dbacc);
+    } else {
+        if (g == 1 && a.ddt_bias) atomicAdd(a.ddt_bias + d, dbacc);
+    }
 }
 
 // B and C as fp32 rows for the [TT x N] fp32 TMA boxes; 8 elements per
