@@ -498,7 +498,7 @@ msc_status msc_selective_scan_bwd(const void* u, const void* dt, const float* A,
         e = msc::launch_scan_bwd_tma(a, dtype, ck, s);
     } else {
         a.ckpt = static_cast<float*>(ck);
-        e = msc::launch_scan_bwd(a, dtype, true, s);
+        e = msc::launch_scan_bwd(a, dtype, s);
     }
     const cudaError_t f = cudaFreeAsync(ck, s);
     if (e == cudaSuccess) e = f;

@@ -48,7 +48,6 @@ struct ScanPlan {
     size_t ws_carry;   // bytes of chunk summaries (a then b), 0 when K == 1
     size_t ws_bc;      // bytes of fp32 copies of B then C for the TMA boxes
     size_t ws_bytes;   // total workspace (carry, then B/C copies, 256-aligned)
-    int summaries_only;  // 1: stop after the chunk summaries and carry prefix (no outputs)
 };
 
 struct UpdateArgs {
@@ -116,10 +115,9 @@ struct BwdArgs {
     int64_t batch, L, d_inner, N, nseg;
     int vec;           // 1: B/C rows can be read 4 elements at a time
 };
-// generic_ckpt: compute the checkpoints with the element-load kernel first
-// (otherwise a.ckpt already holds them).
-cudaError_t launch_scan_bwd(const BwdArgs& a, msc_dtype dtype, bool generic_ckpt,
-                            cudaStream_t s);
+// The element-load checkpoint kernel, then the element-load adjoint (a.ckpt:
+// scan_bwd_ckpt_bytes of scratch).
+cudaError_t launch_scan_bwd(const BwdArgs& a, msc_dtype dtype, cudaStream_t s);
 size_t scan_bwd_ckpt_bytes(int64_t batch, int64_t L, int64_t d_inner, int64_t N);
 // The TMA backward (scan_tma.cu): N in {8, 16, 32, 64}, d_inner % 8 == 0,
 // 16-byte aligned u / dt / z / dout / dB / dC.  One kernel walks each

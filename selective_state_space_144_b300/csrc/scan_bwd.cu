@@ -279,10 +279,10 @@ size_t scan_bwd_ckpt_bytes(int64_t batch, int64_t L, int64_t d_inner, int64_t N)
 }
 
 template <typename T, int G, bool VEC>
-static cudaError_t launch_bwd_g(BwdArgs a, bool generic_ckpt, cudaStream_t s) {
+static cudaError_t launch_bwd_g(BwdArgs a, cudaStream_t s) {
     constexpr int CPB = kBwdThreads / G;
     const dim3 grid((unsigned)((a.d_inner + CPB - 1) / CPB), (unsigned)a.batch);
-    if (generic_ckpt && a.nseg > 1) {
+    if (a.nseg > 1) {
         scan_bwd_ckpt_kernel<T, G, VEC><<<grid, kBwdThreads, 0, s>>>(a);
         profile_count(1);
     }
@@ -298,23 +298,21 @@ static cudaError_t launch_bwd_g(BwdArgs a, bool generic_ckpt, cudaStream_t s) {
 }
 
 template <typename T, bool VEC>
-static cudaError_t launch_bwd_v(const BwdArgs& a, bool gc, cudaStream_t s) {
+static cudaError_t launch_bwd_v(const BwdArgs& a, cudaStream_t s) {
     switch (lanes_per_channel(a.N)) {
-        case 1: return launch_bwd_g<T, 1, VEC>(a, gc, s);
-        case 2: return launch_bwd_g<T, 2, VEC>(a, gc, s);
-        case 4: return launch_bwd_g<T, 4, VEC>(a, gc, s);
-        case 8: return launch_bwd_g<T, 8, VEC>(a, gc, s);
-        default: return launch_bwd_g<T, 16, VEC>(a, gc, s);
+        case 1: return launch_bwd_g<T, 1, VEC>(a, s);
+        case 2: return launch_bwd_g<T, 2, VEC>(a, s);
+        case 4: return launch_bwd_g<T, 4, VEC>(a, s);
+        case 8: return launch_bwd_g<T, 8, VEC>(a, s);
+        default: return launch_bwd_g<T, 16, VEC>(a, s);
     }
 }
 
-cudaError_t launch_scan_bwd(const BwdArgs& a, msc_dtype dtype, bool generic_ckpt,
-                            cudaStream_t s) {
+cudaError_t launch_scan_bwd(const BwdArgs& a, msc_dtype dtype, cudaStream_t s) {
     if (dtype == MSC_BF16)
-        return a.vec ? launch_bwd_v<__nv_bfloat16, true>(a, generic_ckpt, s)
-                     : launch_bwd_v<__nv_bfloat16, false>(a, generic_ckpt, s);
-    return a.vec ? launch_bwd_v<float, true>(a, generic_ckpt, s)
-                 : launch_bwd_v<float, false>(a, generic_ckpt, s);
+        return a.vec ? launch_bwd_v<__nv_bfloat16, true>(a, s)
+                     : launch_bwd_v<__nv_bfloat16, false>(a, s);
+    return a.vec ? launch_bwd_v<float, true>(a, s) : launch_bwd_v<float, false>(a, s);
 }
 
 }  // namespace msc

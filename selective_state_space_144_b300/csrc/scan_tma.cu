@@ -1266,10 +1266,6 @@ static cudaError_t launch_tma_d(const ScanArgs& a, const ScanPlan& p, const CUte
         const cudaError_t e = launch_carry_prefix(a, s);
         if (e != cudaSuccess) return e;
     }
-    if (p.summaries_only) {
-        profile_count(p.K > 1 ? 2 : 0);
-        return cudaGetLastError();
-    }
     const int64_t nb = a.batch * (int64_t)p.K * p.ntile;
     const ProfileMark m = profile_begin(s, MSC_PROF_SCAN);
     auto kern = scan_tma_kernel<T, G, NS, TT, S, DISC>;
