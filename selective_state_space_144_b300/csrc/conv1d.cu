@@ -25,7 +25,7 @@
 namespace msc {
 
 constexpr int kConvThreads = 128;
-constexpr int kTileT = 16;
+constexpr int kTileT = 32;
 
 template <typename T, int V> struct Vec;
 template <> struct Vec<float, 1> { using type = float; };
