@@ -123,3 +123,36 @@ def test_bwd_after_scratch_release():
     check(x, seed=12)
     msc.scratch_release()
     check(x, seed=12)
+
+
+def test_bwd_tma_one_channel_group_long():
+    """One CTA (batch 1, 8 channels) over 17 tiles of 16 steps, the last
+    ragged: every checkpoint of the forward walk is used by the reverse walk."""
+    x = synth.scan_inputs(1, 257, 8, 16, dtype="bf16", seed=970, D="normal")
+    h0 = np.random.default_rng(13).standard_normal((1, 8, 16)).astype(np.float32)
+    check(x, h0=h0, seed=14)
+
+
+def test_bwd_tma_d_state_64_many_tiles():
+    """d_state 64 (16 states per lane, the largest register footprint) over
+    38 tiles of 8 steps, fp32 storage."""
+    x = synth.scan_inputs(2, 300, 16, 64, dtype="f32", seed=975, D="normal", A_kind="random")
+    check(x, seed=15)
+
+
+def test_bwd_tma_repeatable():
+    """The gradients written without atomics (du, ddt, dz, dh0) are bitwise
+    equal from call to call; the atomically summed ones agree to rounding."""
+    x = synth.scan_inputs(2, 200, 64, 16, dtype="bf16", seed=980, D="normal")
+    a = scan_device_args(x)
+    dout = to_device(synth.round_bf16(np.random.default_rng(16).standard_normal(
+        x.u.shape).astype(np.float32)), "bf16")
+    g1 = msc.selective_scan_bwd(a["u"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                                a["dt_bias"], dout=dout, want_dh0=True)
+    g2 = msc.selective_scan_bwd(a["u"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                                a["dt_bias"], dout=dout, want_dh0=True)
+    torch.cuda.synchronize()
+    for k in ("du", "ddt", "dz", "dh0"):
+        assert torch.equal(g1[k], g2[k]), k
+    for k in ("dA", "dB", "dC", "dD", "ddt_bias"):
+        assert rel_l2(from_device(g1[k]), from_device(g2[k]).astype(np.float64)) <= 1e-6, k
