@@ -60,7 +60,7 @@ def test_conv_shapes(dtype, d_conv, d_inner):
           conv_case(2, 1, d_inner, d_conv, dtype, 1, with_state=True)[3], dtype)
 
 
-@pytest.mark.parametrize("L", [0, 1, 2, 3, 4, 63, 64, 65, 129])
+@pytest.mark.parametrize("L", [0, 1, 2, 3, 4, 31, 32, 33, 63, 64, 65, 129])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_conv_lengths(L, dtype):
     """Sequences shorter than the window, exactly one tile, ragged tiles; the
