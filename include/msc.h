@@ -88,8 +88,9 @@ typedef enum msc_status {
  *   D, dt_bias    : (d_inner) fp32                     nullable: 0
  *   last_state    : (batch, d_inner, d_state) fp32     nullable: not written
  * With L == 0 last_state is set to zero.  Scratch for the inter-chunk carry,
- * when the plan needs it, is taken stream-ordered (cudaMallocAsync /
- * cudaFreeAsync on `stream`); use msc_selective_scan_fwd_ws to pass it in.
+ * when the plan needs it, is taken stream-ordered on `stream` from the
+ * library's memory pool (see msc_scratch_release); use
+ * msc_selective_scan_fwd_ws to pass it in.
  */
 msc_status msc_selective_scan_fwd(
     const void* u, const void* dt, const float* A, const void* B,
