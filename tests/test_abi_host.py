@@ -223,3 +223,34 @@ def test_conv_entry_points_validate(lib):
         ctypes.c_void_p]
     assert g(None, FAKE, FAKE, None, FAKE, 2, 16, 4, 1, 1, None) == 1   # state needed
     assert g(FAKE, FAKE, FAKE, None, FAKE, 2, 16, 12, 1, 1, None) == 2
+
+
+def test_bwd_entry_point_validates(lib):
+    """msc_selective_scan_bwd refuses bad arguments before touching the GPU;
+    an empty batch is a no-op."""
+    f = lib.msc_selective_scan_bwd
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 20 + [ctypes.c_int64] * 4 + [ctypes.c_int, ctypes.c_void_p]
+
+    def bwd(**k):
+        p = {n: k.get(n, FAKE) for n in ("u", "dt", "A", "B", "C", "dout", "du", "ddt",
+                                         "dA", "dB", "dC")}
+        return f(p["u"], p["dt"], p["A"], p["B"], p["C"], None, None, None, None, p["dout"],
+                 None, p["du"], p["ddt"], p["dA"], p["dB"], p["dC"], None, None, None,
+                 k.get("dh0", None), k.get("batch", 2), k.get("L", 8), 16, k.get("N", 16),
+                 k.get("dtype", 1), None)
+
+    assert bwd(dtype=3) == 1                       # unknown dtype
+    assert bwd(N=0) == 2 and bwd(N=65) == 2        # d_state outside 1..64
+    assert bwd(L=-1) == 1
+    assert bwd(dout=None) == 1 and bwd(dA=None) == 1 and bwd(dB=None) == 1
+    assert bwd(u=FAKE + 1) == 3                    # bf16 storage: 2-byte alignment
+    assert bwd(dA=FAKE + 2) == 3 and bwd(dh0=FAKE + 2) == 3   # fp32 outputs
+    assert bwd(batch=70000) == 2
+    assert bwd(batch=0) == 0                       # nothing to do
+
+
+def test_scratch_release_without_pools(lib):
+    """Before any call has taken scratch there is no pool to trim."""
+    lib.msc_scratch_release.restype = ctypes.c_int
+    assert lib.msc_scratch_release() == 0
