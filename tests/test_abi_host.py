@@ -254,3 +254,29 @@ def test_scratch_release_without_pools(lib):
     """Before any call has taken scratch there is no pool to trim."""
     lib.msc_scratch_release.restype = ctypes.c_int
     assert lib.msc_scratch_release() == 0
+
+
+def test_trapezoid_entry_points_validate(lib):
+    """The exponential-trapezoid scan and decode token need lam; its
+    alignment is checked like the other storage arrays; an empty batch is a
+    no-op."""
+    f = lib.msc_selective_scan_trap_fwd
+    f.restype = ctypes.c_int
+    f.argtypes = ([ctypes.c_void_p] * 14 + [ctypes.c_int64] * 4
+                  + [ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p])
+
+    def trap(lam=FAKE, batch=2, prev=None):
+        return f(FAKE, FAKE, lam, FAKE, FAKE, FAKE, None, None, None, None, prev, prev,
+                 FAKE, None, batch, 8, 16, 16, 1, None, 0, None)
+
+    assert trap(lam=None) == 1
+    assert trap(lam=FAKE + 1) == 3                 # bf16 storage
+    assert trap(prev=FAKE + 1) == 3                # u_prev / B_prev too
+    assert trap(batch=0) == 0
+    g = lib.msc_selective_state_update_trap
+    g.restype = ctypes.c_int
+    g.argtypes = [ctypes.c_void_p] * 13 + [ctypes.c_int64] * 3 + [ctypes.c_int, ctypes.c_void_p]
+    assert g(FAKE, None, None, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, None, None, FAKE,
+             4, 16, 16, 1, None) == 1              # lam required
+    assert g(FAKE, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE,
+             4, 16, 0, 1, None) == 2               # d_state 0
