@@ -137,9 +137,18 @@ msc_status msc_selective_scan_fwd_ws(
  *   - A problem whose plan needs more scratch than that returns
  *     MSC_ERR_SCRATCH_LIMIT before anything is launched (query the need with
  *     msc_selective_scan_workspace_size).
- *   - The first call on each device looks up the array's device address
- *     with cudaGetSymbolAddress while that device is current; make that
- *     first call before any stream capture on that device.
+ *   - Every call whose stream is not being captured looks up the array's
+ *     device address with cudaGetSymbolAddress on the current device (so
+ *     the address is right again after a device reset, which reloads the
+ *     module, possibly at another address); a call on a capturing stream
+ *     uses the address the last uncaptured call on that device found, and
+ *     fails with MSC_ERR_CUDA when there was none.  Make the first call on
+ *     each device before any stream capture on it.
+ *   - With CUDA's default lazy module loading, the array is mapped on a
+ *     device by the first call into this library on that device, and that
+ *     mapping is a device allocation.  A caller that may not allocate while
+ *     serving makes one call into the library on each device at start-up
+ *     (a scan of any size will do), before serving begins.
  *   - All calls share the one array, and it keeps the last call's contents;
  *     nothing in it needs to start at zero (every byte a call reads was
  *     written earlier in the same call).  Calls whose executions overlap on
@@ -321,6 +330,9 @@ msc_status msc_selective_state_update_trap(
  * reads that word -- call it after synchronising the streams the library
  * was used on -- and returns MSC_ERR_TIMEOUT when it is set, MSC_OK
  * otherwise; a nonzero `clear` resets it.  MSC_ERR_CUDA if the read fails.
+ * Each device has its own word and this reads the CURRENT device's only: a
+ * caller that runs the library on several devices calls it once per device,
+ * with that device current.
  */
 msc_status msc_check_device_error(int clear);
 
@@ -341,6 +353,16 @@ msc_status msc_scratch_release(void);
  *   "scan_min_chunk" shortest chunk the automatic plan will make (steps)
  *   "scan_path"     0 = automatic, 1 = element-load kernels only (no TMA)
  *   "scan_lanes"    lanes per channel of the TMA kernels: 0 = automatic, 2, 4
+ *   "update_path"   0 = automatic (N = 16: the copy-engine streaming decode
+ *                   kernel where sizes and alignment allow), 1 = the
+ *                   thread-per-channel decode kernels only
+ *   "debug_starve_copies"  failure-detection test, 0 (default) = off; n > 0:
+ *                   the forward scan's TMA kernels issue none of their data
+ *                   copies and give up each wait after n polls, so every
+ *                   such launch ends through the bounded-wait exit (device
+ *                   word set, msc_check_device_error -> MSC_ERR_TIMEOUT,
+ *                   outputs not written).  No copy is in flight when the
+ *                   kernel returns and nothing faults.
  * Process-wide and not thread-safe; returns MSC_ERR_INVALID_ARG for an
  * unknown key or a negative value.
  */

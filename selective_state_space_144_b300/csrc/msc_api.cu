@@ -14,6 +14,8 @@ int64_t g_force_chunks = 0;    // "scan_chunks"
 int64_t g_min_chunk = 512;     // "scan_min_chunk"
 int64_t g_scan_path = 0;       // "scan_path": 0 auto, 1 element-load kernels only
 int64_t g_scan_lanes = 0;      // "scan_lanes": TMA kernels' lanes per channel, 0 auto
+int64_t g_starve = 0;          // "debug_starve_copies": poll limit of starved waits, 0 off
+int64_t g_update_path = 1;     // "update_path": 0 auto, 1 thread-per-channel kernels only
 
 bool aligned(const void* p, size_t a) {
     return (reinterpret_cast<uintptr_t>(p) % a) == 0;
@@ -232,6 +234,8 @@ static msc_status run_scan(const void* u, const void* dt, const float* A, const 
     a.ws_b = c.plan.ws_carry ? static_cast<float*>(w) + half : nullptr;
     a.batch = batch; a.L = L; a.d_inner = d_inner; a.N = d_state;
     a.chunk = c.plan.chunk; a.K = c.plan.K; a.ntile = c.plan.ntile; a.vec = c.vec;
+    a.wait_limit = g_starve > 0 ? (uint32_t)g_starve : msc::kWaitLimit;
+    a.starve = g_starve > 0;
     cudaError_t e;
     if (c.plan.tma) {
         float* Bf = nullptr;
@@ -256,13 +260,40 @@ static msc_status run_scan(const void* u, const void* dt, const float* A, const 
 // Callers that may not allocate device memory (a runtime whose allocator owns
 // the device, no allocation while requests are served) get the scan with its
 // scratch here.  Host code must not use the array's name as an address: its
-// device address is looked up once per device with cudaGetSymbolAddress.
+// device address comes from cudaGetSymbolAddress with the device current.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MSC_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kNoallocMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  Looked up
+// afresh on every call whose stream is not being captured (cheap once the
+// module is loaded, and correct again after a device reset reloaded the
+// module at another address); while the stream is being captured the
+// address found by the last such lookup on this device is used, and a
+// capture before any lookup is refused.
+cudaError_t noalloc_scratch(cudaStream_t s, void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kNoallocMaxDevices) return cudaErrorInvalidDevice;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(s, &cap);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (e == cudaSuccess && cap == cudaStreamCaptureStatusNone) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        if (!p) return cudaErrorInvalidSymbol;
+        g_noalloc_addr[dev] = p;
+    } else if (!g_noalloc_addr[dev]) {
+        return e != cudaSuccess ? e : cudaErrorStreamCaptureUnsupported;
+    }
+    *out = g_noalloc_addr[dev];
+    return cudaSuccess;
+}
 }  // namespace
 
 extern "C" {
@@ -279,19 +310,9 @@ msc_status msc_selective_scan_fwd_noalloc(const void* u, const void* dt, const f
     if (batch == 0 || d_inner == 0) return MSC_OK;
     if (c.plan.ws_bytes > MSC_NOALLOC_SCRATCH_BYTES) return MSC_ERR_SCRATCH_LIMIT;
     void* scratch = nullptr;
-    if (c.plan.ws_bytes > 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess) return MSC_ERR_CUDA;
-        if (dev < 0 || dev >= kNoallocMaxDevices) return MSC_ERR_UNSUPPORTED;
-        std::lock_guard<std::mutex> lock(g_noalloc_mu);
-        if (!g_noalloc_addr[dev]) {  // set-up, once per device, that device current
-            void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
-                return MSC_ERR_CUDA;
-            g_noalloc_addr[dev] = p;
-        }
-        scratch = g_noalloc_addr[dev];
-    }
+    if (c.plan.ws_bytes > 0 &&
+        noalloc_scratch(reinterpret_cast<cudaStream_t>(stream), &scratch) != cudaSuccess)
+        return MSC_ERR_CUDA;
     return run_scan(u, dt, A, B, C, D, z, dt_bias, out, last_state, batch, L, d_inner, d_state,
                     dtype, scratch, MSC_NOALLOC_SCRATCH_BYTES, false, stream);
 }
@@ -403,6 +424,9 @@ static msc_status run_update(float* state, const void* u, const void* dt, const 
     a.vec = (d_state % 4 == 0) && aligned(state, 16) && aligned(B, 4 * es) && aligned(C, 4 * es);
     a.zoh = zoh;
     a.trap = lam != nullptr; a.lam = lam; a.u_prev = u_prev; a.B_prev = B_prev;
+    a.stream_ok = g_update_path == 0;
+    a.sms = sm_count();
+    a.wait_limit = msc::kWaitLimit;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     msc::ProfileMark m = msc::profile_begin(s, MSC_PROF_UPDATE);
     cudaError_t e = msc::launch_state_update(a, dtype, s);
@@ -572,6 +596,16 @@ msc_status msc_tuning_set(const char* key, int64_t value) {
         g_scan_path = value;
         return MSC_OK;
     }
+    if (std::strcmp(key, "update_path") == 0) {
+        if (value > 1) return MSC_ERR_INVALID_ARG;
+        g_update_path = value;
+        return MSC_OK;
+    }
+    if (std::strcmp(key, "debug_starve_copies") == 0) {
+        if (value > (int64_t)msc::kWaitLimit) return MSC_ERR_INVALID_ARG;
+        g_starve = value;
+        return MSC_OK;
+    }
     if (std::strcmp(key, "scan_min_chunk") == 0) {
         g_min_chunk = value > 0 ? value : 1;
         return MSC_OK;
@@ -609,9 +643,10 @@ msc_status msc_profile_read(int64_t* launches, int64_t* timed, double* total_ms)
 }
 
 msc_status msc_check_device_error(int clear) {
-    unsigned int v = 0;
+    unsigned int v = 0, w = 0;
     if (msc::scan_error_word(&v, clear != 0) != cudaSuccess) return MSC_ERR_CUDA;
-    return v ? MSC_ERR_TIMEOUT : MSC_OK;
+    if (msc::update_error_word(&w, clear != 0) != cudaSuccess) return MSC_ERR_CUDA;
+    return (v | w) ? MSC_ERR_TIMEOUT : MSC_OK;
 }
 
 msc_status msc_scratch_release(void) {

@@ -148,6 +148,14 @@ template <> struct Elem<__nv_bfloat16> {
     }
 };
 
+// A shared-memory element as fp32 (bf16: its bits are the high half).
+template <typename T> __device__ __forceinline__ float lds_scalar(const T* p);
+template <> __device__ __forceinline__ float lds_scalar<float>(const float* p) { return *p; }
+template <> __device__ __forceinline__ float lds_scalar<__nv_bfloat16>(const __nv_bfloat16* p) {
+    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p))
+                           << 16);
+}
+
 // Load elements [n0, n0 + 4) of a row of `n` elements into v, zero past n.
 template <typename T, bool VEC>
 __device__ __forceinline__ void load_row4(const T* row, int n0, int n, float (&v)[4]) {

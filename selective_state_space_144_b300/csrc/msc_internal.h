@@ -35,6 +35,8 @@ struct ScanArgs {
     int K;             // number of chunks
     int ntile;         // channel tiles per (batch, chunk)
     int vec;           // 1: B/C rows can be read 4 elements at a time
+    uint32_t wait_limit;   // polls before a TMA kernel's wait for a copy gives up
+    int starve;            // failure-detection test: 1 = TMA kernels issue no copies
 };
 
 // How one scan call is cut up.
@@ -68,6 +70,9 @@ struct UpdateArgs {
     const void* lam;   // (batch, d_inner) trapezoid mixing coefficient
     const void* u_prev;  // previous token's u (batch, d_inner) or nullptr
     const void* B_prev;  // previous token's B (batch, N) or nullptr
+    int stream_ok;       // 1: the copy-engine streaming kernel may be used
+    int sms;             // multiprocessor count of the device
+    uint32_t wait_limit; // polls before a bounded wait gives up
 };
 
 // The causal depthwise conv1d before the scan (conv1d.cu).  For the decode
@@ -160,10 +165,12 @@ cudaError_t launch_scan(const ScanArgs& a, const ScanPlan& p, msc_dtype dtype,
 bool tma_scan_supported(int64_t N, int64_t d_inner, msc_dtype dtype, const void* u,
                         const void* dt, const void* z, const void* lam = nullptr);
 int tma_scan_tile(int64_t N);
+constexpr uint32_t kWaitLimit = 1u << 22;  // polls of a bounded wait (~1 s at most)
 cudaError_t launch_scan_tma(const ScanArgs& a, const ScanPlan& p, msc_dtype dtype, float* Bf,
                             float* Cf, cudaStream_t stream);
 cudaError_t scan_error_word(unsigned int* value, bool clear);
 cudaError_t launch_state_update(const UpdateArgs& a, msc_dtype dtype,
                                 cudaStream_t stream);
+cudaError_t update_error_word(unsigned int* value, bool clear);
 
 }  // namespace msc

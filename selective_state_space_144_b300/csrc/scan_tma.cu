@@ -56,7 +56,6 @@ namespace msc {
 // Set (bit 0) by a kernel whose bounded wait for a TMA copy gave up.
 __device__ unsigned int g_scan_error;
 
-constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kOct = 8;  // steps per iteration
 // Row stride (in float2) of a channel's (delta, delta*u) row in shared
 // memory: 8 steps padded to 10 so that the prologue's 8-byte stores from 8
@@ -177,11 +176,12 @@ __device__ __forceinline__ void reduce_scatter(const float (&y)[kOct], int lane,
 // (the lane's channel row of one sDU buffer, indexed by step) for the core.  The u of those steps is returned as pairs for the D*u
 // term.  MASK: steps at or past `nsteps` get delta = 0 and no input (the
 // state passes through).
-template <typename T, int G, int TT, bool MASK, int DISC>
+template <typename T, int G, int TT, bool MASK, int DISC, bool GATE = false>
 __device__ __forceinline__ void octet_prologue(const unsigned char* stage, int row0, int lane_x,
                                                float2* dst, float2* dst2, u64 bias2,
                                                int s0_first, int nsteps,
-                                               u64 (&uu)[kOct / G / 2]) {
+                                               u64 (&uu)[kOct / G / 2],
+                                               u64* gz = nullptr, bool has_z = false) {
     constexpr int CPW = 32 / G;
     constexpr int PPL = kOct / G / 2;
     const T* sx = reinterpret_cast<const T*>(stage) + row0 * CPW + lane_x;
@@ -189,6 +189,11 @@ __device__ __forceinline__ void octet_prologue(const unsigned char* stage, int r
     for (int p = 0; p < PPL; ++p) {
         const int r0 = G * (2 * p) * CPW, r1 = r0 + G * CPW;
         uu[p] = pk2(lds_elem<T>(sx + r0), lds_elem<T>(sx + r1));
+        if constexpr (GATE) {  // silu(z) of the same steps, for the output epilogue
+            if (has_z)
+                gz[p] = silu2(pk2(lds_elem<T>(sx + 2 * TT * CPW + r0),
+                                  lds_elem<T>(sx + 2 * TT * CPW + r1)));
+        }
         const u64 x =
             add2(pk2(lds_elem<T>(sx + TT * CPW + r0), lds_elem<T>(sx + TT * CPW + r1)), bias2);
         const u64 dl = softplus2(x);
@@ -307,7 +312,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         tma_load_3d(st + Lay::kBoff, &tm_B, bar, 0, tt, b);
         tma_load_3d(st + Lay::kCoff, &tm_C, bar, 0, tt, b);
     };
-    int issued = min(S, ntiles);
+    int issued = a.starve ? 0 : min(S, ntiles);
     if (lane == 0)
         for (int i = 0; i < issued; ++i) issue(i);
 
@@ -343,15 +348,22 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const int lane_x = g * CPW + ch;  // element (row g, channel ch) of a [row][CPW] tile
 
 
-    bool ok = ntiles == 0 || __all_sync(0xffffffffu, mbar_wait(bar0, 0, kWaitLimit));
-    int waited = ntiles > 0 ? 1 : 0;  // tiles [0, waited) are known complete
-    u64 u_cur[PPL], u_nxt[PPL];
+    bool ok = ntiles == 0 || __all_sync(0xffffffffu, mbar_wait(bar0, 0, a.wait_limit));
+    int waited = (ntiles > 0 && ok) ? 1 : 0;  // tiles [0, waited) are known complete
+    // Per octet parity: the prologue's u and silu(z) of the lane's output
+    // steps, and the core's per-step partial sums C.h.  The output epilogue
+    // of an octet runs one octet later, beside the next octet's core, so
+    // that its shuffle and store chains overlap independent work.
+    u64 uz[2][PPL], gz[2][PPL];
+    float yv[2][kOct];
 #pragma unroll
-    for (int p = 0; p < PPL; ++p) u_cur[p] = u_nxt[p] = pk2(0.0f, 0.0f);
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int p = 0; p < PPL; ++p) uz[q][p] = gz[q][p] = pk2(0.0f, 0.0f);
     if (ok && ntiles > 0)
-        octet_prologue<T, G, TT, true, DISC>(smem, 0, lane_x, sDU + ch * kDUStride + g,
-                                             sDU + ch * kDUStride + g + kD2, bias2, g, nsteps,
-                                             u_cur);
+        octet_prologue<T, G, TT, true, DISC, true>(smem, 0, lane_x, sDU + ch * kDUStride + g,
+                                                   sDU + ch * kDUStride + g + kD2, bias2, g,
+                                                   nsteps, uz[0], gz[0], has_z);
     __syncwarp();
 
     const u64 D2 = pk2(Dd, Dd);
@@ -360,26 +372,65 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     T* out_p = static_cast<T*>(a.out) + ((int64_t)b * a.L + tc0 + g) * dinner + d;
     int st_idx = 0;                               // stage of tile i
 
-    // One tile: OPT octets, unrolled so that every shared-memory offset is a
-    // constant.  FULL: the tile lies inside the chunk, no step is masked.
+    // Outputs of steps g + G*m of channel ch of the octet of parity Q whose
+    // first row is chunk step sb, at op: reduce-scatter the partial sums,
+    // add D*u, apply the gate, store.  MASKED: only steps before nsteps.
+    auto epilogue = [&](auto q_tag, auto masked_tag, int sb, T* op) {
+        constexpr int Q = decltype(q_tag)::value;
+        constexpr bool MASKED = decltype(masked_tag)::value;
+        float ys[SPL];
+        reduce_scatter<G>(yv[Q], lane, ys);
+#pragma unroll
+        for (int p = 0; p < PPL; ++p) {
+            u64 y2 = fma2(D2, uz[Q][p], pk2(ys[2 * p], ys[2 * p + 1]));
+            if (has_z) y2 = mul2(y2, gz[Q][p]);
+            T* o = op + (2 * p) * gstride;
+            if (!MASKED) {
+                Elem<T>::store(o, lo2(y2));
+                Elem<T>::store(o + gstride, hi2(y2));
+            } else {
+                const int s0 = sb + g + G * (2 * p);
+                if (s0 < nsteps) Elem<T>::store(o, lo2(y2));
+                if (s0 + G < nsteps) Elem<T>::store(o + gstride, hi2(y2));
+            }
+        }
+    };
+    using P0 = std::integral_constant<int, 0>;
+    using P1 = std::integral_constant<int, 1>;
+    using Unmasked = std::integral_constant<bool, false>;
+    using Masked = std::integral_constant<bool, true>;
+
+    // One tile: OPT octets, unrolled so that every shared-memory offset and
+    // every parity index is a constant.  FULL: the tile lies inside the
+    // chunk, no step is masked.  OPT is even, so the octet of parity 1 that
+    // ends a tile is the one pending when the next tile starts.
+    static_assert(OPT % 2 == 0, "parity ring needs an even number of octets per tile");
     auto tile_body = [&](int i, auto full_tag) {
         constexpr bool FULL = decltype(full_tag)::value;
         const unsigned char* st = smem + st_idx * Lay::kStage;
         const int nxt_idx = st_idx + 1 == S ? 0 : st_idx + 1;
         const float* sB0 = reinterpret_cast<const float*>(st + Lay::kBoff) + n0;
         const float* sC0 = reinterpret_cast<const float*>(st + Lay::kCoff) + n0;
-        const T* sz0 = reinterpret_cast<const T*>(st + 2 * Lay::kX) + lane_x;
+        bool flushed = false;
 #pragma unroll
         for (int oo = 0; oo < OPT; ++oo) {
             const int sb = i * TT + kOct * oo;  // chunk step of the octet's first row
-            if (!FULL && sb >= nsteps) break;   // past the end of a partial tile
+            if (!FULL && sb >= nsteps) {        // past the end of a partial tile:
+                if (oo > 0) {                   // emit the pending octet, oo - 1
+                    if ((oo - 1) & 1)
+                        epilogue(P1{}, Masked{}, sb - kOct, out_p - kOct * dinner);
+                    else
+                        epilogue(P0{}, Masked{}, sb - kOct, out_p - kOct * dinner);
+                }
+                flushed = true;
+                break;
+            }
             // (1) the state updates of this octet
             const float4* sd =
                 reinterpret_cast<const float4*>(sDU + ((oo & 1) * CPW + ch) * kDUStride);
             [[maybe_unused]] const float4* sd2 = sd + kD2 / 2;  // trapezoid: ((1-lambda)*delta, u)
             const float* sB = sB0 + kOct * oo * N;
             const float* sC = sC0 + kOct * oo * N;
-            float yv[kOct];
 #pragma unroll
             for (int j = 0; j < kOct; ++j) {
                 const float4 v2 = sd[j >> 1];  // steps j & ~1 and (j & ~1) + 1
@@ -424,51 +475,52 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                     hp[i2] = fma2(dA, hp[i2], inj);
                     y2 = fma2(Cp[i2], hp[i2], y2);
                 }
-                yv[j] = lo2(y2) + hi2(y2);
+                yv[oo & 1][j] = lo2(y2) + hi2(y2);
             }
-            // (2) the next octet's step sizes, after the core's reads of this
-            //     octet's (next tile: wait for it first)
+            // (2) outputs of the previous octet (the last of the previous
+            //     tile for oo = 0, a full tile: unmasked)
+            if (oo > 0) {
+                if ((oo - 1) & 1)
+                    epilogue(P1{}, std::integral_constant<bool, !FULL>{}, sb - kOct,
+                             out_p - kOct * dinner);
+                else
+                    epilogue(P0{}, std::integral_constant<bool, !FULL>{}, sb - kOct,
+                             out_p - kOct * dinner);
+            } else if (i > 0) {
+                epilogue(P1{}, Unmasked{}, sb - kOct, out_p - kOct * dinner);
+            }
+            // (3) the next octet's step sizes, u and gate (next tile: wait
+            //     for it first)
             float2* const dnx = sDU + (((oo + 1) & 1) * CPW + ch) * kDUStride + g;
+            u64(&un)[PPL] = uz[(oo + 1) & 1];
+            u64* gn = gz[(oo + 1) & 1];
             if (oo + 1 < OPT) {
-                octet_prologue<T, G, TT, !FULL, DISC>(st, kOct * (oo + 1), lane_x, dnx, dnx + kD2, bias2,
-                                                sb + kOct + g, nsteps, u_nxt);
+                octet_prologue<T, G, TT, !FULL, DISC, true>(st, kOct * (oo + 1), lane_x, dnx,
+                                                            dnx + kD2, bias2, sb + kOct + g,
+                                                            nsteps, un, gn, has_z);
             } else if (i + 1 < ntiles) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * nxt_idx,
-                                                       ((i + 1) / S) & 1, kWaitLimit));
+                                                       ((i + 1) / S) & 1, a.wait_limit));
                 if (!ok) return;
                 waited = i + 2;
                 const unsigned char* stn = smem + nxt_idx * Lay::kStage;
                 if ((i + 2) * TT <= nsteps)
-                    octet_prologue<T, G, TT, false, DISC>(stn, 0, lane_x, dnx, dnx + kD2, bias2, sb + kOct + g,
-                                                    nsteps, u_nxt);
+                    octet_prologue<T, G, TT, false, DISC, true>(stn, 0, lane_x, dnx, dnx + kD2,
+                                                                bias2, sb + kOct + g, nsteps,
+                                                                un, gn, has_z);
                 else
-                    octet_prologue<T, G, TT, true, DISC>(stn, 0, lane_x, dnx, dnx + kD2, bias2, sb + kOct + g,
-                                                   nsteps, u_nxt);
-            }
-            // (3) outputs of steps g + G*m of channel ch
-            float ys[SPL];
-            reduce_scatter<G>(yv, lane, ys);
-#pragma unroll
-            for (int p = 0; p < PPL; ++p) {
-                u64 y2 = fma2(D2, u_cur[p], pk2(ys[2 * p], ys[2 * p + 1]));
-                const int r0 = (kOct * oo + G * (2 * p)) * CPW, r1 = r0 + G * CPW;
-                if (has_z)
-                    y2 = mul2(y2, silu2(pk2(lds_elem<T>(sz0 + r0), lds_elem<T>(sz0 + r1))));
-                T* op = out_p + (2 * p) * gstride;
-                if (FULL) {
-                    Elem<T>::store(op, lo2(y2));
-                    Elem<T>::store(op + gstride, hi2(y2));
-                } else {
-                    const int s0 = sb + g + G * (2 * p);
-                    if (s0 < nsteps) Elem<T>::store(op, lo2(y2));
-                    if (s0 + G < nsteps) Elem<T>::store(op + gstride, hi2(y2));
-                }
+                    octet_prologue<T, G, TT, true, DISC, true>(stn, 0, lane_x, dnx, dnx + kD2,
+                                                               bias2, sb + kOct + g, nsteps,
+                                                               un, gn, has_z);
             }
             out_p += kOct * dinner;
             __syncwarp();
-#pragma unroll
-            for (int p = 0; p < PPL; ++p) u_cur[p] = u_nxt[p];
         }
+        // the chunk's last octet of a full tile is still pending
+        if (FULL && i + 1 == ntiles && !flushed)
+            epilogue(P1{}, Unmasked{}, i * TT + TT - kOct, out_p - kOct * dinner);
+        if (!FULL && !flushed)  // a partial tile whose octets were all run
+            epilogue(P1{}, Masked{}, i * TT + TT - kOct, out_p - kOct * dinner);
         // (4) the tile is consumed: refill its stage
         if (i + S < ntiles) {
             if (lane == 0) {
@@ -491,7 +543,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         // a copy never completed: flag it, give the copies still in flight a
         // bounded chance to land in this CTA's shared memory, then leave
         if (lane == 0) atomicOr(&g_scan_error, 1u);
-        for (int i = waited; i < issued; ++i) mbar_wait(bar0 + 8 * (i % S), (i / S) & 1, kWaitLimit);
+        for (int i = waited; i < issued; ++i) mbar_wait(bar0 + 8 * (i % S), (i / S) & 1, a.wait_limit);
         return;
     }
 
@@ -569,7 +621,7 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
         if (TRAP) tma_load_3d(st + Lay::kLam, &tm_lam, bar, d0, tt, b);
         tma_load_3d(st + Lay::kBoff, &tm_B, bar, 0, tt, b);
     };
-    int issued = min(S, ntiles);
+    int issued = a.starve ? 0 : min(S, ntiles);
     if (lane == 0)
         for (int r = 0; r < issued; ++r) issue(r);
 
@@ -591,8 +643,8 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
     const int lane_x = g * CPW + ch;
     u64 uu[PPL];
 
-    bool ok = ntiles == 0 || __all_sync(0xffffffffu, mbar_wait(bar0, 0, kWaitLimit));
-    int waited = ntiles > 0 ? 1 : 0;
+    bool ok = ntiles == 0 || __all_sync(0xffffffffu, mbar_wait(bar0, 0, a.wait_limit));
+    int waited = (ntiles > 0 && ok) ? 1 : 0;
     if (ok && ntiles > 0)
         octet_prologue<T, G, TT, false, DISC>(smem, kOct * (OPT - 1), lane_x,
                                               sDU + ch * kDUStride + g,
@@ -658,7 +710,7 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
                 octet_prologue<T, G, TT, false, DISC>(st, kOct * (oo - 1), lane_x, dnx, dnx + kD2, bias2, 0, 0, uu);
             } else if (r + 1 < ntiles) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * ((r + 1) % S),
-                                                       ((r + 1) / S) & 1, kWaitLimit));
+                                                       ((r + 1) / S) & 1, a.wait_limit));
                 if (!ok) break;
                 waited = r + 2;
                 octet_prologue<T, G, TT, false, DISC>(smem + ((r + 1) % S) * Lay::kStage,
@@ -685,7 +737,7 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
         }
     }
     // copies still in flight (early stop or a failed wait) land before exit
-    for (int r = waited; r < issued; ++r) mbar_wait(bar0 + 8 * (r % S), (r / S) & 1, kWaitLimit);
+    for (int r = waited; r < issued; ++r) mbar_wait(bar0 + 8 * (r % S), (r / S) & 1, a.wait_limit);
     if (!ok) {
         if (lane == 0) atomicOr(&g_scan_error, 1u);
         return;

@@ -177,8 +177,197 @@ state_update_row_kernel(UpdateArgs a) {
     Elem<T>::store(static_cast<T*>(a.out) + ch, y);
 }
 
+// Set (bit 0) by a decode kernel whose bounded wait for a copy gave up.
+__device__ unsigned int g_update_error;
+
+// Decode step for N = 16 with the state streamed by the copy engine.  A CTA
+// owns one tile of kStreamCh channels of every R-th batch row (rows r, r+R,
+// ...) and walks those tiles through a ring of kStreamStages shared-memory
+// stages: one thread issues 1-D bulk copies of each tile's state rows (8 KB),
+// u, dt, z (kStreamCh elements each) and the row's B, C into a stage,
+// completing the stage's mbarrier, kStreamAhead tiles ahead; the CTA updates
+// the states in place in shared memory and the same thread copies the tile's
+// state back with a bulk store.  So the HBM stream is kept in flight by the
+// copy engine rather than by the threads' registers, and A, dt_bias and D
+// of the CTA's channels are read once per CTA.  Work split inside a tile:
+// thread t owns the float4 of states (t % 4) of channels t / 4, 32 + t / 4,
+// 64 + t / 4, 96 + t / 4, so every shared access of a warp is 512
+// contiguous bytes; the four partial C.h of a channel are summed with two
+// shuffles.
+constexpr int kStreamCh = 128;
+constexpr int kStreamStages = 6;
+constexpr int kStreamAhead = 4;   // tiles loading while one is updated and one stored
+constexpr int kStreamThreads = 128;
+
+template <typename T>
+struct StreamLayout {
+    static constexpr int N = 16;
+    static constexpr int kState = kStreamCh * N * 4;                    // 8192
+    static constexpr int kX = kStreamCh * (int)sizeof(T);               // u / dt / z
+    static constexpr int kBC = N * (int)sizeof(T);                      // B / C row
+    static constexpr int kU = kState, kDt = kU + kX, kZ = kDt + kX;
+    static constexpr int kB = kZ + kX, kC = kB + ((kBC + 15) / 16) * 16;
+    static constexpr int kStage = ((kC + kBC + 127) / 128) * 128;
+    static constexpr int kBar = kStreamStages * kStage;
+    static constexpr int kTotal = kBar + kStreamStages * 8;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kStreamThreads)
+state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
+    using Lay = StreamLayout<T>;
+    constexpr int N = Lay::N;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x;
+    const int q = tid & 3;
+    const int j = blockIdx.x % nJ;
+    const int r = blockIdx.x / nJ;
+    const int64_t c0 = (int64_t)j * kStreamCh;
+    const int nch = (int)min((int64_t)kStreamCh, a.d_inner - c0);
+    const int nt = r < a.batch ? (int)((a.batch - 1 - r) / R + 1) : 0;
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + Lay::kBar;
+    const uint32_t xbytes = (uint32_t)(nch * sizeof(T));
+    const uint32_t tx = (uint32_t)(nch * N * 4) + (a.z ? 3u : 2u) * xbytes + 2u * Lay::kBC;
+
+    if (tid == 0) {
+        for (int s2 = 0; s2 < kStreamStages; ++s2) mbar_init(bar0 + 8 * s2, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    auto issue = [&](int t) {  // thread 0: tile t (batch row r + t*R) into stage t % S
+        const int st = t % kStreamStages;
+        const uint32_t dst = sbase + st * Lay::kStage;
+        const uint32_t bar = bar0 + 8 * st;
+        const int64_t b = r + (int64_t)t * R;
+        const int64_t ch = b * a.d_inner + c0;
+        fence_proxy_async_smem();  // earlier generic accesses of the stage come first
+        mbar_expect_tx(bar, tx);
+        bulk_load(dst, a.state + ch * N, (uint32_t)(nch * N * 4), bar);
+        bulk_load(dst + Lay::kU, static_cast<const T*>(a.u) + ch, xbytes, bar);
+        bulk_load(dst + Lay::kDt, static_cast<const T*>(a.dt) + ch, xbytes, bar);
+        if (a.z) bulk_load(dst + Lay::kZ, static_cast<const T*>(a.z) + ch, xbytes, bar);
+        bulk_load(dst + Lay::kB, static_cast<const T*>(a.B) + b * N, Lay::kBC, bar);
+        bulk_load(dst + Lay::kC, static_cast<const T*>(a.C) + b * N, Lay::kBC, bar);
+    };
+    int issued = 0;
+    if (tid == 0) {
+        issued = min(kStreamAhead, nt);
+        for (int t = 0; t < issued; ++t) issue(t);
+    }
+
+    // per-channel constants of the CTA's channels, once
+    float A2[4][4], bias[4], Dd[4];
+    bool valid[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int cl = it * 32 + (tid >> 2);
+        valid[it] = cl < nch;
+        const int64_t d = c0 + (valid[it] ? cl : 0);
+        const float4 av = __ldg(reinterpret_cast<const float4*>(a.A + d * N) + q);
+        A2[it][0] = av.x * kLog2e; A2[it][1] = av.y * kLog2e;
+        A2[it][2] = av.z * kLog2e; A2[it][3] = av.w * kLog2e;
+        bias[it] = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
+        Dd[it] = a.D ? __ldg(a.D + d) : 0.0f;
+    }
+
+    bool ok = true;
+    int t = 0;
+    for (; t < nt; ++t) {
+        const int st = t % kStreamStages;
+        // refill: tile t + Ahead goes into the stage tile t + Ahead - S used;
+        // its state store (committed two iterations ago) must have read it
+        if (tid == 0 && t + kStreamAhead < nt) {
+            bulk_wait_read<1>();
+            issue(t + kStreamAhead);
+            issued = t + kStreamAhead + 1;
+        }
+        ok = __syncthreads_and(mbar_wait(bar0 + 8 * st, (t / kStreamStages) & 1, wait_limit));
+        if (!ok) break;
+        unsigned char* sp = smem + st * Lay::kStage;
+        const T* su = reinterpret_cast<const T*>(sp + Lay::kU);
+        const T* sdt = reinterpret_cast<const T*>(sp + Lay::kDt);
+        const T* sz = reinterpret_cast<const T*>(sp + Lay::kZ);
+        float Bv[4], Cv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            Bv[k] = lds_scalar<T>(reinterpret_cast<const T*>(sp + Lay::kB) + 4 * q + k);
+            Cv[k] = lds_scalar<T>(reinterpret_cast<const T*>(sp + Lay::kC) + 4 * q + k);
+        }
+        const int64_t b = r + (int64_t)t * R;
+        T* outp = static_cast<T*>(a.out) + b * a.d_inner + c0;
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int cl = it * 32 + (tid >> 2);
+            float4* hp = reinterpret_cast<float4*>(sp) + it * kStreamThreads + tid;
+            float4 h = *hp;
+            const float uu = lds_scalar<T>(su + cl);
+            const float delta = softplus(lds_scalar<T>(sdt + cl) + bias[it]);
+            const float du = delta * uu;
+            float hv[4] = {h.x, h.y, h.z, h.w};
+            float y = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float dA = ex2(delta * A2[it][k]);  // same rounding as the scan
+                hv[k] = fmaf(dA, hv[k], du * Bv[k]);
+                y = fmaf(Cv[k], hv[k], y);
+            }
+            *hp = make_float4(hv[0], hv[1], hv[2], hv[3]);
+            y += __shfl_xor_sync(0xffffffffu, y, 1);
+            y += __shfl_xor_sync(0xffffffffu, y, 2);
+            if (q == 0 && valid[it]) {
+                y = fmaf(Dd[it], uu, y);
+                if (a.z) y *= silu(lds_scalar<T>(sz + cl));
+                Elem<T>::store(outp + cl, y);
+            }
+        }
+        fence_proxy_async_smem();  // this thread's states, visible to the bulk store
+        __syncthreads();           // ... and every thread's
+        if (tid == 0) {
+            bulk_store(a.state + (b * a.d_inner + c0) * N, sbase + st * Lay::kStage,
+                       (uint32_t)(nch * N * 4));
+            bulk_commit();
+        }
+    }
+    if (!ok) {
+        // a copy never completed: flag it and give the loads still in flight
+        // a bounded chance to land before the shared memory is released
+        if (tid == 0) {
+            atomicOr(&g_update_error, 1u);
+            for (int w = t; w < issued; ++w)
+                mbar_wait(bar0 + 8 * (w % kStreamStages), (w / kStreamStages) & 1, wait_limit);
+        }
+    }
+    if (tid == 0) bulk_wait_all();  // the stores have read shared memory and landed
+}
+
+bool stream_update_supported(const UpdateArgs& a, size_t es) {
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    return a.N == 16 && !a.zoh && !a.trap && (a.d_inner * (int64_t)es) % 16 == 0 &&
+           al16(a.state) && al16(a.A) && al16(a.u) && al16(a.dt) && al16(a.B) && al16(a.C) &&
+           (!a.z || al16(a.z));
+}
+
+template <typename T>
+static cudaError_t launch_stream(const UpdateArgs& a, int sms, cudaStream_t s) {
+    using Lay = StreamLayout<T>;
+    const int nJ = (int)((a.d_inner + kStreamCh - 1) / kStreamCh);
+    const int64_t target = (int64_t)sms * 3;  // 3 CTAs per SM (48+ KB of stages each)
+    int64_t R = target / nJ;
+    R = R < 1 ? 1 : (R > a.batch ? a.batch : R);
+    const int64_t grid = (int64_t)nJ * R;
+    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+    auto kern = state_update_stream_kernel<T>;
+    if (Lay::kTotal > 48 * 1024)
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kTotal);
+    kern<<<(unsigned)grid, kStreamThreads, Lay::kTotal, s>>>(a, nJ, (int)R, a.wait_limit);
+    return cudaGetLastError();
+}
+
 template <typename T, bool VEC>
 static cudaError_t launch_update_v(const UpdateArgs& a, cudaStream_t s) {
+    if (a.stream_ok && stream_update_supported(a, sizeof(T)))
+        return launch_stream<T>(a, a.sms, s);
     if (VEC && a.batch <= 65535 && (a.N == 8 || a.N == 16 || a.N == 32) &&
         reinterpret_cast<uintptr_t>(a.A) % 16 == 0) {
         const dim3 grid((unsigned)((a.d_inner + 127) / 128), (unsigned)a.batch);
@@ -200,6 +389,15 @@ static cudaError_t launch_update_v(const UpdateArgs& a, cudaStream_t s) {
         default: state_update_kernel<T, 16, VEC><<<nb, kUpdateThreads, 0, s>>>(a); break;
     }
     return cudaGetLastError();
+}
+
+cudaError_t update_error_word(unsigned int* value, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(value, g_update_error, sizeof(unsigned int));
+    if (e == cudaSuccess && clear && *value) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_update_error, &zero, sizeof(unsigned int));
+    }
+    return e;
 }
 
 cudaError_t launch_state_update(const UpdateArgs& a, msc_dtype dtype, cudaStream_t s) {

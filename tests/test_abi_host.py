@@ -130,6 +130,9 @@ def test_tuning_keys(lib):
     assert lib.msc_tuning_set(b"scan_chunks", -1) == 1
     assert lib.msc_tuning_set(None, 1) == 1
     assert lib.msc_tuning_set(b"scan_min_chunk", 512) == 0
+    assert lib.msc_tuning_set(b"debug_starve_copies", -1) == 1
+    assert lib.msc_tuning_set(b"debug_starve_copies", (1 << 22) + 1) == 1
+    assert lib.msc_tuning_set(b"debug_starve_copies", 0) == 0
 
 
 def upd(lib, *, state=FAKE, u=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None,
