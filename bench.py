@@ -165,9 +165,10 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
-    summary, or None when absent or taken on a different kernel source."""
+def recorded_traffic(kernel: str, workload: str, field: str = "dram_bytes_per_launch"):
+    """A per-launch counter (default: DRAM bytes) of `kernel` on `workload`
+    from the committed ncu summary, or None when absent or taken on a
+    different kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -177,7 +178,7 @@ def recorded_traffic(kernel: str, workload: str):
     r = rec.get(f"{kernel}:{workload}")
     if not r or r.get("source_hash") != kernel_source_hash():
         return None
-    return r.get("dram_bytes_per_launch")
+    return r.get(field)
 
 
 # ---------------------------------------------------------------------------
@@ -329,12 +330,17 @@ def run_ours(args):
         step()
     torch.cuda.synchronize(dev)
 
-    # MUFU ex2 peak on this GPU now (sustained ~0.4 s), for the roofline
+    # MUFU ex2 peak on this GPU now (sustained ~0.4 s), for the roofline; the
+    # FP32 FFMA / packed FFMA2 rates for the diagnostic issue bound
     pk = ctypes.CDLL(msc_build.lib_path("libmsc_peaks.so"))
-    pk.msc_peak_ex2.restype = ctypes.c_int
-    pk.msc_peak_ex2.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
-                                ctypes.c_int64, ctypes.c_void_p,
-                                ctypes.POINTER(ctypes.c_float)]
+    for fn in ("msc_peak_ex2", "msc_peak_ffma", "msc_peak_ffma2", "msc_peak_scan_core"):
+        getattr(pk, fn).restype = ctypes.c_int
+        getattr(pk, fn).argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int64, ctypes.c_void_p,
+                                    ctypes.POINTER(ctypes.c_float)]
+    pk.msc_peak_copy.restype = ctypes.c_int
+    pk.msc_peak_copy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                 ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_float)]
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     sink = torch.zeros(4, device=dev)
     msf = ctypes.c_float(0)
@@ -343,30 +349,91 @@ def run_ours(args):
     pk.msc_peak_ex2(sink.data_ptr(), sms * 8, 256, 2000, stream, ctypes.byref(msf))
     pk.msc_peak_ex2(sink.data_ptr(), sms * 8, 256, iters, stream, ctypes.byref(msf))
     ex2_peak = sms * 8 * 256 * iters * 8 / (msf.value * 1e-3)
+    pk.msc_peak_ffma(sink.data_ptr(), sms * 8, 256, 2000, stream, ctypes.byref(msf))
+    pk.msc_peak_ffma(sink.data_ptr(), sms * 8, 256, iters, stream, ctypes.byref(msf))
+    ffma_peak = sms * 8 * 256 * iters * 8 / (msf.value * 1e-3)          # fp32 FMA/s
+    pk.msc_peak_ffma2(sink.data_ptr(), sms * 8, 256, iters, stream, ctypes.byref(msf))
+    ffma2_peak = sms * 8 * 256 * iters * 16 / (msf.value * 1e-3)        # fp32 FMA/s
+    # the scan's update arithmetic alone (registers only), 16 warps per SM
+    core_iters = 20000
+    pk.msc_peak_scan_core(sink.data_ptr(), sms * 4, 128, 500, stream, ctypes.byref(msf))
+    pk.msc_peak_scan_core(sink.data_ptr(), sms * 4, 128, core_iters, stream, ctypes.byref(msf))
+    core_peak = sms * 4 * 128 * core_iters * 32 / (msf.value * 1e-3)     # updates/s
+    # streaming copy of 1 GiB (read + write bytes), the HBM figure of this run
+    cp_src = torch.empty(2**28, dtype=torch.float32, device=dev)
+    cp_dst = torch.empty_like(cp_src)
+    copy_gbs = 0.0
+    for _ in range(3):
+        pk.msc_peak_copy(cp_dst.data_ptr(), cp_src.data_ptr(), 2**30 // 16, sms * 8, stream,
+                         ctypes.byref(msf))
+        copy_gbs = max(copy_gbs, 2 * 2**30 / (msf.value * 1e-3) / 1e9)
+    del cp_src, cp_dst
 
-    # ---- timed region ----------------------------------------------------
+    # ---- the step as a CUDA graph -----------------------------------------
+    # The scan with a caller workspace and the decode step allocate nothing,
+    # so the step (B/C conversion, scan, decode) is captured once and
+    # replayed: the timed region then measures the kernels back to back,
+    # not the Python and C host path of each call (tens to hundreds of
+    # microseconds per call on a busy host, the same order as the kernels).
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K steps, nothing else on the path -------------------
     if ws_n > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize(dev)
-    msc.profile_read()
-    msc.profile_enable(True)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         e0.record()
         for _ in range(args.steps):
-            step()
+            graph.replay()
         e1.record()
         e1.synchronize()
     if ws_n > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    msc.profile_enable(False)
-    launches, kinds = msc.profile_read()
     msc.check_device_error()
     el_ms, value = combine_ranks(e0.elapsed_time(e1), upd_step, args.steps,
                                  ws_n, device=dev)
+
+    # ---- the same K steps as eager calls through the Python API ------------
+    torch.cuda.synchronize(dev)
+    host_s = 0.0
+    e0.record()
+    for _ in range(args.steps):
+        h0_ = time.perf_counter()
+        step()
+        host_s += time.perf_counter() - h0_
+    e1.record()
+    e1.synchronize()
+    eager_ms = e0.elapsed_time(e1) / args.steps
+
+    # ---- kernel times, in a separate pass of the same steps ----------------
+    # The library's measurement hook brackets each call's main kernel with an
+    # event pair on its launch stream and counts the kernels launched; it is
+    # kept out of the timed region above so that its event records and host
+    # bookkeeping do not stretch the step.
+    nk = max(3, min(args.steps, 50))
+    msc.profile_read()
+    msc.profile_enable(True)
+    for _ in range(nk):
+        step()
+    torch.cuda.synchronize(dev)
+    msc.profile_enable(False)
+    launches, kinds = msc.profile_read()
+    launches_per_step = launches / nk
 
     if rank != 0:
         dist.destroy_process_group()
@@ -375,9 +442,24 @@ def run_ours(args):
     peaks, peak_src = measured_peaks()
     n_scan, ms_scan = kinds["scan"]
     scan_ms = ms_scan / max(n_scan, 1)
+    n_upd, ms_upd = kinds["update"]
+    upd_ms = ms_upd / max(n_upd, 1)
     achieved_mufu = mufu_scan / (scan_ms * 1e-3)
     hbm = peaks["hbm_gbs"] * 1e9
     traffic = recorded_traffic("scan_tma_kernel", MAIN)
+    inst = recorded_traffic("scan_tma_kernel", MAIN, field="warp_instructions_per_launch")
+    # issue bound: one warp instruction per clock per SM sub-partition; the
+    # FP32 FFMA rate measured above is that rate times 32 lanes
+    issue_peak = ffma_peak / 32.0
+    issue = None
+    if inst:
+        issue = {"warp_instructions_per_launch": inst,
+                 "per_1024_updates": inst / (upd_scan / 1024.0),
+                 "issue_peak_warp_instr_per_s": issue_peak,
+                 "bound_ms": inst / issue_peak * 1e3,
+                 "frac": (inst / issue_peak) / (scan_ms * 1e-3),
+                 "source": "warp instructions from an ncu capture of this kernel source "
+                           "(profiles/traffic.json); issue rate = measured FFMA rate / 32"}
     roofline = {
         "bound": "alu", "kernel": "scan_tma_kernel (output pass)",
         "achieved": achieved_mufu / 1e12, "peak": ex2_peak / 1e12,
@@ -387,12 +469,29 @@ def run_ours(args):
                         f"({sms} SMs x 8 CTAs x 256 threads x 8 chains)"),
         "traffic": traffic,
         "kernel_ms": scan_ms,
+        "kernel_timing": (f"mean of {n_scan} launches, event pairs on the launch stream "
+                          "in a pass after the timed region"),
         "hbm": {"achieved_gbs": bytes_scan / (scan_ms * 1e-3) / 1e9,
                 "peak_gbs": peaks["hbm_gbs"], "peak_source": peak_src,
                 "frac": bytes_scan / (scan_ms * 1e-3) / hbm,
                 "algorithmic_bytes": bytes_scan},
+        "diagnostic": {
+            "ffma_tflops_measured": ffma_peak * 2 / 1e12,
+            "ffma2_tflops_measured": ffma2_peak * 2 / 1e12,
+            "update_core_ceiling": {
+                "updates_per_s": core_peak,
+                "frac_of_mufu_roofline": core_peak * (1.0 + 4.0 / N_) / ex2_peak,
+                "achieved_frac": (upd_scan / (scan_ms * 1e-3)) / core_peak,
+                "what": ("the scan's per-update instruction mix (mul.f32x2, 2 ex2, mul.f32x2, "
+                         "fma.f32x2, fma.f32x2 per state pair) run from registers with no "
+                         "memory traffic at 16 warps per SM: the rate MUFU and the FMA pipe "
+                         "reach together, the ceiling of the update core"),
+            },
+            "copy_gbs_this_run": copy_gbs,
+            "issue": issue,
+        },
     }
-
+    step_kernels_ms = scan_ms + upd_ms
     # ---- CPU oracle baseline (rank 0, N = 1) ------------------------------
     cpu = None
     if ws_n == 1:
@@ -505,7 +604,19 @@ def run_ours(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": launches,
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "step_timing": {
+            "timed": "CUDA-graph replays of the captured step (3 kernels each)",
+            "main_kernels_ms_per_step": step_kernels_ms,
+            "scan_kernel_ms": scan_ms, "decode_kernel_ms": upd_ms,
+            "kernels_per_step": launches_per_step,
+            "eager_ms_per_step": eager_ms,
+            "eager_host_us_per_step": host_s / args.steps * 1e6,
+            "note": ("eager = the same K steps as Python API calls after the timed region, "
+                     "host time = perf_counter around each step; kernel times from the "
+                     "separate hook pass (the B/C fp32 conversion kernel, a few us, is not "
+                     "in the sum)"),
+        },
         "clocks": clocks,
         "workloads": extras,
     }

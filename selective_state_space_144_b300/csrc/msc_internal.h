@@ -71,6 +71,7 @@ struct UpdateArgs {
     const void* u_prev;  // previous token's u (batch, d_inner) or nullptr
     const void* B_prev;  // previous token's B (batch, N) or nullptr
     int stream_ok;       // 1: the copy-engine streaming kernel may be used
+    int stream_cfg;      // its ring depth / CTAs per SM choice
     int sms;             // multiprocessor count of the device
     uint32_t wait_limit; // polls before a bounded wait gives up
 };

@@ -1,5 +1,6 @@
 // peaks.cu -- roofline denominators measured on the running GPU: MUFU ex2
-// throughput, FP32 FFMA and packed FFMA2 throughput, and a streaming copy.
+// throughput, FP32 FFMA and packed FFMA2 throughput, the rate of the scan's
+// per-update arithmetic alone, and a streaming copy.
 // Each entry point launches its kernel once on `stream` and returns the
 // device time in milliseconds, bracketed by CUDA events on that stream.
 // The operation counts the caller divides by are stated per function.
@@ -70,85 +71,71 @@ __global__ void k_ffma2(float* sink, int64_t iters, float a, float b) {
     if (s == 1234.5f) sink[0] = s;
 }
 
-// The scan's per-update arithmetic without memory traffic: per iteration and
-// thread 16 state updates (1 ex2, 2 FMUL, 2 FFMA each).
-__global__ void k_update_core(float* sink, int64_t iters) {
-    float A2[16], h[16], Bv[16], Cv[16];
+// The scan's per-update arithmetic with no memory traffic at all, as the
+// scan kernels issue it: a lane holds 4 states as two fp32 pairs and per
+// step forms dA = 2^(delta*A2) on MUFU (mul.f32x2 + 2 ex2), the input term
+// (delta*u)*B (mul.f32x2), h = dA*h + input (fma.f32x2) and the partial
+// C.h (fma.f32x2), then adds the pair's halves.  Its rate is the ceiling
+// the scan's update core can reach on this GPU: per update one MUFU
+// operation and four FMA-pipe operations (two packed instructions of two
+// lanes each), issued through the same sub-partition.
+__device__ __forceinline__ unsigned long long pk2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float lo2(unsigned long long v) {
+    return __uint_as_float(static_cast<unsigned>(v & 0xffffffffull));
+}
+__device__ __forceinline__ float hi2(unsigned long long v) {
+    return __uint_as_float(static_cast<unsigned>(v >> 32));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float ex2_f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__global__ void k_scan_core(float* sink, int64_t iters) {
+    unsigned long long A2[2], h[2], B[2], C[2];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        A2[j] = -1.4426950f * (j + 1);
-        h[j] = 0.f;
-        Bv[j] = 0.1f * j - 0.7f;
-        Cv[j] = 0.3f - 0.02f * j;
+    for (int i = 0; i < 2; ++i) {
+        A2[i] = pk2(-1.4426950f * (2 * i + 1), -1.4426950f * (2 * i + 2));
+        h[i] = pk2(0.f, 0.f);
+        B[i] = pk2(0.1f * i - 0.7f, 0.2f - 0.1f * i);
+        C[i] = pk2(0.3f - 0.02f * i, 0.1f * i);
     }
-    float delta = 0.01f + 1e-6f * threadIdx.x, du = 0.5f, acc = 0.f;
+    float dl = 0.01f + 1e-6f * threadIdx.x, du = 0.5f, acc = 0.f;
     for (int64_t it = 0; it < iters; ++it) {
-        float y = 0.f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float dA = ex2_ftz(delta * A2[j]);
-            h[j] = fmaf(dA, h[j], du * Bv[j]);
-            y = fmaf(Cv[j], h[j], y);
+        for (int j = 0; j < 8; ++j) {
+            const float vdl = dl + 1e-7f * j, vdu = du - 1e-7f * j;
+            const unsigned long long dl2 = pk2(vdl, vdl), du2 = pk2(vdu, vdu);
+            unsigned long long y2 = pk2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const unsigned long long x2 = mul2(dl2, A2[i]);
+                const unsigned long long dA = pk2(ex2_f(lo2(x2)), ex2_f(hi2(x2)));
+                h[i] = fma2(dA, h[i], mul2(du2, B[i]));
+                y2 = fma2(C[i], h[i], y2);
+            }
+            acc += lo2(y2) + hi2(y2);
         }
-        acc += y;
-        delta = fmaf(delta, 0.999f, 1e-5f);
+        dl = fmaf(dl, 0.999f, 1e-5f);
         du = fmaf(du, 0.999f, 1e-4f);
     }
     if (acc == 1234.5f) sink[0] = acc;
-}
-
-// Shared-memory load throughput by access pattern: each iteration every
-// lane issues 8 independent volatile loads of W bytes (W = 4, 8 or 16) from
-// 8 precomputed addresses (so the loop is 8 loads + 8 adds).  The element
-// a lane reads within each 512-byte block is set by `pattern`:
-//   0 all lanes the same       1 lane & 3       2 lane >> 2      3 lane
-//   4 lane >> 4                5 lane >> 3      6 lane & 7
-template <int W>
-__global__ void k_lds(float* sink, int64_t iters, int pattern) {
-    __shared__ __align__(16) float sm[4096];
-    for (int i = threadIdx.x; i < 4096; i += blockDim.x) sm[i] = 0.001f * i;
-    __syncthreads();
-    const int lane = threadIdx.x & 31;
-    int sel;
-    switch (pattern) {
-        case 0: sel = 0; break;
-        case 1: sel = lane & 3; break;
-        case 2: sel = lane >> 2; break;
-        case 3: sel = lane; break;
-        case 4: sel = lane >> 4; break;
-        case 5: sel = lane >> 3; break;
-        default: sel = lane & 7; break;
-    }
-    constexpr int E = W / 4;  // floats per load
-    unsigned addr[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-        addr[r] = static_cast<unsigned>(__cvta_generic_to_shared(sm + r * 128 * E / 4 * 4 + sel * E));
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int64_t it = 0; it < iters; ++it) {
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            if (E == 4) {
-                float x, y, z, w;
-                asm volatile("ld.volatile.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                             : "=f"(x), "=f"(y), "=f"(z), "=f"(w) : "r"(addr[r]));
-                acc[r] += x;
-            } else if (E == 2) {
-                float x, y;
-                asm volatile("ld.volatile.shared.v2.f32 {%0, %1}, [%2];"
-                             : "=f"(x), "=f"(y) : "r"(addr[r]));
-                acc[r] += x;
-            } else {
-                float x;
-                asm volatile("ld.volatile.shared.f32 %0, [%1];" : "=f"(x) : "r"(addr[r]));
-                acc[r] += x;
-            }
-        }
-    }
-    float s = 0.f;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) s += acc[r];
-    if (s == 1234.5f) sink[0] = s;
 }
 
 __global__ void k_copy(float4* __restrict__ dst, const float4* __restrict__ src, int64_t n) {
@@ -200,22 +187,10 @@ int msc_peak_ffma2(float* sink, int blocks, int threads, int64_t iters, cudaStre
                  [&] { k_ffma2<<<blocks, threads, 0, s>>>(sink, iters, 0.9999f, 1e-4f); });
 }
 
-// state updates = blocks * threads * iters * 16.
-int msc_peak_update_core(float* sink, int blocks, int threads, int64_t iters,
-                         cudaStream_t s, float* ms) {
-    return timed(s, ms, [&] { k_update_core<<<blocks, threads, 0, s>>>(sink, iters); });
-}
-
-// shared loads (warp instructions) = blocks * (threads / 32) * iters * 8.
-int msc_peak_lds(float* sink, int blocks, int threads, int64_t iters, int width_bytes,
-                 int pattern, cudaStream_t s, float* ms) {
-    if (width_bytes == 16)
-        return timed(s, ms,
-                     [&] { k_lds<16><<<blocks, threads, 0, s>>>(sink, iters, pattern); });
-    if (width_bytes == 8)
-        return timed(s, ms,
-                     [&] { k_lds<8><<<blocks, threads, 0, s>>>(sink, iters, pattern); });
-    return timed(s, ms, [&] { k_lds<4><<<blocks, threads, 0, s>>>(sink, iters, pattern); });
+// state updates = blocks * threads * iters * 32 (8 steps x 4 states).
+int msc_peak_scan_core(float* sink, int blocks, int threads, int64_t iters, cudaStream_t s,
+                       float* ms) {
+    return timed(s, ms, [&] { k_scan_core<<<blocks, threads, 0, s>>>(sink, iters); });
 }
 
 // bytes moved = 2 * n16 * 16 (read + write); n16 = number of 16-byte words.

@@ -58,14 +58,16 @@ __device__ unsigned int g_scan_error;
 
 constexpr int kOct = 8;  // steps per iteration
 // Row stride (in float2) of a channel's (delta, delta*u) row in shared
-// memory: 8 steps padded to 10 so that the prologue's 8-byte stores from 8
-// channels and the core's 16-byte loads (2 steps) hit distinct banks.
-constexpr int kDUStride = 10;
+// memory: the steps of a group padded by 2 (8 -> 10, 16 -> 18) so that the
+// prologue's 8-byte stores from 8 channels and the core's 16-byte loads
+// (2 steps) hit distinct banks.
+constexpr int kDUStride = kOct + 2;
 
 // Shared memory of one CTA: S stages of [u | dt | z | (lambda) | B | C]
 // tiles, the (delta, delta*u) buffers (trapezoid: two sets), the barriers.
-template <typename T, int G, int NS, int TT, int S, bool TRAP = false>
+template <typename T, int G, int NS, int TT, int S, bool TRAP = false, int OCT = kOct>
 struct TmaLayout {
+    static constexpr int DUS = OCT + 2;                 // sDU row stride (float2)
     static constexpr int CPW = 32 / G;                  // channels per warp
     static constexpr int N = G * NS;
     static constexpr int NX = TRAP ? 4 : 3;             // [TT x CPW] tiles per stage
@@ -75,12 +77,12 @@ struct TmaLayout {
     static constexpr int kBoff = NX * kX;               // B tile
     static constexpr int kCoff = kBoff + kBC;           // C tile
     static constexpr int kStage = NX * kX + 2 * kBC;
-    static constexpr int kDU = S * kStage;              // float2 [2][CPW][kDUStride]
-    static constexpr int kDUsz = 2 * CPW * kDUStride * 8;
+    static constexpr int kDU = S * kStage;              // float2 [2][CPW][DUS]
+    static constexpr int kDUsz = 2 * CPW * DUS * 8;
     static constexpr int kBar = kDU + (TRAP ? 2 : 1) * kDUsz;
     static constexpr int kTotal = kBar + S * 8;
     static_assert(kX % 128 == 0 && kBC % 128 == 0, "TMA destinations must stay 128B aligned");
-    static_assert(TT % kOct == 0, "tiles hold whole octets");
+    static_assert(TT % OCT == 0, "tiles hold whole groups of steps");
 };
 
 template <typename T> __device__ __forceinline__ float lds_elem(const T* p);
@@ -133,17 +135,17 @@ __device__ __forceinline__ u64 injection2(u64 x2, u64 dA, u64 dl2, u64 du2, u64 
         return mul2(du2, B2);
 }
 
-// Reduce-scatter of the 8 per-step partial sums over the G lanes of a
+// Reduce-scatter of the V per-step partial sums over the G lanes of a
 // channel (lanes ch, ch + CPW, ...): afterwards out[m] holds the full sum of
-// step g + G*m, m < 8/G.
-template <int G>
-__device__ __forceinline__ void reduce_scatter(const float (&y)[kOct], int lane,
-                                               float (&out)[kOct / G]) {
+// step g + G*m, m < V/G.
+template <int G, int V = kOct>
+__device__ __forceinline__ void reduce_scatter(const float (&y)[V], int lane,
+                                               float (&out)[V / G]) {
     constexpr int CPW = 32 / G;
     if constexpr (G == 2) {
         const bool b0 = (lane / CPW) & 1;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {  // pair (2m, 2m+1): keep step 2m + b0
+        for (int m = 0; m < V / 2; ++m) {  // pair (2m, 2m+1): keep step 2m + b0
             const float send = b0 ? y[2 * m] : y[2 * m + 1];
             const float keep = b0 ? y[2 * m + 1] : y[2 * m];
             out[m] = keep + __shfl_xor_sync(0xffffffffu, send, CPW);
@@ -152,16 +154,16 @@ __device__ __forceinline__ void reduce_scatter(const float (&y)[kOct], int lane,
         static_assert(G == 4, "2 or 4 lanes per channel");
         const int g = lane / CPW;
         const bool b1 = (g >> 1) & 1, b0 = g & 1;
-        float k[4];
+        float k[V / 2];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {  // steps (p, p+2), p = 0,1,4,5: keep p + 2*b1
+        for (int m = 0; m < V / 2; ++m) {  // steps (p, p+2), p = 4q + {0,1}: keep p + 2*b1
             const int p = (m & 1) + 4 * (m >> 1);
             const float send = b1 ? y[p] : y[p + 2];
             const float keep = b1 ? y[p + 2] : y[p];
             k[m] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * CPW);
         }
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {  // (k[2m], k[2m+1]) = steps (4m+2b1, +1): keep +b0
+        for (int m = 0; m < V / 4; ++m) {  // (k[2m], k[2m+1]) = steps (4m+2b1, +1): keep +b0
             const float send = b0 ? k[2 * m] : k[2 * m + 1];
             const float keep = b0 ? k[2 * m + 1] : k[2 * m];
             out[m] = keep + __shfl_xor_sync(0xffffffffu, send, CPW);
@@ -176,14 +178,14 @@ __device__ __forceinline__ void reduce_scatter(const float (&y)[kOct], int lane,
 // (the lane's channel row of one sDU buffer, indexed by step) for the core.  The u of those steps is returned as pairs for the D*u
 // term.  MASK: steps at or past `nsteps` get delta = 0 and no input (the
 // state passes through).
-template <typename T, int G, int TT, bool MASK, int DISC, bool GATE = false>
+template <typename T, int G, int TT, bool MASK, int DISC, bool GATE = false, int OCT = kOct>
 __device__ __forceinline__ void octet_prologue(const unsigned char* stage, int row0, int lane_x,
                                                float2* dst, float2* dst2, u64 bias2,
                                                int s0_first, int nsteps,
-                                               u64 (&uu)[kOct / G / 2],
+                                               u64 (&uu)[OCT / G / 2],
                                                u64* gz = nullptr, bool has_z = false) {
     constexpr int CPW = 32 / G;
-    constexpr int PPL = kOct / G / 2;
+    constexpr int PPL = OCT / G / 2;
     const T* sx = reinterpret_cast<const T*>(stage) + row0 * CPW + lane_x;
 #pragma unroll
     for (int p = 0; p < PPL; ++p) {
@@ -251,20 +253,21 @@ __device__ __forceinline__ void trap_seed(const ScanArgs& a, int b, int64_t d, i
         bx[i] = pk2(uq * Elem<T>::load(Br + 2 * i), uq * Elem<T>::load(Br + 2 * i + 1));
 }
 
-template <typename T, int G, int NS, int TT, int S, int DISC>
+template <typename T, int G, int NS, int TT, int S, int DISC, int OCT>
 __global__ void __launch_bounds__(32)
 scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dt,
                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
                 const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_lam,
                 const ScanArgs a, const int kgrid) {
     constexpr bool ZOH = DISC == 1, TRAP = DISC == 2;
-    using Lay = TmaLayout<T, G, NS, TT, S, TRAP>;
+    using Lay = TmaLayout<T, G, NS, TT, S, TRAP, OCT>;
+    constexpr int kDUStride = Lay::DUS;
     constexpr int kD2 = Lay::kDUsz / 8;  // second (delta) buffer, trapezoid only
     constexpr int CPW = Lay::CPW;
     constexpr int N = Lay::N;
     constexpr int NP = NS / 2;         // state pairs per lane
-    constexpr int OPT = TT / kOct;     // octets per tile
-    constexpr int SPL = kOct / G;      // steps per lane in the prologue / epilogue
+    constexpr int OPT = TT / OCT;     // octets per tile
+    constexpr int SPL = OCT / G;      // steps per lane in the prologue / epilogue
     constexpr int PPL = SPL / 2;       // ... as fp32 pairs
     extern __shared__ __align__(128) unsigned char smem[];
 
@@ -355,13 +358,13 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     // of an octet runs one octet later, beside the next octet's core, so
     // that its shuffle and store chains overlap independent work.
     u64 uz[2][PPL], gz[2][PPL];
-    float yv[2][kOct];
+    float yv[2][OCT];
 #pragma unroll
     for (int q = 0; q < 2; ++q)
 #pragma unroll
         for (int p = 0; p < PPL; ++p) uz[q][p] = gz[q][p] = pk2(0.0f, 0.0f);
     if (ok && ntiles > 0)
-        octet_prologue<T, G, TT, true, DISC, true>(smem, 0, lane_x, sDU + ch * kDUStride + g,
+        octet_prologue<T, G, TT, true, DISC, true, OCT>(smem, 0, lane_x, sDU + ch * kDUStride + g,
                                                    sDU + ch * kDUStride + g + kD2, bias2, g,
                                                    nsteps, uz[0], gz[0], has_z);
     __syncwarp();
@@ -379,7 +382,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         constexpr int Q = decltype(q_tag)::value;
         constexpr bool MASKED = decltype(masked_tag)::value;
         float ys[SPL];
-        reduce_scatter<G>(yv[Q], lane, ys);
+        reduce_scatter<G, OCT>(yv[Q], lane, ys);
 #pragma unroll
         for (int p = 0; p < PPL; ++p) {
             u64 y2 = fma2(D2, uz[Q][p], pk2(ys[2 * p], ys[2 * p + 1]));
@@ -414,13 +417,13 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         bool flushed = false;
 #pragma unroll
         for (int oo = 0; oo < OPT; ++oo) {
-            const int sb = i * TT + kOct * oo;  // chunk step of the octet's first row
+            const int sb = i * TT + OCT * oo;  // chunk step of the octet's first row
             if (!FULL && sb >= nsteps) {        // past the end of a partial tile:
                 if (oo > 0) {                   // emit the pending octet, oo - 1
                     if ((oo - 1) & 1)
-                        epilogue(P1{}, Masked{}, sb - kOct, out_p - kOct * dinner);
+                        epilogue(P1{}, Masked{}, sb - OCT, out_p - OCT * dinner);
                     else
-                        epilogue(P0{}, Masked{}, sb - kOct, out_p - kOct * dinner);
+                        epilogue(P0{}, Masked{}, sb - OCT, out_p - OCT * dinner);
                 }
                 flushed = true;
                 break;
@@ -429,10 +432,10 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             const float4* sd =
                 reinterpret_cast<const float4*>(sDU + ((oo & 1) * CPW + ch) * kDUStride);
             [[maybe_unused]] const float4* sd2 = sd + kD2 / 2;  // trapezoid: ((1-lambda)*delta, u)
-            const float* sB = sB0 + kOct * oo * N;
-            const float* sC = sC0 + kOct * oo * N;
+            const float* sB = sB0 + OCT * oo * N;
+            const float* sC = sC0 + OCT * oo * N;
 #pragma unroll
-            for (int j = 0; j < kOct; ++j) {
+            for (int j = 0; j < OCT; ++j) {
                 const float4 v2 = sd[j >> 1];  // steps j & ~1 and (j & ~1) + 1
                 const float vdl = (j & 1) ? v2.z : v2.x, vdu = (j & 1) ? v2.w : v2.y;
                 const u64 dl2 = pk2(vdl, vdl), du2 = pk2(vdu, vdu);
@@ -481,13 +484,13 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             //     tile for oo = 0, a full tile: unmasked)
             if (oo > 0) {
                 if ((oo - 1) & 1)
-                    epilogue(P1{}, std::integral_constant<bool, !FULL>{}, sb - kOct,
-                             out_p - kOct * dinner);
+                    epilogue(P1{}, std::integral_constant<bool, !FULL>{}, sb - OCT,
+                             out_p - OCT * dinner);
                 else
-                    epilogue(P0{}, std::integral_constant<bool, !FULL>{}, sb - kOct,
-                             out_p - kOct * dinner);
+                    epilogue(P0{}, std::integral_constant<bool, !FULL>{}, sb - OCT,
+                             out_p - OCT * dinner);
             } else if (i > 0) {
-                epilogue(P1{}, Unmasked{}, sb - kOct, out_p - kOct * dinner);
+                epilogue(P1{}, Unmasked{}, sb - OCT, out_p - OCT * dinner);
             }
             // (3) the next octet's step sizes, u and gate (next tile: wait
             //     for it first)
@@ -495,8 +498,8 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             u64(&un)[PPL] = uz[(oo + 1) & 1];
             u64* gn = gz[(oo + 1) & 1];
             if (oo + 1 < OPT) {
-                octet_prologue<T, G, TT, !FULL, DISC, true>(st, kOct * (oo + 1), lane_x, dnx,
-                                                            dnx + kD2, bias2, sb + kOct + g,
+                octet_prologue<T, G, TT, !FULL, DISC, true, OCT>(st, OCT * (oo + 1), lane_x, dnx,
+                                                            dnx + kD2, bias2, sb + OCT + g,
                                                             nsteps, un, gn, has_z);
             } else if (i + 1 < ntiles) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * nxt_idx,
@@ -505,22 +508,22 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 waited = i + 2;
                 const unsigned char* stn = smem + nxt_idx * Lay::kStage;
                 if ((i + 2) * TT <= nsteps)
-                    octet_prologue<T, G, TT, false, DISC, true>(stn, 0, lane_x, dnx, dnx + kD2,
-                                                                bias2, sb + kOct + g, nsteps,
+                    octet_prologue<T, G, TT, false, DISC, true, OCT>(stn, 0, lane_x, dnx, dnx + kD2,
+                                                                bias2, sb + OCT + g, nsteps,
                                                                 un, gn, has_z);
                 else
-                    octet_prologue<T, G, TT, true, DISC, true>(stn, 0, lane_x, dnx, dnx + kD2,
-                                                               bias2, sb + kOct + g, nsteps,
+                    octet_prologue<T, G, TT, true, DISC, true, OCT>(stn, 0, lane_x, dnx, dnx + kD2,
+                                                               bias2, sb + OCT + g, nsteps,
                                                                un, gn, has_z);
             }
-            out_p += kOct * dinner;
+            out_p += OCT * dinner;
             __syncwarp();
         }
         // the chunk's last octet of a full tile is still pending
         if (FULL && i + 1 == ntiles && !flushed)
-            epilogue(P1{}, Unmasked{}, i * TT + TT - kOct, out_p - kOct * dinner);
+            epilogue(P1{}, Unmasked{}, i * TT + TT - OCT, out_p - OCT * dinner);
         if (!FULL && !flushed)  // a partial tile whose octets were all run
-            epilogue(P1{}, Masked{}, i * TT + TT - kOct, out_p - kOct * dinner);
+            epilogue(P1{}, Masked{}, i * TT + TT - OCT, out_p - OCT * dinner);
         // (4) the tile is consumed: refill its stage
         if (i + S < ntiles) {
             if (lane == 0) {
@@ -1320,7 +1323,7 @@ static cudaError_t launch_tma_d(const ScanArgs& a, const ScanPlan& p, const CUte
     }
     const int64_t nb = a.batch * (int64_t)p.K * p.ntile;
     const ProfileMark m = profile_begin(s, MSC_PROF_SCAN);
-    auto kern = scan_tma_kernel<T, G, NS, TT, S, DISC>;
+    auto kern = scan_tma_kernel<T, G, NS, TT, S, DISC, kOct>;
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     kern<<<(unsigned)nb, 32, smem, s>>>(mu, mdt, mz, mB, mC, ml, a, p.K);

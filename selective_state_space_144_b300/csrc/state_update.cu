@@ -195,11 +195,11 @@ __device__ unsigned int g_update_error;
 // contiguous bytes; the four partial C.h of a channel are summed with two
 // shuffles.
 constexpr int kStreamCh = 128;
-constexpr int kStreamStages = 6;
-constexpr int kStreamAhead = 4;   // tiles loading while one is updated and one stored
 constexpr int kStreamThreads = 128;
 
-template <typename T>
+// SS stages; the tile AHEAD steps ahead is loaded while one is updated and
+// the store of an earlier one (SS - AHEAD stages) may still read its stage.
+template <typename T, int SS>
 struct StreamLayout {
     static constexpr int N = 16;
     static constexpr int kState = kStreamCh * N * 4;                    // 8192
@@ -208,14 +208,17 @@ struct StreamLayout {
     static constexpr int kU = kState, kDt = kU + kX, kZ = kDt + kX;
     static constexpr int kB = kZ + kX, kC = kB + ((kBC + 15) / 16) * 16;
     static constexpr int kStage = ((kC + kBC + 127) / 128) * 128;
-    static constexpr int kBar = kStreamStages * kStage;
-    static constexpr int kTotal = kBar + kStreamStages * 8;
+    static constexpr int kBar = SS * kStage;
+    static constexpr int kTotal = kBar + SS * 8;
 };
 
-template <typename T>
+template <typename T, int SS, int AHEAD>
 __global__ void __launch_bounds__(kStreamThreads)
 state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
-    using Lay = StreamLayout<T>;
+    static_assert(AHEAD >= 1 && AHEAD <= SS - 2, "a stage for the update and one for a store");
+    constexpr int kStreamStages = SS;
+    constexpr int kStreamAhead = AHEAD;
+    using Lay = StreamLayout<T, SS>;
     constexpr int N = Lay::N;
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x;
@@ -278,7 +281,7 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
         // refill: tile t + Ahead goes into the stage tile t + Ahead - S used;
         // its state store (committed two iterations ago) must have read it
         if (tid == 0 && t + kStreamAhead < nt) {
-            bulk_wait_read<1>();
+            bulk_wait_read<SS - AHEAD - 1>();
             issue(t + kStreamAhead);
             issued = t + kStreamAhead + 1;
         }
@@ -348,26 +351,36 @@ bool stream_update_supported(const UpdateArgs& a, size_t es) {
            (!a.z || al16(a.z));
 }
 
-template <typename T>
-static cudaError_t launch_stream(const UpdateArgs& a, int sms, cudaStream_t s) {
-    using Lay = StreamLayout<T>;
+template <typename T, int SS, int AHEAD>
+static cudaError_t launch_stream_s(const UpdateArgs& a, int ctas_per_sm, cudaStream_t s) {
+    using Lay = StreamLayout<T, SS>;
     const int nJ = (int)((a.d_inner + kStreamCh - 1) / kStreamCh);
-    const int64_t target = (int64_t)sms * 3;  // 3 CTAs per SM (48+ KB of stages each)
+    const int64_t target = (int64_t)a.sms * ctas_per_sm;
     int64_t R = target / nJ;
     R = R < 1 ? 1 : (R > a.batch ? a.batch : R);
     const int64_t grid = (int64_t)nJ * R;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-    auto kern = state_update_stream_kernel<T>;
+    auto kern = state_update_stream_kernel<T, SS, AHEAD>;
     if (Lay::kTotal > 48 * 1024)
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kTotal);
     kern<<<(unsigned)grid, kStreamThreads, Lay::kTotal, s>>>(a, nJ, (int)R, a.wait_limit);
     return cudaGetLastError();
 }
 
+template <typename T>
+static cudaError_t launch_stream(const UpdateArgs& a, cudaStream_t s) {
+    switch (a.stream_cfg) {
+        case 1: return launch_stream_s<T, 4, 2>(a, 6, s);
+        case 2: return launch_stream_s<T, 3, 1>(a, 8, s);
+        case 3: return launch_stream_s<T, 5, 3>(a, 4, s);
+        default: return launch_stream_s<T, 6, 4>(a, 3, s);
+    }
+}
+
 template <typename T, bool VEC>
 static cudaError_t launch_update_v(const UpdateArgs& a, cudaStream_t s) {
     if (a.stream_ok && stream_update_supported(a, sizeof(T)))
-        return launch_stream<T>(a, a.sms, s);
+        return launch_stream<T>(a, s);
     if (VEC && a.batch <= 65535 && (a.N == 8 || a.N == 16 || a.N == 32) &&
         reinterpret_cast<uintptr_t>(a.A) % 16 == 0) {
         const dim3 grid((unsigned)((a.d_inner + 127) / 128), (unsigned)a.batch);
