@@ -359,6 +359,15 @@ def run_ours(args):
     pk.msc_peak_scan_core(sink.data_ptr(), sms * 4, 128, 500, stream, ctypes.byref(msf))
     pk.msc_peak_scan_core(sink.data_ptr(), sms * 4, 128, core_iters, stream, ctypes.byref(msf))
     core_peak = sms * 4 * 128 * core_iters * 32 / (msf.value * 1e-3)     # updates/s
+    # MUFU with 0 and 4 packed FMAs per pair of ex2: how far the pipes overlap
+    pk.msc_peak_mufu_fma.restype = ctypes.c_int
+    pk.msc_peak_mufu_fma.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                                     ctypes.POINTER(ctypes.c_float)]
+    mix = {}
+    for k2 in (0, 4):
+        pk.msc_peak_mufu_fma(sink.data_ptr(), sms * 4, 128, 20000, k2, stream, ctypes.byref(msf))
+        mix[k2] = sms * 4 * 128 * 20000 * 8 / (msf.value * 1e-3)       # ex2/s
     # streaming copy of 1 GiB (read + write bytes), the HBM figure of this run
     cp_src = torch.empty(2**28, dtype=torch.float32, device=dev)
     cp_dst = torch.empty_like(cp_src)
@@ -486,6 +495,13 @@ def run_ours(args):
                          "fma.f32x2, fma.f32x2 per state pair) run from registers with no "
                          "memory traffic at 16 warps per SM: the rate MUFU and the FMA pipe "
                          "reach together, the ceiling of the update core"),
+            },
+            "mufu_fma_overlap": {
+                "ex2_per_s_alone": mix[0],
+                "ex2_per_s_with_4_ffma2_per_2_ex2": mix[4],
+                "what": ("ex2 throughput with only its operand arithmetic, and with four "
+                         "packed FMAs per pair of ex2 (the update core's ratio); equal rates "
+                         "would mean the FMA work hides under MUFU"),
             },
             "copy_gbs_this_run": copy_gbs,
             "issue": issue,
@@ -684,11 +700,57 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
     c_cold = hook_cold_ms(cstep, "conv")
     c_b2b = back_to_back_ms(cstep, 200)
     c_bytes = 2 * Bc * Lc * Dc * 2 + Dc * Kc * 4 + Dc * 4 + Bc * Dc * (Kc - 1) * 2
+
+    # device time per launch without launch latency: 30 launches in a CUDA
+    # graph cycling over 3 input / output sets (300 MB, more than L2)
+    def conv_graph_us(nset=3, reps=30):
+        xs = [xc] + [xc.clone() for _ in range(nset - 1)]
+        outs_ = [torch.empty_like(xc) for _ in range(nset)]
+        sts = [torch.empty_like(sc) for _ in range(nset)]
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for k in range(nset):
+                msc.causal_conv1d_fwd(xs[k], wc, bc, out=outs_[k], state_out=sts[k])
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for k in range(reps):
+                msc.causal_conv1d_fwd(xs[k % nset], wc, bc, out=outs_[k % nset],
+                                      state_out=sts[k % nset])
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(5):
+            flush()
+            torch.cuda.synchronize(dev)
+            g0 = torch.cuda.Event(enable_timing=True)
+            g1 = torch.cuda.Event(enable_timing=True)
+            g0.record()
+            graph.replay()
+            g1.record()
+            g1.synchronize()
+            ts.append(g0.elapsed_time(g1) * 1e3 / reps)
+        del xs, outs_, sts
+        return statistics.median(ts)
+
+    try:
+        c_graph = conv_graph_us()
+    except RuntimeError as exc:  # capture unavailable: report the others
+        print(f"conv prefill graph timing skipped: {exc}", file=sys.stderr)
+        c_graph = None
     res["conv1d_prefill_8x2048x1536_k4"] = {
         "shape": [Bc, Lc, Dc, Kc], "us_l2_flushed": c_cold * 1e3, "us_back_to_back": c_b2b * 1e3,
+        "us_graph_streamed": c_graph,
         "algorithmic_bytes": c_bytes,
         "hbm_frac_l2_flushed": (c_bytes / (c_cold * 1e-3)) / (peaks["hbm_gbs"] * 1e9),
-        "note": "x read and u written once (50 MB each); back to back, part of x stays in L2",
+        "hbm_frac_graph_streamed": (None if c_graph is None else
+                                    (c_bytes / (c_graph * 1e-6)) / (peaks["hbm_gbs"] * 1e9)),
+        "note": ("x read and u written once (50 MB each); a single launch after an L2 flush "
+                 "includes the launch latency (a few us of a ~25 us kernel); the graph replay "
+                 "streams 3 sets of 100 MB back to back; back to back on one set, part of x "
+                 "stays in L2"),
     }
     del xc, oc
     Bu, Du = 256, 5120

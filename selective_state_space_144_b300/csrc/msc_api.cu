@@ -424,8 +424,7 @@ static msc_status run_update(float* state, const void* u, const void* dt, const 
     a.vec = (d_state % 4 == 0) && aligned(state, 16) && aligned(B, 4 * es) && aligned(C, 4 * es);
     a.zoh = zoh;
     a.trap = lam != nullptr; a.lam = lam; a.u_prev = u_prev; a.B_prev = B_prev;
-    a.stream_ok = g_update_path == 0 || g_update_path >= 2;
-    a.stream_cfg = g_update_path >= 2 ? (int)(g_update_path - 1) : 0;
+    a.stream_ok = g_update_path == 0;
     a.sms = sm_count();
     a.wait_limit = msc::kWaitLimit;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -598,7 +597,7 @@ msc_status msc_tuning_set(const char* key, int64_t value) {
         return MSC_OK;
     }
     if (std::strcmp(key, "update_path") == 0) {
-        if (value > 4) return MSC_ERR_INVALID_ARG;
+        if (value > 1) return MSC_ERR_INVALID_ARG;
         g_update_path = value;
         return MSC_OK;
     }

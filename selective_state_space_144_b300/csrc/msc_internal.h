@@ -2,6 +2,7 @@
 // (msc_api.cu) and the kernel files.  Not installed, not part of the ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -71,7 +72,6 @@ struct UpdateArgs {
     const void* u_prev;  // previous token's u (batch, d_inner) or nullptr
     const void* B_prev;  // previous token's B (batch, N) or nullptr
     int stream_ok;       // 1: the copy-engine streaming kernel may be used
-    int stream_cfg;      // its ring depth / CTAs per SM choice
     int sms;             // multiprocessor count of the device
     uint32_t wait_limit; // polls before a bounded wait gives up
 };
@@ -160,6 +160,11 @@ ScanPlan make_tma_plan(int64_t batch, int64_t L, int64_t d_inner, int64_t N, int
 cudaError_t launch_carry_prefix(const ScanArgs& a, cudaStream_t s);
 cudaError_t launch_scan(const ScanArgs& a, const ScanPlan& p, msc_dtype dtype,
                         cudaStream_t stream);
+
+// Tiled tensor map of a row-major (batch, L, cols) array, box [box0 cols,
+// box1 rows, 1] (scan_tma.cu); false when the driver refuses it.
+bool make_tensor_map_3d(CUtensorMap* m, CUtensorMapDataType t, int es, const void* base,
+                        int64_t cols, int64_t L, int64_t batch, int box0, int box1);
 
 // TMA path (scan_tma.cu): supported shapes, time-tile length, launch, and
 // the device word its bounded waits set when a copy never lands.

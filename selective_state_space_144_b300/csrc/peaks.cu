@@ -138,6 +138,35 @@ __global__ void k_scan_core(float* sink, int64_t iters) {
     if (acc == 1234.5f) sink[0] = acc;
 }
 
+// MUFU and the FMA pipe together: per iteration and thread 8 independent
+// ex2 and K2 packed fma.rn.f32x2 per pair of ex2 (K2 = 0 gives the ex2 rate
+// with its operand arithmetic alone, K2 = 4 the scan core's ratio), so the
+// caller can see how far the two pipes overlap.
+template <int K2>
+__global__ void k_mufu_fma(float* sink, int64_t iters) {
+    float e[8];
+    unsigned long long f[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        e[i] = -0.1f * (i + 1) - 1e-7f * threadIdx.x;
+        f[i] = pk2(0.5f + 0.01f * i, 0.3f);
+    }
+    const unsigned long long a = pk2(0.9999f, 0.9998f), b = pk2(1e-4f, 2e-4f);
+    for (int64_t it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            e[i] = ex2_f(-e[i] * 0.5f - 0.01f);
+            e[i + 1] = ex2_f(-e[i + 1] * 0.5f - 0.01f);
+#pragma unroll
+            for (int k = 0; k < K2; ++k) f[(i + k) & 7] = fma2(f[(i + k) & 7], a, b);
+        }
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += e[i] + lo2(f[i]) + hi2(f[i]);
+    if (s == 1234.5f) sink[0] = s;
+}
+
 __global__ void k_copy(float4* __restrict__ dst, const float4* __restrict__ src, int64_t n) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
@@ -191,6 +220,15 @@ int msc_peak_ffma2(float* sink, int blocks, int threads, int64_t iters, cudaStre
 int msc_peak_scan_core(float* sink, int blocks, int threads, int64_t iters, cudaStream_t s,
                        float* ms) {
     return timed(s, ms, [&] { k_scan_core<<<blocks, threads, 0, s>>>(sink, iters); });
+}
+
+// ex2 operations = blocks * threads * iters * 8, with k2 (0, 2 or 4) packed
+// FMAs per pair of them.
+int msc_peak_mufu_fma(float* sink, int blocks, int threads, int64_t iters, int k2,
+                      cudaStream_t s, float* ms) {
+    if (k2 == 4) return timed(s, ms, [&] { k_mufu_fma<4><<<blocks, threads, 0, s>>>(sink, iters); });
+    if (k2 == 2) return timed(s, ms, [&] { k_mufu_fma<2><<<blocks, threads, 0, s>>>(sink, iters); });
+    return timed(s, ms, [&] { k_mufu_fma<0><<<blocks, threads, 0, s>>>(sink, iters); });
 }
 
 // bytes moved = 2 * n16 * 16 (read + write); n16 = number of 16-byte words.

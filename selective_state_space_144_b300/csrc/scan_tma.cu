@@ -1114,13 +1114,12 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
                     const u64 ea = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
                     dh[i] = fma2(Cq[i], dy2, dh[i]);
                     dC[i] = mul2(dy2, ht[i]);
-                    const u64 dae = mul2(mul2(dh[i], hp[i]), ea);
+                    sp = fma2(dh[i], Bq[i], sp);
+                    dB[i] = mul2(dh[i], du2);
+                    dh[i] = mul2(dh[i], ea);              // the adjoint carried to step j-1
+                    const u64 dae = mul2(dh[i], hp[i]);   // dh * e^{delta A} * h_{j-1}
                     dAacc[i] = fma2(dae, dl2, dAacc[i]);
                     ddp = fma2(dae, An[i], ddp);
-                    const u64 dhB = mul2(dh[i], Bq[i]);
-                    sp = add2(sp, dhB);
-                    dB[i] = mul2(dh[i], du2);
-                    dh[i] = mul2(dh[i], ea);
                 }
                 const float ssum = lo2(sp) + hi2(sp);
                 const float yp = lo2(y2) + hi2(y2);
@@ -1279,8 +1278,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 3-D map over a (batch, L, cols) row-major array, box [box0 cols, box1 steps, 1].
-static bool make_map(CUtensorMap* m, CUtensorMapDataType t, int es, const void* base,
-                     int64_t cols, int64_t L, int64_t batch, int box0, int box1) {
+bool make_tensor_map_3d(CUtensorMap* m, CUtensorMapDataType t, int es, const void* base,
+                        int64_t cols, int64_t L, int64_t batch, int box0, int box1) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)L, (cuuint64_t)batch};
@@ -1340,12 +1339,12 @@ static cudaError_t launch_tma_ns(const ScanArgs& a, const ScanPlan& p, const flo
         sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const int es = (int)sizeof(T);
     CUtensorMap mu, mdt, mz, mB, mC, ml;
-    if (!make_map(&mu, tt, es, a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
-        !make_map(&mdt, tt, es, a.dt, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
-        !make_map(&mz, tt, es, a.z ? a.z : a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
-        !make_map(&ml, tt, es, a.trap ? a.lam : a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
-        !make_map(&mB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Bf, a.N, a.L, a.batch, (int)a.N, TT) ||
-        !make_map(&mC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Cf, a.N, a.L, a.batch, (int)a.N, TT))
+    if (!make_tensor_map_3d(&mu, tt, es, a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_tensor_map_3d(&mdt, tt, es, a.dt, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_tensor_map_3d(&mz, tt, es, a.z ? a.z : a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_tensor_map_3d(&ml, tt, es, a.trap ? a.lam : a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_tensor_map_3d(&mB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Bf, a.N, a.L, a.batch, (int)a.N, TT) ||
+        !make_tensor_map_3d(&mC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Cf, a.N, a.L, a.batch, (int)a.N, TT))
         return cudaErrorInvalidValue;
     if (a.trap) return launch_tma_d<T, G, NS, TT, S, 2>(a, p, mu, mdt, mz, mB, mC, ml, s);
     if (a.zoh) return launch_tma_d<T, G, NS, TT, S, 1>(a, p, mu, mdt, mz, mB, mC, ml, s);
@@ -1423,12 +1422,12 @@ static cudaError_t launch_bwd_tma_n(const BwdArgs& a, const float* Bf, const flo
         sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const int es = (int)sizeof(T);
     CUtensorMap mu, mdt, mz, mg, mB, mC;
-    if (!make_map(&mu, tt, es, a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
-        !make_map(&mdt, tt, es, a.dt, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
-        !make_map(&mz, tt, es, a.z ? a.z : a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
-        !make_map(&mg, tt, es, a.dout, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
-        !make_map(&mB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Bf, a.N, a.L, a.batch, (int)a.N, TT) ||
-        !make_map(&mC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Cf, a.N, a.L, a.batch, (int)a.N, TT))
+    if (!make_tensor_map_3d(&mu, tt, es, a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_tensor_map_3d(&mdt, tt, es, a.dt, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_tensor_map_3d(&mz, tt, es, a.z ? a.z : a.u, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_tensor_map_3d(&mg, tt, es, a.dout, a.d_inner, a.L, a.batch, Lay::CPW, TT) ||
+        !make_tensor_map_3d(&mB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Bf, a.N, a.L, a.batch, (int)a.N, TT) ||
+        !make_tensor_map_3d(&mC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Cf, a.N, a.L, a.batch, (int)a.N, TT))
         return cudaErrorInvalidValue;
     auto kern = scan_bwd_tma_kernel<T, NS, TT, S>;
     const size_t smem = Lay::kTotal;

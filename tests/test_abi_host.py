@@ -133,6 +133,10 @@ def test_tuning_keys(lib):
     assert lib.msc_tuning_set(b"debug_starve_copies", -1) == 1
     assert lib.msc_tuning_set(b"debug_starve_copies", (1 << 22) + 1) == 1
     assert lib.msc_tuning_set(b"debug_starve_copies", 0) == 0
+    for key in (b"update_path",):
+        assert lib.msc_tuning_set(key, 2) == 1
+        assert lib.msc_tuning_set(key, 1) == 0
+        assert lib.msc_tuning_set(key, 0) == 0
 
 
 def upd(lib, *, state=FAKE, u=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None,
