@@ -357,12 +357,13 @@ msc_status msc_scratch_release(void);
  *                   kernel where sizes and alignment allow), 1 = the
  *                   thread-per-channel decode kernels only
  *   "debug_starve_copies"  failure-detection test, 0 (default) = off; n > 0:
- *                   the forward scan's TMA kernels issue none of their data
- *                   copies and give up each wait after n polls, so every
- *                   such launch ends through the bounded-wait exit (device
- *                   word set, msc_check_device_error -> MSC_ERR_TIMEOUT,
- *                   outputs not written).  No copy is in flight when the
- *                   kernel returns and nothing faults.
+ *                   the forward scan's TMA kernels and the streaming decode
+ *                   kernel issue none of their data copies and give up each
+ *                   wait after n polls, so every such launch ends through the
+ *                   bounded-wait exit (device word set, msc_check_device_error
+ *                   -> MSC_ERR_TIMEOUT, outputs and state not written).  No
+ *                   copy is in flight when the kernel returns and nothing
+ *                   faults.
  * Process-wide and not thread-safe; returns MSC_ERR_INVALID_ARG for an
  * unknown key or a negative value.
  */

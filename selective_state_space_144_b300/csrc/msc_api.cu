@@ -426,7 +426,8 @@ static msc_status run_update(float* state, const void* u, const void* dt, const 
     a.trap = lam != nullptr; a.lam = lam; a.u_prev = u_prev; a.B_prev = B_prev;
     a.stream_ok = g_update_path == 0;
     a.sms = sm_count();
-    a.wait_limit = msc::kWaitLimit;
+    a.wait_limit = g_starve > 0 ? (uint32_t)g_starve : msc::kWaitLimit;
+    a.starve = g_starve > 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     msc::ProfileMark m = msc::profile_begin(s, MSC_PROF_UPDATE);
     cudaError_t e = msc::launch_state_update(a, dtype, s);

@@ -74,6 +74,7 @@ struct UpdateArgs {
     int stream_ok;       // 1: the copy-engine streaming kernel may be used
     int sms;             // multiprocessor count of the device
     uint32_t wait_limit; // polls before a bounded wait gives up
+    int starve;          // failure-detection test: 1 = the streaming kernel issues no copies
 };
 
 // The causal depthwise conv1d before the scan (conv1d.cu).  For the decode

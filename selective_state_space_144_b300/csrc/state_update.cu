@@ -256,7 +256,7 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
     };
     int issued = 0;
     if (tid == 0) {
-        issued = min(kStreamAhead, nt);
+        issued = a.starve ? 0 : min(kStreamAhead, nt);
         for (int t = 0; t < issued; ++t) issue(t);
     }
 
@@ -281,7 +281,7 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
         const int st = t % kStreamStages;
         // refill: tile t + Ahead goes into the stage tile t + Ahead - S used;
         // its state store (committed two iterations ago) must have read it
-        if (tid == 0 && t + kStreamAhead < nt) {
+        if (tid == 0 && t + kStreamAhead < nt && !a.starve) {
             bulk_wait_read<SS - AHEAD - 1>();
             issue(t + kStreamAhead);
             issued = t + kStreamAhead + 1;

@@ -126,3 +126,43 @@ def test_decode_general_kernel_with_unaligned_A():
                                              p.D, s.z, p.dt_bias)
     assert rel_l2(from_device(out), ref_out) <= TOL["f32"]
     assert rel_l2(from_device(state), ref_state) <= TOL["f32"]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("batch,d_inner", [(1, 8), (3, 136), (5, 1000), (7, 264), (40, 640)])
+def test_decode_stream_kernel_shapes(dtype, batch, d_inner):
+    """d_state 16 with aligned arrays takes the copy-engine streaming kernel:
+    partial 128-channel tiles, batch rows spread over CTAs, fp32 and bf16
+    storage.  Four steps against the oracle, and the state bit for bit
+    against the thread-per-channel kernel (the same operations per state)."""
+    N, steps = 16, 4
+    p = synth.decode_params(batch, d_inner, N, seed=60 + d_inner, dtype=dtype)
+    A, D, bias = to_device(p.A, "f32"), to_device(p.D, "f32"), to_device(p.dt_bias, "f32")
+    states = {}
+    outs = {}
+    try:
+        for path in (0, 1):
+            msc.tuning_set("update_path", path)
+            state = torch.from_numpy(p.state0).cuda()
+            ref_state = p.state0.astype(np.float64)
+            worst = 0.0
+            for k in range(steps):
+                s = synth.decode_step(batch, d_inner, N, k, seed=60 + d_inner, dtype=dtype)
+                dv = _step_dev(s, dtype)
+                out = torch.full((batch, d_inner), float("nan"), dtype=dv["u"].dtype,
+                                 device="cuda")
+                msc.selective_state_update(state, dv["u"], dv["dt"], A, dv["B"], dv["C"], D,
+                                           dv["z"], bias, out=out)
+                ref_state, ref_out = oracle.state_update(ref_state, s.u, s.dt_raw, p.A, s.B,
+                                                         s.C, p.D, s.z, p.dt_bias)
+                got = from_device(out)
+                assert np.all(np.isfinite(got))
+                worst = max(worst, rel_l2(got, as_stored(ref_out, dtype)))
+            torch.cuda.synchronize()
+            assert worst <= TOL[dtype], (path, worst)
+            assert rel_l2(from_device(state), ref_state) <= TOL[dtype]
+            states[path] = state.cpu()
+            outs[path] = out.float().cpu()
+    finally:
+        msc.tuning_set("update_path", 0)
+    assert torch.equal(states[0], states[1])

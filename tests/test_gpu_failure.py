@@ -15,7 +15,7 @@ import pytest
 import oracle
 import selective_state_space_144_b300 as msc
 from selective_state_space_144_b300 import synth
-from tests.helpers import TOL, as_stored, from_device, rel_l2, scan_device_args
+from tests.helpers import TOL, as_stored, from_device, rel_l2, scan_device_args, to_device
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -77,3 +77,37 @@ def test_starved_waits_report_timeout_and_context_survives(chunks):
     assert np.all(np.isfinite(got))
     assert rel_l2(got, as_stored(y_ref, "bf16")) <= TOL["bf16"]
     assert rel_l2(from_device(last), s_ref) <= TOL["bf16"]
+
+
+def test_starved_decode_reports_timeout_and_context_survives():
+    """The streaming decode kernel (d_state 16, aligned arrays): its waits run
+    out with no copy issued; the state is left untouched; a normal step
+    afterwards matches the oracle."""
+    batch, d_inner, N = 2, 256, 16
+    p = synth.decode_params(batch, d_inner, N)
+    s = synth.decode_step(batch, d_inner, N, 0)
+    lib = msc.load()
+    dev = {k: to_device(getattr(s, k), "bf16") for k in ("u", "dt_raw", "z", "B", "C")}
+    A, D, bias = (to_device(p.A, "f32"), to_device(p.D, "f32"), to_device(p.dt_bias, "f32"))
+    state = torch.from_numpy(p.state0).cuda()
+    out = torch.full((batch, d_inner), float("nan"), dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        msc.selective_state_update(state, dev["u"], dev["dt_raw"], A, dev["B"], dev["C"],
+                                   D, dev["z"], bias, out=out)
+        torch.cuda.synchronize()
+
+    msc.tuning_set("debug_starve_copies", 64)
+    step()
+    assert lib.msc_check_device_error(1) == MSC_ERR_TIMEOUT
+    assert lib.msc_check_device_error(0) == 0
+    assert torch.isnan(out.float()).all()
+    assert torch.equal(state.cpu(), torch.from_numpy(p.state0))
+
+    msc.tuning_set("debug_starve_copies", 0)
+    step()
+    assert lib.msc_check_device_error(0) == 0
+    ref_state, ref_out = oracle.state_update(p.state0, s.u, s.dt_raw, p.A, s.B, s.C, p.D,
+                                             s.z, p.dt_bias)
+    assert rel_l2(from_device(out), as_stored(ref_out, "bf16")) <= TOL["bf16"]
+    assert rel_l2(from_device(state), ref_state) <= TOL["bf16"]
