@@ -67,7 +67,8 @@ def parse():
                     help="profiling driver: run only the scan (or, for "
                          "decode_256x5120, the decode step; for conv1d_prefill "
                          "/ conv1d_update, the conv; for scan_bwd, the backward "
-                         "pass on the 130M layer) on WORKLOAD "
+                         "pass on the 130M layer; for scan_bwd_ckpt, the backward "
+                         "from forward-written checkpoints) on WORKLOAD "
                          "--warmup + --steps times, print nothing else "
                          "(for ncu; see profiles/)")
     return ap.parse_args()
@@ -826,27 +827,30 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
         xb.u.shape).astype(np.float32)), "bf16")
     Bb_, Lb_, Db_, Nb_ = xb.u.shape + (xb.B.shape[-1],)
     del xb
-    bstep = lambda k: msc.selective_scan_bwd(**ab, dout=gout)
-    for k in range(2):
-        bstep(k)
-    tb, kb = [], []
-    for _ in range(5):
-        flush()
-        torch.cuda.synchronize(dev)
-        msc.profile_read()
-        msc.profile_enable(True)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        bstep(0)
-        e1.record()
-        e1.synchronize()
-        msc.profile_enable(False)
-        _, kinds = msc.profile_read()
-        kb.append(kinds["scan_bwd"][1])
-        tb.append(e0.elapsed_time(e1))
+    def call_ms(fn, kind, reps=5):
+        """Median (whole-call ms, main-kernel ms) over reps calls, L2 flushed."""
+        for _ in range(2):
+            fn()
+        tb, kb = [], []
+        for _ in range(reps):
+            flush()
+            torch.cuda.synchronize(dev)
+            msc.profile_read()
+            msc.profile_enable(True)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            msc.profile_enable(False)
+            _, kinds = msc.profile_read()
+            kb.append(kinds[kind][1])
+            tb.append(e0.elapsed_time(e1))
+        return statistics.median(tb), statistics.median(kb)
+
     updb = Bb_ * Lb_ * Db_ * Nb_
-    bms, bkms = statistics.median(tb), statistics.median(kb)
+    bms, bkms = call_ms(lambda: msc.selective_scan_bwd(**ab, dout=gout), "scan_bwd")
     # algorithmic work of a recompute backward: the forward exponential again
     # and the adjoint's, 2 ex2 per update, plus softplus, sigmoid(dt), sigmoid(z)
     # per (step, channel); HBM: u, dt, z, dout read, du, ddt, dz written (2 B
@@ -860,7 +864,30 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
         "hbm_frac": (b_bytes / (bms * 1e-3)) / (peaks["hbm_gbs"] * 1e9),
         "timing": "whole call (memsets, checkpoint and adjoint kernels, stream-ordered scratch)",
     }
-    del ab, gout
+    # training with forward-written checkpoints: the forward also stores the
+    # state entering every 16 steps, the backward reads them and skips its
+    # own forward re-walk (one of its three exponentials per update)
+    _, ck_bytes = msc.scan_checkpoint_size(Bb_, Lb_, Db_, Nb_)
+    ck = torch.empty(ck_bytes // 4, dtype=torch.float32, device=dev).view(
+        Bb_, -1, Db_, Nb_)
+    fo = torch.empty(Bb_, Lb_, Db_, dtype=torch.bfloat16, device=dev)
+    fl = torch.empty(Bb_, Db_, Nb_, dtype=torch.float32, device=dev)
+    f_ms, f_kms = call_ms(lambda: msc.selective_scan_fwd(**ab, out=fo, last_state=fl), "scan")
+    fc_ms, fc_kms = call_ms(lambda: msc.selective_scan_fwd_ckpt(
+        **ab, out=fo, last_state=fl, ckpt=ck), "scan")
+    bc_ms, bc_kms = call_ms(lambda: msc.selective_scan_bwd(**ab, dout=gout, ckpt=ck),
+                            "scan_bwd")
+    res["scan_train_ckpt_mamba130m_layer"] = {
+        "shape": [Bb_, Lb_, Db_, Nb_], "checkpoint_bytes": ck_bytes,
+        "fwd_ms": f_ms, "fwd_kernel_ms": f_kms,
+        "fwd_ckpt_ms": fc_ms, "fwd_ckpt_kernel_ms": fc_kms,
+        "bwd_recompute_ms": bms, "bwd_from_ckpt_ms": bc_ms, "bwd_from_ckpt_kernel_ms": bc_kms,
+        "fwd_plus_bwd_recompute_ms": f_ms + bms, "fwd_ckpt_plus_bwd_ms": fc_ms + bc_ms,
+        "bwd_from_ckpt_mufu_frac": (b_mufu / (bc_ms * 1e-3)) / ex2_peak,
+        "timing": "whole calls, L2 flushed before each; kernel ms from the library's "
+                  "event pair around its main kernel",
+    }
+    del ab, gout, ck, fo, fl
     torch.cuda.empty_cache()
 
     # (workload, discretisation): the other two scan workloads, and the
@@ -979,8 +1006,10 @@ def run_profile(args):
             return torch.from_numpy(bits.copy()).to(dev).view(torch.bfloat16)
         return torch.from_numpy(np.ascontiguousarray(arr, np.float32)).to(dev)
 
-    if name == "scan_bwd":
-        # backward pass of the scan on the 8 x 2048 x 1536 x 16 layer, bf16
+    if name in ("scan_bwd", "scan_bwd_ckpt"):
+        # backward pass of the scan on the 8 x 2048 x 1536 x 16 layer, bf16;
+        # scan_bwd_ckpt: the checkpointing forward once, then the backward
+        # from its checkpoints
         x = synth.workload_inputs("mamba130m_layer")
         a = dict(u=dev_t(x.u, "bf16"), dt=dev_t(x.dt_raw, "bf16"), A=dev_t(x.A, "f32"),
                  B=dev_t(x.B, "bf16"), C=dev_t(x.C, "bf16"), D=dev_t(x.D, "f32"),
@@ -988,8 +1017,9 @@ def run_profile(args):
         gout = dev_t(synth.round_bf16(np.random.default_rng(14).standard_normal(
             x.u.shape).astype(np.float32)), "bf16")
         del x
+        ck = msc.selective_scan_fwd_ckpt(**a)[2] if name == "scan_bwd_ckpt" else None
         for _ in range(args.warmup + args.steps):
-            msc.selective_scan_bwd(**a, dout=gout)
+            msc.selective_scan_bwd(**a, dout=gout, ckpt=ck)
         torch.cuda.synchronize(dev)
         msc.check_device_error()
         print(f"profile run done: {name}, {args.warmup + args.steps} calls", flush=True)

@@ -259,6 +259,68 @@ msc_status msc_selective_scan_fwd_ex(
     msc_stream_t stream);
 
 /*
+ * Training without the backward's re-walk.  msc_selective_scan_bwd recomputes
+ * the states at the start of every tile of its own by walking the sequence
+ * forward again (one exponential per state update, about a fifth of its
+ * work).  A forward scan that is followed by a backward can write those
+ * states as it goes -- the pages' "save the states at chunk boundaries,
+ * recompute inside the chunk" scheme ("Deep dive into Mamba", section 7.3) --
+ * and the backward then starts at once from the last tile.
+ *
+ * msc_scan_checkpoint_size: the interval (steps between checkpoints: 16 for
+ * d_state 8 and 16, 8 for 32 and 64) and the bytes of the checkpoint array,
+ *     (batch, rows, d_inner, d_state) fp32, rows = ceil(L / interval),
+ * row k = the state entering step k * interval (row 0 = h0, or zero).
+ * d_state other than 8, 16, 32, 64 is MSC_ERR_UNSUPPORTED; negative sizes
+ * MSC_ERR_INVALID_ARG; sizes whose byte count overflows MSC_ERR_UNSUPPORTED.
+ */
+msc_status msc_scan_checkpoint_size(int64_t batch, int64_t L, int64_t d_inner,
+                                    int64_t d_state, int64_t* interval,
+                                    size_t* bytes);
+
+/*
+ * msc_selective_scan_fwd_ex (Euler form, optional h0) that also writes the
+ * checkpoint array `ckpt` (caller-owned device memory, 16-byte aligned,
+ * msc_scan_checkpoint_size bytes; every row is written).  Other arguments,
+ * the workspace and the results as msc_selective_scan_fwd_ex: out and
+ * last_state are bit-identical to that call's.  The checkpoints are written
+ * by the TMA-staged kernel only: d_state 8, 16, 32 or 64, d_inner a multiple
+ * of 8, u, dt, z 16-byte aligned; other shapes are MSC_ERR_UNSUPPORTED (use
+ * msc_selective_scan_bwd, which recomputes them).  ckpt NULL with work to do:
+ * MSC_ERR_INVALID_ARG.
+ */
+msc_status msc_selective_scan_fwd_ckpt(
+    const void* u, const void* dt, const float* A, const void* B,
+    const void* C, const float* D, const void* z, const float* dt_bias,
+    const float* h0, void* out, float* last_state, float* ckpt, int64_t batch,
+    int64_t L, int64_t d_inner, int64_t d_state, msc_dtype dtype,
+    void* workspace, size_t workspace_bytes, msc_stream_t stream);
+
+/*
+ * msc_selective_scan_bwd reading the checkpoints `ckpt` that
+ * msc_selective_scan_fwd_ckpt wrote for the same inputs (and h0) instead of
+ * recomputing them; nothing of ckpt is written.  Arguments, results and
+ * errors as msc_selective_scan_bwd, plus: the TMA backward is required
+ * (d_state 8, 16, 32, 64, d_inner a multiple of 8, u, dt, z, dout, dB, dC
+ * 16-byte aligned), else MSC_ERR_UNSUPPORTED; ckpt 16-byte aligned, else
+ * MSC_ERR_ALIGNMENT; NULL with work to do, MSC_ERR_INVALID_ARG.  When the
+ * forward ran in one time chunk, its checkpoints are the states the backward
+ * would recompute, bit for bit, and du, ddt, dz, dh0 equal
+ * msc_selective_scan_bwd's bit for bit (the atomically summed gradients up to
+ * the order of their adds); when it split time into chunks (long sequences
+ * over few channels), the rows at chunk starts carry the chunked scan's
+ * rounding.  Scratch: only the fp32 copies of B and C for bf16 storage (or
+ * unaligned fp32).
+ */
+msc_status msc_selective_scan_bwd_ckpt(
+    const void* u, const void* dt, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* dt_bias, const float* h0,
+    const float* ckpt, const void* dout, const float* dlast_state, void* du,
+    void* ddt, float* dA, float* dB, float* dC, float* dD, void* dz,
+    float* ddt_bias, float* dh0, int64_t batch, int64_t L, int64_t d_inner,
+    int64_t d_state, msc_dtype dtype, msc_stream_t stream);
+
+/*
  * The Mamba-3 exponential-trapezoid scan ("State space models and the Mamba
  * series", section 2.1), in the S6 layout: the input term mixes the previous
  * and the current step with a data-dependent lambda in [0, 1],

@@ -22,6 +22,9 @@ import os
 
 __all__ = [
     "MscError", "selective_scan_fwd", "selective_scan_fwd_ws",
+    "selective_scan_fwd_ckpt", "scan_checkpoint_size", "selective_scan_bwd",
+    "selective_scan_trap_fwd", "selective_state_update_trap",
+    "causal_conv1d_fwd", "causal_conv1d_update",
     "selective_state_update", "scan_workspace_size", "tuning_set",
     "check_device_error", "scratch_release", "profile_enable", "profile_read",
     "library_path", "load",
@@ -87,6 +90,14 @@ def load():
     lib.msc_selective_state_update_trap.argtypes = [vp] * 13 + [i64] * 3 + [st, vp]
     lib.msc_selective_scan_bwd.restype = st
     lib.msc_selective_scan_bwd.argtypes = [vp] * 20 + [i64] * 4 + [st, vp]
+    lib.msc_selective_scan_bwd_ckpt.restype = st
+    lib.msc_selective_scan_bwd_ckpt.argtypes = [vp] * 21 + [i64] * 4 + [st, vp]
+    lib.msc_selective_scan_fwd_ckpt.restype = st
+    lib.msc_selective_scan_fwd_ckpt.argtypes = ([vp] * 12 + [i64] * 4
+                                                + [st, vp, sz, vp])
+    lib.msc_scan_checkpoint_size.restype = st
+    lib.msc_scan_checkpoint_size.argtypes = [i64] * 4 + [ctypes.POINTER(i64),
+                                                         ctypes.POINTER(sz)]
     lib.msc_causal_conv1d_fwd.restype = st
     lib.msc_causal_conv1d_fwd.argtypes = [vp] * 6 + [i64] * 4 + [ctypes.c_int, st, vp]
     lib.msc_causal_conv1d_update.restype = st
@@ -353,11 +364,46 @@ def selective_state_update_trap(state, u_prev, B_prev, u, dt, lam, A, B, C, D=No
     return out
 
 
+def scan_checkpoint_size(batch, L, d_inner, d_state):
+    """(interval, bytes) of the checkpoint array selective_scan_fwd_ckpt
+    writes: (batch, ceil(L / interval), d_inner, d_state) fp32."""
+    tt, n = ctypes.c_int64(0), ctypes.c_size_t(0)
+    _check("msc_scan_checkpoint_size", load().msc_scan_checkpoint_size(
+        batch, L, d_inner, d_state, ctypes.byref(tt), ctypes.byref(n)))
+    return int(tt.value), int(n.value)
+
+
+def selective_scan_fwd_ckpt(u, dt, A, B, C, D=None, z=None, dt_bias=None,
+                            h0=None, out=None, last_state=None, ckpt=None):
+    """Euler selective scan that also writes the backward's checkpoints
+    -> (out, last_state, ckpt); ckpt is (batch, rows, d_inner, d_state) fp32,
+    row k the state entering step k * interval (scan_checkpoint_size)."""
+    lib = load()
+    torch = _torch()
+    p, out, last_state, dims, code, dev = _scan_args(
+        u, dt, A, B, C, D, z, dt_bias, out, last_state, True)
+    batch, L, d_inner, d_state = dims
+    tt, _ = scan_checkpoint_size(batch, L, d_inner, d_state)
+    shape = (batch, (L + tt - 1) // tt, d_inner, d_state)
+    if ckpt is None:
+        ckpt = torch.empty(shape, dtype=torch.float32, device=dev)
+    cp = _ptr(ckpt, "ckpt", torch.float32, shape, dev)
+    h0p = _ptr(h0, "h0", torch.float32, (batch, d_inner, d_state), dev)
+    st = lib.msc_selective_scan_fwd_ckpt(
+        p["u"], p["dt"], p["A"], p["B"], p["C"], p["D"], p["z"],
+        p["dt_bias"], h0p, p["out"], p["last_state"], cp, *dims, code, None, 0,
+        _stream(dev))
+    _check("msc_selective_scan_fwd_ckpt", st)
+    return out, last_state, ckpt
+
+
 def selective_scan_bwd(u, dt, A, B, C, D=None, z=None, dt_bias=None, h0=None,
-                       dout=None, dlast_state=None, want_dh0=False):
+                       dout=None, dlast_state=None, want_dh0=False, ckpt=None):
     """Backward pass of selective_scan_fwd on the GPU -> dict of gradients:
     du, ddt, dz (u's dtype), dA, dB, dC, dD, ddt_bias, dh0 (fp32; dz, dD,
-    ddt_bias None when z, D, dt_bias are None; dh0 only with want_dh0)."""
+    ddt_bias None when z, D, dt_bias are None; dh0 only with want_dh0).
+    ckpt: the checkpoints selective_scan_fwd_ckpt wrote for these inputs,
+    read instead of recomputed (None: recomputed)."""
     torch = _torch()
     batch, L, d_inner = u.shape
     d_state = B.shape[-1]
@@ -372,12 +418,19 @@ def selective_scan_bwd(u, dt, A, B, C, D=None, z=None, dt_bias=None, h0=None,
              ddt_bias=torch.empty(d_inner, dtype=f32, device=dev) if dt_bias is not None else None,
              dh0=torch.empty(batch, d_inner, d_state, dtype=f32, device=dev) if want_dh0 else None)
     P = lambda t, name, dt_=None, shape=None: _ptr(t, name, dt_, shape, dev)
-    st = load().msc_selective_scan_bwd(
+    head = [
         P(u, "u", sdt, (batch, L, d_inner)), P(dt, "dt", sdt, (batch, L, d_inner)),
         P(A, "A", f32, (d_inner, d_state)), P(B, "B", sdt, (batch, L, d_state)),
         P(C, "C", sdt, (batch, L, d_state)), P(D, "D", f32, (d_inner,)),
         P(z, "z", sdt, (batch, L, d_inner)), P(dt_bias, "dt_bias", f32, (d_inner,)),
-        P(h0, "h0", f32, (batch, d_inner, d_state)), P(dout, "dout", sdt, (batch, L, d_inner)),
+        P(h0, "h0", f32, (batch, d_inner, d_state))]
+    fn = "msc_selective_scan_bwd"
+    if ckpt is not None:
+        fn = "msc_selective_scan_bwd_ckpt"
+        tt, _ = scan_checkpoint_size(batch, L, d_inner, d_state)
+        head.append(P(ckpt, "ckpt", f32, (batch, (L + tt - 1) // tt, d_inner, d_state)))
+    st = getattr(load(), fn)(
+        *head, P(dout, "dout", sdt, (batch, L, d_inner)),
         P(dlast_state, "dlast_state", f32, (batch, d_inner, d_state)),
         g["du"].data_ptr(), g["ddt"].data_ptr(), g["dA"].data_ptr(), g["dB"].data_ptr(),
         g["dC"].data_ptr(), None if g["dD"] is None else g["dD"].data_ptr(),
@@ -385,7 +438,7 @@ def selective_scan_bwd(u, dt, A, B, C, D=None, z=None, dt_bias=None, h0=None,
         None if g["ddt_bias"] is None else g["ddt_bias"].data_ptr(),
         None if g["dh0"] is None else g["dh0"].data_ptr(),
         batch, L, d_inner, d_state, code, _stream(dev))
-    _check("msc_selective_scan_bwd", st)
+    _check(fn, st)
     return g
 
 

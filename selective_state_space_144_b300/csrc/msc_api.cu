@@ -210,11 +210,17 @@ static msc_status run_scan(const void* u, const void* dt, const float* A, const 
                            int64_t L, int64_t d_inner, int64_t d_state, msc_dtype dtype,
                            void* ws, size_t ws_bytes, bool own_ws, msc_stream_t stream,
                            const float* h0 = nullptr, int zoh = 0, const void* lam = nullptr,
-                           const void* u_prev = nullptr, const void* B_prev = nullptr) {
+                           const void* u_prev = nullptr, const void* B_prev = nullptr,
+                           float* ckpt_out = nullptr) {
     ScanCheck c = check_scan(u, dt, A, B, C, D, z, dt_bias, out, last_state, batch, L, d_inner,
                              d_state, dtype, h0, lam, u_prev, B_prev);
     if (c.st != MSC_OK) return c.st;
     if (batch == 0 || d_inner == 0) return MSC_OK;
+    // backward checkpoints: written by the TMA output kernel only, at octet
+    // starts, so the interval must divide every time chunk
+    const int ck_tt = msc::bwd_tma_tile(d_state);
+    if (ckpt_out && L > 0 && (!c.plan.tma || c.plan.chunk % ck_tt != 0 || zoh || lam))
+        return MSC_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t need = c.plan.ws_bytes;
     void* w = ws;
@@ -236,6 +242,11 @@ static msc_status run_scan(const void* u, const void* dt, const float* A, const 
     a.chunk = c.plan.chunk; a.K = c.plan.K; a.ntile = c.plan.ntile; a.vec = c.vec;
     a.wait_limit = g_starve > 0 ? (uint32_t)g_starve : msc::kWaitLimit;
     a.starve = g_starve > 0;
+    if (ckpt_out && L > 0) {
+        a.ckpt_out = ckpt_out;
+        a.ckpt_shift = ck_tt == 16 ? 4 : 3;
+        a.ckpt_rows = (L + ck_tt - 1) / ck_tt;
+    }
     cudaError_t e;
     if (c.plan.tma) {
         float* Bf = nullptr;
@@ -348,6 +359,46 @@ msc_status msc_selective_scan_fwd_ex(const void* u, const void* dt, const float*
     return run_scan(u, dt, A, B, C, D, z, dt_bias, out, last_state, batch, L, d_inner, d_state,
                     dtype, workspace, workspace_bytes, workspace == nullptr, stream, h0,
                     disc == MSC_DISC_ZOH ? 1 : 0);
+}
+
+msc_status msc_scan_checkpoint_size(int64_t batch, int64_t L, int64_t d_inner, int64_t d_state,
+                                    int64_t* interval, size_t* bytes) {
+    if (!interval || !bytes) return MSC_ERR_INVALID_ARG;
+    if (batch < 0 || L < 0 || d_inner < 0 || d_state < 0) return MSC_ERR_INVALID_ARG;
+    if (!(d_state == 8 || d_state == 16 || d_state == 32 || d_state == 64))
+        return MSC_ERR_UNSUPPORTED;
+    const int64_t tt = msc::bwd_tma_tile(d_state);
+    const int64_t rows = (L + tt - 1) / tt;
+    int64_t br, brd, n;
+    if (!mul_ok(batch, rows, &br) || !mul_ok(br, d_inner, &brd) || !mul_ok(brd, d_state, &n) ||
+        n > std::numeric_limits<int64_t>::max() / 4)
+        return MSC_ERR_UNSUPPORTED;
+    *interval = tt;
+    *bytes = (size_t)n * sizeof(float);
+    return MSC_OK;
+}
+
+msc_status msc_selective_scan_fwd_ckpt(const void* u, const void* dt, const float* A,
+                                       const void* B, const void* C, const float* D,
+                                       const void* z, const float* dt_bias, const float* h0,
+                                       void* out, float* last_state, float* ckpt, int64_t batch,
+                                       int64_t L, int64_t d_inner, int64_t d_state,
+                                       msc_dtype dtype, void* workspace, size_t workspace_bytes,
+                                       msc_stream_t stream) {
+    int64_t tt = 0;
+    size_t bytes = 0;
+    const msc_status st = msc_scan_checkpoint_size(batch < 0 ? 0 : batch, L < 0 ? 0 : L,
+                                                   d_inner < 0 ? 0 : d_inner,
+                                                   d_state < 0 ? 0 : d_state, &tt, &bytes);
+    if (st == MSC_ERR_INVALID_ARG) return st;
+    if (batch > 0 && L > 0 && d_inner > 0) {
+        if (st != MSC_OK) return st;
+        if (!ckpt) return MSC_ERR_INVALID_ARG;
+        if (!aligned(ckpt, 16)) return MSC_ERR_ALIGNMENT;
+    }
+    return run_scan(u, dt, A, B, C, D, z, dt_bias, out, last_state, batch, L, d_inner, d_state,
+                    dtype, workspace, workspace_bytes, workspace == nullptr, stream, h0, 0,
+                    nullptr, nullptr, nullptr, ckpt);
 }
 
 msc_status msc_selective_scan_trap_fwd(const void* u, const void* dt, const void* lam,
@@ -468,13 +519,13 @@ msc_status msc_selective_state_update_trap(float* state, const void* u_prev, con
                       0, stream, lam, u_prev, B_prev);
 }
 
-msc_status msc_selective_scan_bwd(const void* u, const void* dt, const float* A, const void* B,
-                                  const void* C, const float* D, const void* z,
-                                  const float* dt_bias, const float* h0, const void* dout,
-                                  const float* dlast, void* du, void* ddt, float* dA, float* dB,
-                                  float* dC, float* dD, void* dz, float* ddt_bias, float* dh0,
-                                  int64_t batch, int64_t L, int64_t d_inner, int64_t d_state,
-                                  msc_dtype dtype, msc_stream_t stream) {
+static msc_status run_bwd(const void* u, const void* dt, const float* A, const void* B,
+                          const void* C, const float* D, const void* z, const float* dt_bias,
+                          const float* h0, const void* dout, const float* dlast, void* du,
+                          void* ddt, float* dA, float* dB, float* dC, float* dD, void* dz,
+                          float* ddt_bias, float* dh0, int64_t batch, int64_t L,
+                          int64_t d_inner, int64_t d_state, msc_dtype dtype,
+                          msc_stream_t stream, const float* ckpt) {
     if (dtype != MSC_F32 && dtype != MSC_BF16) return MSC_ERR_INVALID_ARG;
     if (batch < 0 || L < 0 || d_inner < 0 || d_state < 0) return MSC_ERR_INVALID_ARG;
     if (d_state < 1 || d_state > 64) return MSC_ERR_UNSUPPORTED;
@@ -494,6 +545,7 @@ msc_status msc_selective_scan_bwd(const void* u, const void* dt, const float* A,
     const void* f32[] = {A, D, dt_bias, h0, dlast, dA, dB, dC, dD, ddt_bias, dh0};
     for (const void* p : f32)
         if (p && !aligned(p, 4)) return MSC_ERR_ALIGNMENT;
+    if (ckpt && !aligned(ckpt, 16)) return MSC_ERR_ALIGNMENT;  // read as 16-byte vectors
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     msc::BwdArgs a{};
     a.u = u; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.dt_bias = dt_bias;
@@ -504,6 +556,11 @@ msc_status msc_selective_scan_bwd(const void* u, const void* dt, const float* A,
     // allows, else the element-load checkpoint and adjoint kernels
     const bool v2 = g_scan_path == 0 && L > 0 &&
                     msc::bwd_tma_supported(d_state, d_inner, u, dt, z, dout, dB, dC);
+    // the forward's checkpoints are read by the TMA backward only
+    const bool ext = ckpt != nullptr && L > 0;
+    if (ext && !v2) return MSC_ERR_UNSUPPORTED;
+    a.ext_ckpt = ext ? 1 : 0;
+    if (ext) a.ckpt = const_cast<float*>(ckpt);  // read only when ext_ckpt
     a.nseg = (L + msc::kBwdSegment - 1) / msc::kBwdSegment;
     a.vec = (d_state % 4 == 0) && (!B || aligned(B, 4 * es)) && (!C || aligned(C, 4 * es));
     // the accumulated gradients start from zero
@@ -517,17 +574,43 @@ msc_status msc_selective_scan_bwd(const void* u, const void* dt, const float* A,
     void* ck = nullptr;
     size_t ck_bytes = v2 ? msc::scan_bwd_tma_scratch(a, dtype)
                          : msc::scan_bwd_ckpt_bytes(batch, L, d_inner, d_state);
-    if (ck_bytes == 0) ck_bytes = 256;
-    if (scratch_alloc(&ck, ck_bytes, s) != cudaSuccess) return MSC_ERR_CUDA;
+    if (ck_bytes == 0 && !ext) ck_bytes = 256;
+    if (ck_bytes > 0 && scratch_alloc(&ck, ck_bytes, s) != cudaSuccess) return MSC_ERR_CUDA;
     if (v2) {
         e = msc::launch_scan_bwd_tma(a, dtype, ck, s);
     } else {
         a.ckpt = static_cast<float*>(ck);
         e = msc::launch_scan_bwd(a, dtype, s);
     }
-    const cudaError_t f = cudaFreeAsync(ck, s);
-    if (e == cudaSuccess) e = f;
+    if (ck) {
+        const cudaError_t f = cudaFreeAsync(ck, s);
+        if (e == cudaSuccess) e = f;
+    }
     return e == cudaSuccess ? MSC_OK : MSC_ERR_CUDA;
+}
+
+msc_status msc_selective_scan_bwd(const void* u, const void* dt, const float* A, const void* B,
+                                  const void* C, const float* D, const void* z,
+                                  const float* dt_bias, const float* h0, const void* dout,
+                                  const float* dlast, void* du, void* ddt, float* dA, float* dB,
+                                  float* dC, float* dD, void* dz, float* ddt_bias, float* dh0,
+                                  int64_t batch, int64_t L, int64_t d_inner, int64_t d_state,
+                                  msc_dtype dtype, msc_stream_t stream) {
+    return run_bwd(u, dt, A, B, C, D, z, dt_bias, h0, dout, dlast, du, ddt, dA, dB, dC, dD, dz,
+                   ddt_bias, dh0, batch, L, d_inner, d_state, dtype, stream, nullptr);
+}
+
+msc_status msc_selective_scan_bwd_ckpt(const void* u, const void* dt, const float* A,
+                                       const void* B, const void* C, const float* D,
+                                       const void* z, const float* dt_bias, const float* h0,
+                                       const float* ckpt, const void* dout, const float* dlast,
+                                       void* du, void* ddt, float* dA, float* dB, float* dC,
+                                       float* dD, void* dz, float* ddt_bias, float* dh0,
+                                       int64_t batch, int64_t L, int64_t d_inner,
+                                       int64_t d_state, msc_dtype dtype, msc_stream_t stream) {
+    if (!ckpt && batch > 0 && L > 0 && d_inner > 0) return MSC_ERR_INVALID_ARG;
+    return run_bwd(u, dt, A, B, C, D, z, dt_bias, h0, dout, dlast, du, ddt, dA, dB, dC, dD, dz,
+                   ddt_bias, dh0, batch, L, d_inner, d_state, dtype, stream, ckpt);
 }
 
 static msc_status run_conv(const void* x, const float* w, const float* bias,

@@ -36,14 +36,18 @@ __device__ __forceinline__ float log1p_unit(float e) {
     p = fmaf(p, s, 0.033152375f);
     p = fmaf(p, s, -0.14426334f);
     p = fmaf(p, s, 0.8109302f);
-    return e * p;
+    return __fmul_rn(e, p);
 }
 
 // softplus(x) = log(1 + e^x) = max(x, 0) + log(1 + e^-|x|).  The step size
-// of the selective scan (the Delta of the pages' selection mechanism).
+// of the selective scan (the Delta of the pages' selection mechanism).  The
+// last multiply and add are separately rounded (not fused), so that every
+// kernel -- scalar here, on pairs in the TMA scan -- gets the same delta bit
+// for bit, and a backward pass recomputing states from checkpoints that a
+// forward kernel wrote walks the very same states.
 __device__ __forceinline__ float softplus(float x) {
     const float e = ex2(-fabsf(x) * kLog2e);
-    return fmaxf(x, 0.0f) + log1p_unit(e);
+    return __fadd_rn(fmaxf(x, 0.0f), log1p_unit(e));
 }
 
 // silu(z) = z * sigmoid(z) = z / (1 + e^-z).  For z -> -inf the divisor

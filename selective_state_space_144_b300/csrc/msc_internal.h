@@ -38,6 +38,9 @@ struct ScanArgs {
     int vec;           // 1: B/C rows can be read 4 elements at a time
     uint32_t wait_limit;   // polls before a TMA kernel's wait for a copy gives up
     int starve;            // failure-detection test: 1 = TMA kernels issue no copies
+    float* ckpt_out;       // TMA output kernel: the states entering every 2^ckpt_shift
+    int ckpt_shift;        //   steps, (batch, ckpt_rows, d_inner, N) fp32, for the
+    int64_t ckpt_rows;     //   backward pass (ckpt_shift >= log2 of the octet)
 };
 
 // How one scan call is cut up.
@@ -121,6 +124,7 @@ struct BwdArgs {
     float* ckpt;
     int64_t batch, L, d_inner, N, nseg;
     int vec;           // 1: B/C rows can be read 4 elements at a time
+    int ext_ckpt;      // TMA path: ckpt holds the forward pass's checkpoints
 };
 // The element-load checkpoint kernel, then the element-load adjoint (a.ckpt:
 // scan_bwd_ckpt_bytes of scratch).

@@ -253,7 +253,7 @@ __device__ __forceinline__ void trap_seed(const ScanArgs& a, int b, int64_t d, i
         bx[i] = pk2(uq * Elem<T>::load(Br + 2 * i), uq * Elem<T>::load(Br + 2 * i + 1));
 }
 
-template <typename T, int G, int NS, int TT, int S, int DISC, int OCT>
+template <typename T, int G, int NS, int TT, int S, int DISC, int OCT, bool CK = false>
 __global__ void __launch_bounds__(32)
 scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dt,
                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
@@ -427,6 +427,16 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 }
                 flushed = true;
                 break;
+            }
+            // checkpoint for the backward pass: the state entering this
+            // octet when it starts an interval of 2^ckpt_shift steps
+            if (CK && ((tc0 + sb) & ((1 << a.ckpt_shift) - 1)) == 0) {
+                float* cp = a.ckpt_out +
+                            (((int64_t)b * a.ckpt_rows + ((tc0 + sb) >> a.ckpt_shift)) * a.d_inner +
+                             d) * N + n0;
+#pragma unroll
+                for (int i2 = 0; i2 < NP; ++i2)
+                    reinterpret_cast<u64*>(cp)[i2] = hp[i2];
             }
             // (1) the state updates of this octet
             const float4* sd =
@@ -924,6 +934,9 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
     const int64_t d = d0 + ch;
     const int nt = (int)a.nseg;
     const int rounds = 2 * nt - 1;
+    // with checkpoints from the forward pass the forward rounds are skipped:
+    // logical rounds r0 .. rounds-1, ring position q = r - r0
+    const int r0 = a.ext_ckpt ? nt - 1 : 0;
     const bool has_z = a.z != nullptr;
     const uint32_t tx_fwd = (uint32_t)(2 * Lay::kX + Lay::kBC);
     const uint32_t tx_rev = (uint32_t)((3 + (has_z ? 1 : 0)) * Lay::kX + 2 * Lay::kBC);
@@ -943,10 +956,12 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
         }
     }
     __syncwarp();
-    // round r: forward tile r (r < nt-1), else reverse tile 2nt-2-r; stage r % S
-    auto issue = [&](int r) {
-        const uint32_t st = sbase + (r % S) * Lay::kStage;
-        const uint32_t bar = bar0 + 8 * (r % S);
+    // round r = r0 + q: forward tile r (r < nt-1), else reverse tile 2nt-2-r;
+    // stage q % S
+    auto issue = [&](int q) {
+        const int r = r0 + q;
+        const uint32_t st = sbase + (q % S) * Lay::kStage;
+        const uint32_t bar = bar0 + 8 * (q % S);
         const bool fwd = r < nt - 1;
         const int32_t tt = (int32_t)((int64_t)(fwd ? r : 2 * nt - 2 - r) * TT);
         mbar_expect_tx(bar, fwd ? tx_fwd : tx_rev);
@@ -959,9 +974,9 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
             tma_load_3d(st + Lay::kCoff, &tm_C, bar, 0, tt, b);
         }
     };
-    int issued = min(S, rounds);
+    int issued = min(S, rounds - r0);
     if (lane == 0)
-        for (int r = 0; r < issued; ++r) issue(r);
+        for (int q = 0; q < issued; ++q) issue(q);
 
     u64 A2[NP], An[NP], h[NP], dh[NP], dAacc[NP];
 #pragma unroll
@@ -983,8 +998,11 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
     float4* const tab = reinterpret_cast<float4*>(smem + Lay::kTab);
     float2* const tab2 = reinterpret_cast<float2*>(smem + Lay::kTab2);
     float* const hb = reinterpret_cast<float*>(smem + Lay::kH);
-    // the CTA's checkpoint rows: entering state of tile k at ck + k * 32*NS
-    float* const ck = a.ckpt + (int64_t)blockIdx.x * nt * (32 * NS) + lane * NS;
+    // checkpoint rows, (batch, tile, d_inner, N): the state entering tile k
+    // (row 0, the state before the sequence, is never read: h0 or zero)
+    auto ck_row = [&](int kk) {
+        return a.ckpt + (((int64_t)b * nt + kk) * a.d_inner + d) * N + n0;
+    };
     // per-lane output of the reverse rounds: g = 0 dz, 1 ddt, 2 du, 3 none
     T* outp = static_cast<T*>(a.du);  // also the (unwritten) address of g = 3
     bool has_out = g < 3;
@@ -1004,11 +1022,12 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
     bool ok = true;
     int waited = 0;
     u64 hin[NP];
-    for (int r = 0; r < rounds; ++r) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (r % S), (r / S) & 1, kWaitLimit));
+    for (int q = 0; q < rounds - r0; ++q) {
+        const int r = r0 + q;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (q % S), (q / S) & 1, kWaitLimit));
         if (!ok) break;
-        waited = r + 1;
-        const unsigned char* st = smem + (r % S) * Lay::kStage;
+        waited = q + 1;
+        const unsigned char* st = smem + (q % S) * Lay::kStage;
         const T* su = reinterpret_cast<const T*>(st);
         const T* sdt = reinterpret_cast<const T*>(st + Lay::kX);
         const T* sz = reinterpret_cast<const T*>(st + 2 * Lay::kX);
@@ -1031,35 +1050,39 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
         if (r < nt - 1) {
             // ---- forward round: tile r is whole (only the last tile can be short)
 #pragma unroll
-            for (int q = 0; q < PQ; ++q) {
-                const int e = lane + 32 * q;  // step g + 4q of channel ch
+            for (int pq = 0; pq < PQ; ++pq) {
+                const int e = lane + 32 * pq;  // step g + 4pq of channel ch
                 const float dl = softplus(lds_elem<T>(sdt + e) + bias);
                 *reinterpret_cast<float2*>(tab + e) = make_float2(dl, dl * lds_elem<T>(su + e));
             }
             __syncwarp();
 #pragma unroll
             for (int j = 0; j < TT; ++j) step(j, h);
-            st_pairs<NP>(ck + (int64_t)(r + 1) * (32 * NS), h);
+            st_pairs<NP>(ck_row(r + 1), h);
         } else {
             // ---- reverse round
             const int it = 2 * nt - 2 - r;
             const int64_t t0 = (int64_t)it * TT;
             const int nst = (int)min((int64_t)TT, a.L - t0);
             if (r == nt - 1) {
+                if (a.ext_ckpt && nt >= 2) {
+                    ld_pairs<NP>(ck_row(nt - 1), hin);     // from the forward pass
+                } else {
 #pragma unroll
-                for (int i = 0; i < NP; ++i) hin[i] = h[i];  // the forward's last state
+                    for (int i = 0; i < NP; ++i) hin[i] = h[i];  // the forward walk's last state
+                }
             }
             // the entering state of the next (earlier) tile, loaded ahead
             u64 hnext[NP];
 #pragma unroll
             for (int i = 0; i < NP; ++i) hnext[i] = pk2(0.0f, 0.0f);
-            if (it >= 2) ld_pairs<NP>(ck + (int64_t)(it - 1) * (32 * NS), hnext);
+            if (it >= 2) ld_pairs<NP>(ck_row(it - 1), hnext);
             else if (it == 1 && h0row) ld_pairs<NP>(h0row, hnext);
             // (1) per-(step, channel) scalars of the tile
 #pragma unroll
-            for (int q = 0; q < PQ; ++q) {
-                const int e = lane + 32 * q;
-                const int j = g + G * q;
+            for (int pq = 0; pq < PQ; ++pq) {
+                const int e = lane + 32 * pq;
+                const int j = g + G * pq;
                 const float x = lds_elem<T>(sdt + e) + bias;
                 const float uu = lds_elem<T>(su + e);
                 const float go = lds_elem<T>(sg + e);
@@ -1173,9 +1196,9 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
                 T* const orow_dt = static_cast<T*>(a.ddt) + o0;
                 T* const orow_du = static_cast<T*>(a.du) + o0;
 #pragma unroll
-                for (int q = 0; q < PQ; ++q) {
-                    const int e = lane + 32 * q;
-                    const int j = g + G * q;
+                for (int pq = 0; pq < PQ; ++pq) {
+                    const int e = lane + 32 * pq;
+                    const int j = g + G * pq;
                     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
                     for (int g2 = 0; g2 < G; ++g2) {
@@ -1200,16 +1223,16 @@ scan_bwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
             for (int i = 0; i < NP; ++i) hin[i] = hnext[i];
         }
         __syncwarp();
-        if (r + S < rounds) {
+        if (q + S < rounds - r0) {
             if (lane == 0) {
                 fence_proxy_async_smem();
-                issue(r + S);
+                issue(q + S);
             }
-            issued = r + S + 1;
+            issued = q + S + 1;
         }
     }
     // copies still in flight (after a failed wait) land before exit
-    for (int r = waited; r < issued; ++r) mbar_wait(bar0 + 8 * (r % S), (r / S) & 1, kWaitLimit);
+    for (int q = waited; q < issued; ++q) mbar_wait(bar0 + 8 * (q % S), (q / S) & 1, kWaitLimit);
     if (!ok) {
         if (lane == 0) atomicOr(&g_scan_error, 1u);
         return;
@@ -1322,7 +1345,10 @@ static cudaError_t launch_tma_d(const ScanArgs& a, const ScanPlan& p, const CUte
     }
     const int64_t nb = a.batch * (int64_t)p.K * p.ntile;
     const ProfileMark m = profile_begin(s, MSC_PROF_SCAN);
-    auto kern = scan_tma_kernel<T, G, NS, TT, S, DISC, kOct>;
+    // checkpoints for the backward pass: a separate instantiation, so that
+    // the plain forward's code is unchanged (Euler only, as the backward)
+    auto kern = (DISC == 0 && a.ckpt_out) ? scan_tma_kernel<T, G, NS, TT, S, DISC, kOct, true>
+                                          : scan_tma_kernel<T, G, NS, TT, S, DISC, kOct, false>;
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     kern<<<(unsigned)nb, 32, smem, s>>>(mu, mdt, mz, mB, mC, ml, a, p.K);
@@ -1458,7 +1484,8 @@ static bool bwd_needs_bc(const BwdArgs& a, msc_dtype dtype) {
 size_t scan_bwd_tma_scratch(const BwdArgs& a, msc_dtype dtype) {
     const int64_t TT = bwd_tma_tile(a.N);
     const int64_t nt = (a.L + TT - 1) / TT;
-    const size_t ck = ((size_t)(a.batch * a.d_inner * a.N * nt) * 4 + 255) / 256 * 256;
+    const size_t ck =
+        a.ext_ckpt ? 0 : ((size_t)(a.batch * a.d_inner * a.N * nt) * 4 + 255) / 256 * 256;
     const size_t bc = bwd_needs_bc(a, dtype) ? 2 * (size_t)(a.batch * a.L * a.N) * 4 : 0;
     return ck + bc;
 }
@@ -1466,8 +1493,9 @@ size_t scan_bwd_tma_scratch(const BwdArgs& a, msc_dtype dtype) {
 cudaError_t launch_scan_bwd_tma(BwdArgs a, msc_dtype dtype, void* scratch, cudaStream_t s) {
     const int64_t TT = bwd_tma_tile(a.N);
     a.nseg = (a.L + TT - 1) / TT;
-    a.ckpt = static_cast<float*>(scratch);
-    const size_t ck = ((size_t)(a.batch * a.d_inner * a.N * a.nseg) * 4 + 255) / 256 * 256;
+    const size_t ck =
+        a.ext_ckpt ? 0 : ((size_t)(a.batch * a.d_inner * a.N * a.nseg) * 4 + 255) / 256 * 256;
+    if (!a.ext_ckpt) a.ckpt = static_cast<float*>(scratch);
     const float* Bf = static_cast<const float*>(a.B);
     const float* Cf = static_cast<const float*>(a.C);
     if (bwd_needs_bc(a, dtype)) {

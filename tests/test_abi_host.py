@@ -257,6 +257,42 @@ def test_bwd_entry_point_validates(lib):
     assert bwd(batch=0) == 0                       # nothing to do
 
 
+def test_checkpoint_entry_points_validate(lib):
+    """msc_scan_checkpoint_size on the host, and the checkpointing forward
+    and backward refusing bad arguments before any launch."""
+    q = lib.msc_scan_checkpoint_size
+    tt, n = ctypes.c_int64(0), ctypes.c_size_t(0)
+    assert q(2, 100, 24, 16, ctypes.byref(tt), ctypes.byref(n)) == 0
+    assert tt.value == 16 and n.value == 2 * 7 * 24 * 16 * 4   # ceil(100 / 16) rows
+    assert q(3, 64, 8, 32, ctypes.byref(tt), ctypes.byref(n)) == 0
+    assert tt.value == 8 and n.value == 3 * 8 * 8 * 32 * 4
+    assert q(2, 0, 8, 64, ctypes.byref(tt), ctypes.byref(n)) == 0 and n.value == 0
+    assert q(2, 8, 8, 12, ctypes.byref(tt), ctypes.byref(n)) == 2    # no TMA path for 12
+    assert q(2, -1, 8, 16, ctypes.byref(tt), ctypes.byref(n)) == 1
+    assert q(2, 8, 8, 16, None, ctypes.byref(n)) == 1
+    assert q(1 << 40, 1 << 20, 1 << 10, 16, ctypes.byref(tt), ctypes.byref(n)) == 2
+
+    f = lib.msc_selective_scan_fwd_ckpt
+    ck = lambda ckpt, N=16, batch=2: f(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+                                       None, FAKE, None, ckpt, batch, 40, 16, N, 1,
+                                       None, 0, None)
+    assert ck(None) == 1                         # checkpoints required
+    assert ck(FAKE + 8) == 3                     # 16-byte aligned
+    assert ck(FAKE, N=12) == 2                   # TMA kernel only
+    assert ck(None, batch=0) == 0                # nothing to do
+
+    g = lib.msc_selective_scan_bwd_ckpt
+
+    def bwd(ckpt, batch=2):
+        return g(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, ckpt, FAKE, None,
+                 FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, batch, 40, 16, 16,
+                 1, None)
+
+    assert bwd(None) == 1
+    assert bwd(FAKE + 4) == 3
+    assert bwd(None, batch=0) == 0
+
+
 def test_scratch_release_without_pools(lib):
     """Before any call has taken scratch there is no pool to trim."""
     lib.msc_scratch_release.restype = ctypes.c_int
