@@ -434,9 +434,16 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 float* cp = a.ckpt_out +
                             (((int64_t)b * a.ckpt_rows + ((tc0 + sb) >> a.ckpt_shift)) * a.d_inner +
                              d) * N + n0;
+                // streaming stores: read again only by the backward pass
+                if constexpr (NP == 1) {
+                    __stcs(reinterpret_cast<float2*>(cp), make_float2(lo2(hp[0]), hi2(hp[0])));
+                } else {
 #pragma unroll
-                for (int i2 = 0; i2 < NP; ++i2)
-                    reinterpret_cast<u64*>(cp)[i2] = hp[i2];
+                    for (int i2 = 0; i2 < NP; i2 += 2)
+                        __stcs(reinterpret_cast<float4*>(cp) + i2 / 2,
+                               make_float4(lo2(hp[i2]), hi2(hp[i2]), lo2(hp[i2 + 1]),
+                                           hi2(hp[i2 + 1])));
+                }
             }
             // (1) the state updates of this octet
             const float4* sd =
