@@ -303,15 +303,18 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     }
     __syncwarp();
 
+    // u, dt, z, lambda are read once (evicted first); B and C, read by every
+    // channel tile of the batch row, keep the default policy
+    const uint64_t once = lane == 0 ? l2_evict_first_policy() : 0;
     auto issue = [&](int i) {  // lane 0: tile i of this chunk into stage i % S
         const uint32_t st = sbase + (i % S) * Lay::kStage;
         const uint32_t bar = bar0 + 8 * (i % S);
         const int32_t tt = (int32_t)(tc0 + (int64_t)i * TT);
         mbar_expect_tx(bar, tx_bytes);
-        tma_load_3d(st, &tm_u, bar, d0, tt, b);
-        tma_load_3d(st + Lay::kX, &tm_dt, bar, d0, tt, b);
-        if (has_z) tma_load_3d(st + 2 * Lay::kX, &tm_z, bar, d0, tt, b);
-        if (TRAP) tma_load_3d(st + Lay::kLam, &tm_lam, bar, d0, tt, b);
+        tma_load_3d_hint(st, &tm_u, bar, d0, tt, b, once);
+        tma_load_3d_hint(st + Lay::kX, &tm_dt, bar, d0, tt, b, once);
+        if (has_z) tma_load_3d_hint(st + 2 * Lay::kX, &tm_z, bar, d0, tt, b, once);
+        if (TRAP) tma_load_3d_hint(st + Lay::kLam, &tm_lam, bar, d0, tt, b, once);
         tma_load_3d(st + Lay::kBoff, &tm_B, bar, 0, tt, b);
         tma_load_3d(st + Lay::kCoff, &tm_C, bar, 0, tt, b);
     };
