@@ -173,3 +173,38 @@ def test_ckpt_workload_layer_sampled():
     got = from_device(ck)[:1, :, ch]
     e = rel_l2(got, ref)
     assert e <= TOL["bf16"], f"checkpoint rows rel-L2 {e:.3e}"
+
+
+def test_ckpt_unsupported_shapes_are_refused():
+    """Shapes without the TMA kernels (d_inner not a multiple of 8, d_state
+    outside 8/16/32/64) are refused by the checkpointing entry points -- the
+    recomputing backward covers them -- and nothing is launched."""
+    x = synth.scan_inputs(2, 40, 12, 16, dtype="bf16", seed=1600)
+    a = scan_device_args(x)
+    with pytest.raises(msc.MscError) as e:
+        msc.selective_scan_fwd_ckpt(a["u"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                                    a["dt_bias"], ckpt=torch.empty(2, 5, 12, 16, device="cuda"))
+    assert e.value.status == 2
+    x = synth.scan_inputs(2, 40, 16, 12, dtype="bf16", seed=1601)
+    with pytest.raises(msc.MscError) as e:
+        msc.scan_checkpoint_size(2, 40, 16, 12)
+    assert e.value.status == 2
+    torch.cuda.synchronize()
+    msc.check_device_error()
+
+
+def test_ckpt_empty_and_single_step():
+    """L = 0 writes nothing and returns last_state = h0; L = 1 is one row,
+    h0 itself, and the backward from it matches the recomputing one."""
+    h0 = np.random.default_rng(31).standard_normal((2, 16, 16)).astype(np.float32)
+    x0 = synth.scan_inputs(2, 0, 16, 16, dtype="bf16", seed=1602)
+    a0 = scan_device_args(x0)
+    out, last, ck = msc.selective_scan_fwd_ckpt(a0["u"], a0["dt"], a0["A"], a0["B"], a0["C"],
+                                                a0["D"], a0["z"], a0["dt_bias"],
+                                                h0=to_device(h0, "f32"))
+    torch.cuda.synchronize()
+    assert ck.numel() == 0 and np.array_equal(from_device(last), h0)
+    x1 = synth.scan_inputs(2, 1, 16, 16, dtype="bf16", seed=1603, D="normal")
+    g_ck, g_re, _, _ = bwd_pair(x1, h0, seed=32)
+    for k in ("du", "ddt", "dz", "dh0"):
+        assert torch.equal(g_ck[k], g_re[k]), k
