@@ -200,26 +200,32 @@ constexpr int kStreamThreads = 128;
 
 // SS stages; the tile AHEAD steps ahead is loaded while one is updated and
 // the store of an earlier one (SS - AHEAD stages) may still read its stage.
-template <typename T, int SS>
+// TRAP: the exponential trapezoid's lambda and previous-token u (kX each)
+// and B row follow the C row.
+template <typename T, int SS, bool TRAP = false>
 struct StreamLayout {
     static constexpr int N = 16;
     static constexpr int kState = kStreamCh * N * 4;                    // 8192
     static constexpr int kX = kStreamCh * (int)sizeof(T);               // u / dt / z
     static constexpr int kBC = N * (int)sizeof(T);                      // B / C row
+    static constexpr int kBCa = ((kBC + 15) / 16) * 16;
     static constexpr int kU = kState, kDt = kU + kX, kZ = kDt + kX;
-    static constexpr int kB = kZ + kX, kC = kB + ((kBC + 15) / 16) * 16;
-    static constexpr int kStage = ((kC + kBC + 127) / 128) * 128;
+    static constexpr int kB = kZ + kX, kC = kB + kBCa;
+    static constexpr int kLam = kC + kBCa, kUp = kLam + kX, kBp = kUp + kX;
+    static constexpr int kEnd = TRAP ? kBp + kBC : kC + kBC;
+    static constexpr int kStage = ((kEnd + 127) / 128) * 128;
     static constexpr int kBar = SS * kStage;
     static constexpr int kTotal = kBar + SS * 8;
 };
 
-template <typename T, int SS, int AHEAD>
+template <typename T, int SS, int AHEAD, int DISC>
 __global__ void __launch_bounds__(kStreamThreads)
 state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
     static_assert(AHEAD >= 1 && AHEAD <= SS - 2, "a stage for the update and one for a store");
     constexpr int kStreamStages = SS;
     constexpr int kStreamAhead = AHEAD;
-    using Lay = StreamLayout<T, SS>;
+    constexpr bool ZOH = DISC == 1, TRAP = DISC == 2;
+    using Lay = StreamLayout<T, SS, TRAP>;
     constexpr int N = Lay::N;
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x;
@@ -232,7 +238,10 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + Lay::kBar;
     const uint32_t xbytes = (uint32_t)(nch * sizeof(T));
-    const uint32_t tx = (uint32_t)(nch * N * 4) + (a.z ? 3u : 2u) * xbytes + 2u * Lay::kBC;
+    // trapezoid: the previous token's u and B, when both are given
+    const bool prev = TRAP && a.u_prev && a.B_prev;
+    const uint32_t tx = (uint32_t)(nch * N * 4) + (a.z ? 3u : 2u) * xbytes + 2u * Lay::kBC +
+                        (TRAP ? xbytes : 0u) + (prev ? xbytes + (uint32_t)Lay::kBC : 0u);
 
     if (tid == 0) {
         for (int s2 = 0; s2 < kStreamStages; ++s2) mbar_init(bar0 + 8 * s2, 1);
@@ -253,6 +262,14 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
         if (a.z) bulk_load(dst + Lay::kZ, static_cast<const T*>(a.z) + ch, xbytes, bar);
         bulk_load(dst + Lay::kB, static_cast<const T*>(a.B) + b * N, Lay::kBC, bar);
         bulk_load(dst + Lay::kC, static_cast<const T*>(a.C) + b * N, Lay::kBC, bar);
+        if constexpr (TRAP) {
+            bulk_load(dst + Lay::kLam, static_cast<const T*>(a.lam) + ch, xbytes, bar);
+            if (prev) {
+                bulk_load(dst + Lay::kUp, static_cast<const T*>(a.u_prev) + ch, xbytes, bar);
+                bulk_load(dst + Lay::kBp, static_cast<const T*>(a.B_prev) + b * N, Lay::kBC,
+                          bar);
+            }
+        }
     };
     int issued = 0;
     if (tid == 0) {
@@ -262,6 +279,7 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
 
     // per-channel constants of the CTA's channels, once
     float A2[4][4], bias[4], Dd[4];
+    [[maybe_unused]] float iA[ZOH ? 4 : 1][4];  // zero-order hold: 1/A
     bool valid[4];
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
@@ -271,6 +289,10 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
         const float4 av = __ldg(reinterpret_cast<const float4*>(a.A + d * N) + q);
         A2[it][0] = av.x * kLog2e; A2[it][1] = av.y * kLog2e;
         A2[it][2] = av.z * kLog2e; A2[it][3] = av.w * kLog2e;
+        if constexpr (ZOH) {
+            iA[it][0] = 1.0f / av.x; iA[it][1] = 1.0f / av.y;
+            iA[it][2] = 1.0f / av.z; iA[it][3] = 1.0f / av.w;
+        }
         bias[it] = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
         Dd[it] = a.D ? __ldg(a.D + d) : 0.0f;
     }
@@ -293,10 +315,14 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
         const T* sdt = reinterpret_cast<const T*>(sp + Lay::kDt);
         const T* sz = reinterpret_cast<const T*>(sp + Lay::kZ);
         float Bv[4], Cv[4];
+        [[maybe_unused]] float Bq[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // trapezoid: B_prev
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             Bv[k] = lds_scalar<T>(reinterpret_cast<const T*>(sp + Lay::kB) + 4 * q + k);
             Cv[k] = lds_scalar<T>(reinterpret_cast<const T*>(sp + Lay::kC) + 4 * q + k);
+            if constexpr (TRAP) {
+                if (prev) Bq[k] = lds_scalar<T>(reinterpret_cast<const T*>(sp + Lay::kBp) + 4 * q + k);
+            }
         }
         const int64_t b = r + (int64_t)t * R;
         T* outp = static_cast<T*>(a.out) + b * a.d_inner + c0;
@@ -310,10 +336,26 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
             const float du = delta * uu;
             float hv[4] = {h.x, h.y, h.z, h.w};
             float y = 0.0f;
+            // the input term as the scan forms it (same operations, same order)
+            [[maybe_unused]] float tra = 0.0f, trc = 0.0f, uq = 0.0f;
+            if constexpr (TRAP) {
+                const float lt = lds_scalar<T>(reinterpret_cast<const T*>(sp + Lay::kLam) + cl);
+                tra = (1.0f - lt) * delta;
+                trc = (lt * delta) * uu;
+                uq = prev ? lds_scalar<T>(reinterpret_cast<const T*>(sp + Lay::kUp) + cl) : 0.0f;
+            }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float dA = ex2(delta * A2[it][k]);  // same rounding as the scan
-                hv[k] = fmaf(dA, hv[k], du * Bv[k]);
+                const float x2 = delta * A2[it][k];
+                const float dA = ex2(x2);  // same rounding as the scan
+                float inj;
+                if constexpr (ZOH)
+                    inj = zoh_gain(x2, dA, delta, iA[it][k]) * uu * Bv[k];
+                else if constexpr (TRAP)
+                    inj = fmaf(tra, uq * Bq[k], trc * Bv[k]);
+                else
+                    inj = du * Bv[k];
+                hv[k] = fmaf(dA, hv[k], inj);
                 y = fmaf(Cv[k], hv[k], y);
             }
             *hp = make_float4(hv[0], hv[1], hv[2], hv[3]);
@@ -347,21 +389,22 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
 
 bool stream_update_supported(const UpdateArgs& a, size_t es) {
     auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-    return a.N == 16 && !a.zoh && !a.trap && (a.d_inner * (int64_t)es) % 16 == 0 &&
-           al16(a.state) && al16(a.A) && al16(a.u) && al16(a.dt) && al16(a.B) && al16(a.C) &&
-           (!a.z || al16(a.z));
+    return a.N == 16 && (a.d_inner * (int64_t)es) % 16 == 0 && al16(a.state) && al16(a.A) &&
+           al16(a.u) && al16(a.dt) && al16(a.B) && al16(a.C) && (!a.z || al16(a.z)) &&
+           (!a.trap || (al16(a.lam) && (!a.u_prev || al16(a.u_prev)) &&
+                        (!a.B_prev || al16(a.B_prev))));
 }
 
-template <typename T, int SS, int AHEAD>
+template <typename T, int SS, int AHEAD, int DISC>
 static cudaError_t launch_stream_s(const UpdateArgs& a, int ctas_per_sm, cudaStream_t s) {
-    using Lay = StreamLayout<T, SS>;
+    using Lay = StreamLayout<T, SS, DISC == 2>;
     const int nJ = (int)((a.d_inner + kStreamCh - 1) / kStreamCh);
     const int64_t target = (int64_t)a.sms * ctas_per_sm;
     int64_t R = target / nJ;
     R = R < 1 ? 1 : (R > a.batch ? a.batch : R);
     const int64_t grid = (int64_t)nJ * R;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-    auto kern = state_update_stream_kernel<T, SS, AHEAD>;
+    auto kern = state_update_stream_kernel<T, SS, AHEAD, DISC>;
     if (Lay::kTotal > 48 * 1024)
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kTotal);
     kern<<<(unsigned)grid, kStreamThreads, Lay::kTotal, s>>>(a, nJ, (int)R, a.wait_limit);
@@ -374,7 +417,9 @@ static cudaError_t launch_stream_s(const UpdateArgs& a, int ctas_per_sm, cudaStr
 // small CTAs keep more tiles in flight than a few deep rings.
 template <typename T>
 static cudaError_t launch_stream(const UpdateArgs& a, cudaStream_t s) {
-    return launch_stream_s<T, 3, 1>(a, 8, s);
+    if (a.trap) return launch_stream_s<T, 3, 1, 2>(a, 8, s);
+    if (a.zoh) return launch_stream_s<T, 3, 1, 1>(a, 8, s);
+    return launch_stream_s<T, 3, 1, 0>(a, 8, s);
 }
 
 template <typename T, bool VEC>

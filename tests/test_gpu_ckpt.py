@@ -183,7 +183,7 @@ def test_ckpt_unsupported_shapes_are_refused():
     a = scan_device_args(x)
     with pytest.raises(msc.MscError) as e:
         msc.selective_scan_fwd_ckpt(a["u"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["z"],
-                                    a["dt_bias"], ckpt=torch.empty(2, 5, 12, 16, device="cuda"))
+                                    a["dt_bias"], ckpt=torch.empty(2, 3, 12, 16, device="cuda"))
     assert e.value.status == 2
     x = synth.scan_inputs(2, 40, 16, 12, dtype="bf16", seed=1601)
     with pytest.raises(msc.MscError) as e:

@@ -166,3 +166,56 @@ def test_decode_stream_kernel_shapes(dtype, batch, d_inner):
     finally:
         msc.tuning_set("update_path", 0)
     assert torch.equal(states[0], states[1])
+
+
+@pytest.mark.parametrize("disc", ["zoh", "trapezoid"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("batch,d_inner", [(3, 136), (5, 1000), (40, 640)])
+def test_decode_stream_kernel_variants(disc, dtype, batch, d_inner):
+    """The streaming decode kernel with the zero-order-hold input and with
+    the exponential trapezoid (lambda, and the previous token's u and B from
+    the second step on): four steps against the oracle on both decode
+    kernels, and the state bit for bit between them."""
+    N, steps = 16, 4
+    p = synth.decode_params(batch, d_inner, N, seed=70 + d_inner, dtype=dtype)
+    A, D, bias = to_device(p.A, "f32"), to_device(p.D, "f32"), to_device(p.dt_bias, "f32")
+    states = {}
+    try:
+        for path in (0, 1):
+            msc.tuning_set("update_path", path)
+            state = torch.from_numpy(p.state0).cuda()
+            ref_state = p.state0.astype(np.float64)
+            rng = np.random.default_rng(71 + d_inner)
+            up = Bp = None
+            worst = 0.0
+            for k in range(steps):
+                s = synth.decode_step(batch, d_inner, N, k, seed=70 + d_inner, dtype=dtype)
+                dv = _step_dev(s, dtype)
+                if disc == "zoh":
+                    out = msc.selective_state_update(state, dv["u"], dv["dt"], A, dv["B"],
+                                                     dv["C"], D, dv["z"], bias, zoh=True)
+                    ref_state, ref_out = oracle.state_update(ref_state, s.u, s.dt_raw, p.A,
+                                                             s.B, s.C, p.D, s.z, p.dt_bias,
+                                                             zoh=True)
+                else:
+                    lam = rng.uniform(0, 1, (batch, d_inner)).astype(np.float32)
+                    if dtype == "bf16":
+                        lam = synth.round_bf16(lam)
+                    out = msc.selective_state_update_trap(
+                        state, None if up is None else to_device(up, dtype),
+                        None if Bp is None else to_device(Bp, dtype), dv["u"], dv["dt"],
+                        to_device(lam, dtype), A, dv["B"], dv["C"], D, dv["z"], bias)
+                    ref_state, ref_out = oracle.state_update_trap(
+                        ref_state, up, Bp, s.u, s.dt_raw, lam, p.A, s.B, s.C, p.D, s.z,
+                        p.dt_bias)
+                    up, Bp = s.u, s.B
+                got = from_device(out)
+                assert np.all(np.isfinite(got))
+                worst = max(worst, rel_l2(got, as_stored(ref_out, dtype)))
+            torch.cuda.synchronize()
+            assert worst <= TOL[dtype], (path, worst)
+            assert rel_l2(from_device(state), ref_state) <= TOL[dtype]
+            states[path] = state.cpu()
+    finally:
+        msc.tuning_set("update_path", 0)
+    assert torch.equal(states[0], states[1])
