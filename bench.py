@@ -996,6 +996,26 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
         "note": ("back-to-back steps keep part of the 84 MB state in the "
                  "126 MB L2; the flushed figure is the cold-cache bound"),
     }
+    # the same step with the zero-order-hold input and with the exponential
+    # trapezoid (lambda ~ U[0, 1]; the previous token's u and B from the pool)
+    lam = dev_t(synth.round_bf16(np.random.default_rng(15).uniform(
+        0.0, 1.0, (Bb, Dd)).astype(np.float32)), "bf16")
+    def zstep(k):
+        uu, dd, zz, BB, CC = pool[k % 8]
+        msc.selective_state_update(state, uu, dd, A, BB, CC, Dv, zz, bias, out=out, zoh=True)
+    def tstep(k):
+        uu, dd, zz, BB, CC = pool[k % 8]
+        up, _, _, Bq, _ = pool[(k + 7) % 8]
+        msc.selective_state_update_trap(state, up, Bq, uu, dd, lam, A, BB, CC, Dv, zz, bias,
+                                        out=out)
+    for vname, call, extra in (("zoh", zstep, 0), ("trapezoid", tstep, 2 * Bb * Dd * 2 + Bb * Nn * 2)):
+        v_ms = hook_cold_ms(call, "update")
+        res[f"{name}_{vname}"] = {
+            "shape": [Bb, Dd, Nn], "us_per_step_l2_flushed": v_ms * 1e3,
+            "hbm_frac_l2_flushed": ((byt + extra) / (v_ms * 1e-3)) / (peaks["hbm_gbs"] * 1e9),
+            "algorithmic_bytes_per_step": byt + extra,
+        }
+    del lam
     return res
 
 
