@@ -1008,7 +1008,8 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
         up, _, _, Bq, _ = pool[(k + 7) % 8]
         msc.selective_state_update_trap(state, up, Bq, uu, dd, lam, A, BB, CC, Dv, zz, bias,
                                         out=out)
-    for vname, call, extra in (("zoh", zstep, 0), ("trapezoid", tstep, 2 * Bb * Dd * 2 + Bb * Nn * 2)):
+    trap_extra = 2 * Bb * Dd * 2 + Bb * Nn * 2   # lambda and u_prev, the B_prev rows
+    for vname, call, extra in (("zoh", zstep, 0), ("trapezoid", tstep, trap_extra)):
         v_ms = hook_cold_ms(call, "update")
         res[f"{name}_{vname}"] = {
             "shape": [Bb, Dd, Nn], "us_per_step_l2_flushed": v_ms * 1e3,
