@@ -82,6 +82,9 @@ cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s) {
     return pool ? cudaMallocFromPoolAsync(p, bytes, pool, s) : cudaMallocAsync(p, bytes, s);
 }
 
+// Longest sequence the TMA kernels take: their box coordinates are int32.
+constexpr int64_t kTmaMaxExtent = (int64_t{1} << 31) - 1024;
+
 struct ScanCheck {
     msc_status st;
     msc::ScanPlan plan;
@@ -137,7 +140,9 @@ ScanCheck check_scan(const void* u, const void* dt, const float* A, const void* 
             r.st = MSC_ERR_ALIGNMENT;
             return r;
         }
-    if (g_scan_path == 0 && L > 0 &&
+    // TMA box coordinates are 32-bit: longer sequences take the element-load
+    // kernels, whose indices are 64-bit
+    if (g_scan_path == 0 && L > 0 && L < kTmaMaxExtent &&
         msc::tma_scan_supported(d_state, d_inner, dtype, u, dt, z, lam)) {
         // fp32 B/C copies unless fp32 inputs already suit 16-byte TMA boxes
         const bool need_bc = dtype == MSC_BF16 || !aligned(B, 16) || !aligned(C, 16);
@@ -554,7 +559,7 @@ static msc_status run_bwd(const void* u, const void* dt, const float* A, const v
     a.batch = batch; a.L = L; a.d_inner = d_inner; a.N = d_state;
     // the TMA backward (checkpoints and adjoint in one kernel) where the shape
     // allows, else the element-load checkpoint and adjoint kernels
-    const bool v2 = g_scan_path == 0 && L > 0 &&
+    const bool v2 = g_scan_path == 0 && L > 0 && L < kTmaMaxExtent &&
                     msc::bwd_tma_supported(d_state, d_inner, u, dt, z, dout, dB, dC);
     // the forward's checkpoints are read by the TMA backward only
     const bool ext = ckpt != nullptr && L > 0;
