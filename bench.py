@@ -369,6 +369,19 @@ def run_ours(args):
     for k2 in (0, 4):
         pk.msc_peak_mufu_fma(sink.data_ptr(), sms * 4, 128, 20000, k2, stream, ctypes.byref(msf))
         mix[k2] = sms * 4 * 128 * 20000 * 8 / (msf.value * 1e-3)       # ex2/s
+    # the same groups (2 ex2 + their 2 operand FMAs) with packed or scalar
+    # FMAs, or the FMAs alone, as SM sub-partition cycles per warp and group
+    pk.msc_peak_mix.restype = ctypes.c_int
+    pk.msc_peak_mix.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_float)]
+    mix_cycles = {}
+    mix_names = ("ex2", "ex2 + 2 fma.f32x2", "ex2 + 4 fma.f32x2", "ex2 + 8 fma.f32",
+                 "4 fma.f32x2 alone")
+    warps_per_smsp = sms * 8 * 256 / 32 / (sms * 4.0)
+    for m, mname in enumerate(mix_names):
+        pk.msc_peak_mix(sink.data_ptr(), sms * 8, 256, 100, m, stream, ctypes.byref(msf))
+        pk.msc_peak_mix(sink.data_ptr(), sms * 8, 256, 20000, m, stream, ctypes.byref(msf))
+        mix_cycles[mname] = msf.value   # ms; cycles once the SM clock is known
     # streaming copy of 1 GiB (read + write bytes), the HBM figure of this run
     cp_src = torch.empty(2**28, dtype=torch.float32, device=dev)
     cp_dst = torch.empty_like(cp_src)
@@ -510,6 +523,10 @@ def run_ours(args):
             "mufu_fma_overlap": {
                 "ex2_per_s_alone": mix[0],
                 "ex2_per_s_with_4_ffma2_per_2_ex2": mix[4],
+                "cycles_per_warp_group": None,   # filled in once the clock is known
+                "cycles_reading": ("per SM sub-partition and warp, a group = 2 ex2 + 2 fma.f32 "
+                                   "(+ the listed FMAs); the clock is the SM clock sampled in "
+                                   "this run"),
                 "what": ("ex2 throughput with only its operand arithmetic, and with four "
                          "packed FMAs per pair of ex2 (the update core's ratio); equal rates "
                          "would mean the FMA work hides under MUFU"),
@@ -612,6 +629,9 @@ def run_ours(args):
         extras = run_extras(torch, msc, dev, ex2_peak, peaks)
 
     clocks = clk.summary()
+    mhz = clocks["sm_mhz"] or 2032.0
+    roofline["diagnostic"]["mufu_fma_overlap"]["cycles_per_warp_group"] = {
+        k: v * 1e-3 * mhz * 1e6 / (warps_per_smsp * 20000 * 4) for k, v in mix_cycles.items()}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n,
         "steps": args.steps, "warmup": args.warmup,

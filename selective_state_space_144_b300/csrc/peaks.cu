@@ -142,28 +142,44 @@ __global__ void k_scan_core(float* sink, int64_t iters) {
 // ex2 and K2 packed fma.rn.f32x2 per pair of ex2 (K2 = 0 gives the ex2 rate
 // with its operand arithmetic alone, K2 = 4 the scan core's ratio), so the
 // caller can see how far the two pipes overlap.
-template <int K2>
+// NE = false drops the ex2 (and their operand FMAs): the FMA work alone.
+// SCALAR: 2*K2 scalar fma.rn.f32 instead of K2 packed ones (the same FLOPs).
+template <int K2, bool NE = true, bool SCALAR = false>
 __global__ void k_mufu_fma(float* sink, int64_t iters) {
-    float e[8];
+    float e[8], g[16];
     unsigned long long f[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         e[i] = -0.1f * (i + 1) - 1e-7f * threadIdx.x;
         f[i] = pk2(0.5f + 0.01f * i, 0.3f);
     }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) g[i] = 0.5f + 0.01f * i;
     const unsigned long long a = pk2(0.9999f, 0.9998f), b = pk2(1e-4f, 2e-4f);
     for (int64_t it = 0; it < iters; ++it) {
 #pragma unroll
         for (int i = 0; i < 8; i += 2) {
-            e[i] = ex2_f(-e[i] * 0.5f - 0.01f);
-            e[i + 1] = ex2_f(-e[i + 1] * 0.5f - 0.01f);
+            if constexpr (NE) {
+                e[i] = ex2_f(-e[i] * 0.5f - 0.01f);
+                e[i + 1] = ex2_f(-e[i + 1] * 0.5f - 0.01f);
+            }
+            if constexpr (SCALAR) {
 #pragma unroll
-            for (int k = 0; k < K2; ++k) f[(i + k) & 7] = fma2(f[(i + k) & 7], a, b);
+                for (int k = 0; k < 2 * K2; ++k) {
+                    float& x = g[(2 * i + k) & 15];
+                    asm volatile("fma.rn.f32 %0, %0, %1, %2;" : "+f"(x) : "f"(0.9999f), "f"(1e-4f));
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < K2; ++k) f[(i + k) & 7] = fma2(f[(i + k) & 7], a, b);
+            }
         }
     }
     float s = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) s += e[i] + lo2(f[i]) + hi2(f[i]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s += g[i];
     if (s == 1234.5f) sink[0] = s;
 }
 
@@ -229,6 +245,28 @@ int msc_peak_mufu_fma(float* sink, int blocks, int threads, int64_t iters, int k
     if (k2 == 4) return timed(s, ms, [&] { k_mufu_fma<4><<<blocks, threads, 0, s>>>(sink, iters); });
     if (k2 == 2) return timed(s, ms, [&] { k_mufu_fma<2><<<blocks, threads, 0, s>>>(sink, iters); });
     return timed(s, ms, [&] { k_mufu_fma<0><<<blocks, threads, 0, s>>>(sink, iters); });
+}
+
+// The same loop in five mixes (per pair of ex2, with their two operand
+// FMAs): 0 ex2 alone, 1 + 2 packed FMAs, 2 + 4 packed FMAs, 3 + 8 scalar
+// FMAs, 4 the 4 packed FMAs without the ex2.  Iterations of 4 such groups per
+// thread; time in ms.
+int msc_peak_mix(float* sink, int blocks, int threads, int64_t iters, int mix,
+                 cudaStream_t s, float* ms) {
+    switch (mix) {
+        case 0: return timed(s, ms, [&] { k_mufu_fma<0><<<blocks, threads, 0, s>>>(sink, iters); });
+        case 1: return timed(s, ms, [&] { k_mufu_fma<2><<<blocks, threads, 0, s>>>(sink, iters); });
+        case 2: return timed(s, ms, [&] { k_mufu_fma<4><<<blocks, threads, 0, s>>>(sink, iters); });
+        case 3:
+            return timed(s, ms, [&] {
+                k_mufu_fma<4, true, true><<<blocks, threads, 0, s>>>(sink, iters);
+            });
+        case 4:
+            return timed(s, ms, [&] {
+                k_mufu_fma<4, false><<<blocks, threads, 0, s>>>(sink, iters);
+            });
+        default: return 1;
+    }
 }
 
 // bytes moved = 2 * n16 * 16 (read + write); n16 = number of 16-byte words.
