@@ -99,7 +99,9 @@ cudaError_t launch_conv1d_update(const ConvArgs& a, msc_dtype dtype, cudaStream_
 // Backward pass of the scan.  Element-load path (scan_bwd.cu): ckpt is
 // (batch, nseg - 1, d_inner, N) fp32, the states entering segments
 // 1 .. nseg-1 of the recompute; segment 0 starts from h0 (or zero).  TMA path
-// (scan_tma.cu): ckpt is the kernel's own scratch, nseg its tile count.
+// (scan_tma.cu): ckpt is (batch, nseg, d_inner, N) fp32, row k the state
+// entering tile k, nseg the tile count -- the kernel's own scratch, or with
+// ext_ckpt the rows a checkpointing forward scan wrote (read only).
 struct BwdArgs {
     const void* u;
     const void* dt;

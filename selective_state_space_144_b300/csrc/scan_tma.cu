@@ -788,8 +788,10 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
 // the CTA makes one pass of 2*nt - 1 rounds over them through a TMA ring of
 // S stages:
 //   * forward rounds, tiles 0 .. nt-2 (u, dt, B loaded): the recurrence from
-//     h0 (or zero), the state entering each next tile stored to the CTA's
-//     own checkpoint rows in global memory (they stay in L2);
+//     h0 (or zero), the state entering each next tile stored to the
+//     checkpoint rows (batch, tile, d_inner, N) in global memory (they stay
+//     in L2) -- skipped when a.ext_ckpt says the forward scan wrote those
+//     rows already, the pass then starting at the last tile;
 //   * reverse rounds, tiles nt-1 .. 0 (u, dt, z, dout, B, C loaded):
 //       1. a tile prologue: every lane computes the per-(step, channel)
 //          scalars for TT/4 of the tile's (step, channel) pairs -- delta,
