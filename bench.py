@@ -489,6 +489,9 @@ def run_ours(args):
     # issue bound: one warp instruction per clock per SM sub-partition; the
     # FP32 FFMA rate measured above is that rate times 32 lanes
     issue_peak = ffma_peak / 32.0
+    packed = recorded_traffic("scan_tma_kernel", MAIN,
+                              field="packed_fp32x2_warp_instructions_per_launch")
+    mufu_inst = recorded_traffic("scan_tma_kernel", MAIN, field="mufu_warp_instructions_per_launch")
     issue = None
     if inst:
         issue = {"warp_instructions_per_launch": inst,
@@ -498,6 +501,13 @@ def run_ours(args):
                  "frac": (inst / issue_peak) / (scan_ms * 1e-3),
                  "source": "warp instructions from an ncu capture of this kernel source "
                            "(profiles/traffic.json); issue rate = measured FFMA rate / 32"}
+        if packed and mufu_inst:
+            # a packed fp32x2 instruction and an ex2 each hold a sub-partition's
+            # dispatch for two cycles (msc_peak_mix), every other instruction one
+            disp = inst + packed + mufu_inst
+            issue["dispatch_cycles_per_launch"] = disp
+            issue["dispatch_bound_ms"] = disp / issue_peak * 1e3
+            issue["dispatch_frac"] = (disp / issue_peak) / (scan_ms * 1e-3)
     roofline = {
         "bound": "alu", "kernel": "scan_tma_kernel (output pass)",
         "achieved": achieved_mufu / 1e12, "peak": ex2_peak / 1e12,
