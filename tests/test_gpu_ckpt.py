@@ -208,3 +208,21 @@ def test_ckpt_empty_and_single_step():
     g_ck, g_re, _, _ = bwd_pair(x1, h0, seed=32)
     for k in ("du", "ddt", "dz", "dh0"):
         assert torch.equal(g_ck[k], g_re[k]), k
+
+
+@pytest.mark.parametrize("d_state", [8, 16, 32])
+def test_ckpt_rows_two_lanes_per_channel(d_state):
+    """The TMA kernels with two lanes per channel (more states per lane)
+    write the same checkpoint layout."""
+    x = synth.scan_inputs(2, 100, 64, d_state, dtype="bf16", seed=1700 + d_state,
+                          D="normal", A_kind="random")
+    h0 = np.random.default_rng(d_state).standard_normal((2, 64, d_state)).astype(np.float32)
+    msc.tuning_set("scan_lanes", 2)
+    try:
+        _, _, (out, last, ck), (out0, last0) = fwd_ckpt(x, h0)
+    finally:
+        msc.tuning_set("scan_lanes", 0)
+    assert torch.equal(out, out0) and torch.equal(last, last0)
+    interval, _ = msc.scan_checkpoint_size(2, 100, 64, d_state)
+    e = rel_l2(from_device(ck), oracle_ckpt_rows(x, h0, interval))
+    assert e <= TOL["bf16"], f"checkpoint rows rel-L2 {e:.3e}"
