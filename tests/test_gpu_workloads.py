@@ -135,3 +135,48 @@ def test_backward_workload_whole_tensors():
     for k in ("dA", "dB", "dC", "dD", "ddt_bias", "dh0"):
         e = rel_l2(got[k], ref[k])
         assert e <= 2e-5, f"{k} rel-L2 {e:.3e}"
+
+
+def test_bench_step_graph_replay_bitwise():
+    """The bench's timed step -- the 130M-like layer's scan with a caller
+    workspace, then one decode token from its last state -- replayed from a
+    CUDA graph gives the eager step's outputs bit for bit (so the graph-timed
+    launches compute what the whole-tensor test above checked)."""
+    x = synth.workload_inputs("mamba130m_layer")
+    a = scan_device_args(x)
+    batch, L, d_inner = x.u.shape
+    N = x.B.shape[-1]
+    tok = synth.decode_step(batch, d_inner, N, 0, seed=11)
+    t = {k: to_device(getattr(tok, k), "bf16") for k in ("u", "dt_raw", "z", "B", "C")}
+    nws = msc.scan_workspace_size(batch, L, d_inner, N, torch.bfloat16)
+    wsp = torch.empty(max(nws, 1), dtype=torch.uint8, device="cuda")
+    out = torch.empty(batch, L, d_inner, dtype=torch.bfloat16, device="cuda")
+    last = torch.empty(batch, d_inner, N, device="cuda")
+    tout = torch.empty(batch, d_inner, dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        msc.selective_scan_fwd_ws(**a, out=out, last_state=last, workspace=wsp)
+        msc.selective_state_update(last, t["u"], t["dt_raw"], a["A"], t["B"], t["C"], a["D"],
+                                   t["z"], a["dt_bias"], out=tout)
+
+    step()
+    torch.cuda.synchronize()
+    ref = (out.clone(), last.clone(), tout.clone())
+    for buf in (out, last, tout):
+        buf.fill_(float("nan"))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for buf in (out, last, tout):
+        buf.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    for got, want in zip((out, last, tout), ref):
+        assert torch.equal(got.view(torch.int16) if got.dtype == torch.bfloat16 else got,
+                           want.view(torch.int16) if want.dtype == torch.bfloat16 else want)
