@@ -1017,7 +1017,47 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
     def dstep(k):
         uu, dd, zz, BB, CC = pool[k % 8]
         msc.selective_state_update(state, uu, dd, A, BB, CC, Dv, zz, bias, out=out)
-    b2b_ms = back_to_back_ms(dstep, steps)   # no event pairs between the launches
+    # the workload as defined: `steps` sequential tokens, each with its own
+    # inputs pre-staged on the device (7.9 GB for 1000 tokens, drawn from a
+    # seeded device generator with the workload's distributions), the state
+    # updated in place; the steps are replayed from one CUDA graph, so the
+    # timed region holds the kernels back to back and no host work
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w["seed"])
+
+    def draw(shape, scale=1.0):
+        return (torch.randn(shape, generator=gen, device=dev) * scale).to(torch.bfloat16)
+
+    Us, Zs = draw((steps, Bb, Dd)), draw((steps, Bb, Dd))
+    Ts = draw((steps, Bb, Dd), 0.5)
+    Bs, Cs = draw((steps, Bb, Nn)), draw((steps, Bb, Nn))
+
+    def gstep(k):
+        msc.selective_state_update(state, Us[k], Ts[k], A, Bs[k], Cs[k], Dv, Zs[k], bias,
+                                   out=out)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for k in range(3):
+            gstep(k)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    dgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(dgraph):
+        for k in range(steps):
+            gstep(k)
+    dgraph.replay()
+    torch.cuda.synchronize(dev)
+    flush()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    dgraph.replay()
+    e1.record()
+    e1.synchronize()
+    b2b_ms = e0.elapsed_time(e1) / steps
+    del dgraph, Us, Zs, Ts, Bs, Cs
+    torch.cuda.empty_cache()
     cold_ms = hook_cold_ms(dstep, "update")
     byt = 2 * Bb * Dd * Nn * 4 + 4 * Bb * Dd * 2 + 2 * Bb * Nn * 2 + Dd * Nn * 4 + 2 * Dd * 4
     upd = Bb * Dd * Nn
@@ -1029,8 +1069,10 @@ def run_extras(torch, msc, dev, ex2_peak, peaks):
         "hbm_frac_l2_flushed": (byt / (cold_ms * 1e-3)) / (peaks["hbm_gbs"] * 1e9),
         "hbm_frac_back_to_back": (byt / (b2b_ms * 1e-3)) / (peaks["hbm_gbs"] * 1e9),
         "algorithmic_bytes_per_step": byt,
-        "note": ("back-to-back steps keep part of the 84 MB state in the "
-                 "126 MB L2; the flushed figure is the cold-cache bound"),
+        "note": ("back to back: the workload's 1000 tokens with distinct pre-staged inputs, "
+                 "replayed from one CUDA graph (part of the 84 MB state stays in the "
+                 "126 MB L2 from token to token); l2_flushed: one token after a 512 MiB "
+                 "read, the cold-cache bound"),
     }
     # the same step with the zero-order-hold input and with the exponential
     # trapezoid (lambda ~ U[0, 1]; the previous token's u and B from the pool)
