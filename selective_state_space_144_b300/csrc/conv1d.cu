@@ -187,6 +187,47 @@ conv1d_update_kernel(T* __restrict__ state, const T* __restrict__ x,
     if (H > 0) Elem<T>::store(state + i * H + (H > 0 ? H - 1 : 0), cur);
 }
 
+// Decode, batch rows per thread: a thread owns channel d of kUpdRows
+// consecutive batch rows, so its weights and bias are loaded once and the
+// rows' state and input loads (independent of one another) are all in
+// flight together.  The same operations per (row, channel) as above.
+constexpr int kUpdRows = 8;
+template <typename T, int KC>
+__global__ void __launch_bounds__(256)
+conv1d_update_rows_kernel(T* __restrict__ state, const T* __restrict__ x,
+                          const float* __restrict__ w, const float* __restrict__ bias,
+                          T* __restrict__ out, int64_t batch, int64_t d_inner, int silu_on) {
+    constexpr int H = KC - 1;
+    const int64_t d = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (d >= d_inner) return;
+    const int64_t b0 = (int64_t)blockIdx.y * kUpdRows;
+    float wk[KC];
+#pragma unroll
+    for (int k = 0; k < KC; ++k) wk[k] = __ldg(w + d * KC + k);
+    const float bs = bias ? __ldg(bias + d) : 0.0f;
+    float st[kUpdRows][H > 0 ? H : 1], cur[kUpdRows];
+#pragma unroll
+    for (int r = 0; r < kUpdRows; ++r) {
+        const int64_t i = (b0 + r < batch ? b0 + r : batch - 1) * d_inner + d;
+#pragma unroll
+        for (int k = 0; k < H; ++k) st[r][k] = to_f32(state[i * H + k]);
+        cur[r] = Elem<T>::load(x + i);
+    }
+#pragma unroll
+    for (int r = 0; r < kUpdRows; ++r) {
+        if (b0 + r >= batch) break;
+        const int64_t i = (b0 + r) * d_inner + d;
+        float acc = bs;
+#pragma unroll
+        for (int k = 0; k < H; ++k) acc = fmaf(wk[k], st[r][k], acc);
+        acc = fmaf(wk[H], cur[r], acc);
+        Elem<T>::store(out + i, silu_on ? silu_rcp(acc) : acc);  // same rounding as the prefill
+#pragma unroll
+        for (int k = 0; k + 1 < H; ++k) Elem<T>::store(state + i * H + k, st[r][k + 1]);
+        if (H > 0) Elem<T>::store(state + i * H + (H > 0 ? H - 1 : 0), cur[r]);
+    }
+}
+
 template <typename T, int V, int KC>
 static cudaError_t launch_conv_v(const ConvArgs& a, cudaStream_t s) {
     const int64_t groups = (a.d_inner + (int64_t)kConvThreads * V - 1) / ((int64_t)kConvThreads * V);
@@ -211,9 +252,17 @@ template <typename T, int KC>
 static cudaError_t launch_update_k(const ConvArgs& a, cudaStream_t s) {
     const int64_t n = a.batch * a.d_inner;
     const ProfileMark m = profile_begin(s, MSC_PROF_CONV_UPDATE);
-    conv1d_update_kernel<T, KC><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
-        static_cast<T*>(a.state_out), static_cast<const T*>(a.x), a.w, a.bias,
-        static_cast<T*>(a.out), n, a.d_inner, a.silu);
+    const int64_t rgroups = (a.batch + kUpdRows - 1) / kUpdRows;
+    if (a.batch >= kUpdRows && rgroups <= 65535) {
+        const dim3 grid((unsigned)((a.d_inner + 255) / 256), (unsigned)rgroups);
+        conv1d_update_rows_kernel<T, KC><<<grid, 256, 0, s>>>(
+            static_cast<T*>(a.state_out), static_cast<const T*>(a.x), a.w, a.bias,
+            static_cast<T*>(a.out), a.batch, a.d_inner, a.silu);
+    } else {
+        conv1d_update_kernel<T, KC><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
+            static_cast<T*>(a.state_out), static_cast<const T*>(a.x), a.w, a.bias,
+            static_cast<T*>(a.out), n, a.d_inner, a.silu);
+    }
     profile_end(m, s);
     return cudaGetLastError();
 }

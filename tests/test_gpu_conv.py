@@ -100,9 +100,12 @@ def test_conv_split_prefill(dtype):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("d_conv", [1, 2, 4, 6])
-def test_conv_update(dtype, d_conv):
-    """Decode tokens against the oracle, and decode == prefill."""
-    batch, L, d_inner = 3, 9, 96
+@pytest.mark.parametrize("batch,d_inner", [(3, 96), (13, 300), (16, 64)])
+def test_conv_update(dtype, d_conv, batch, d_inner):
+    """Decode tokens against the oracle, and decode == prefill (batch 3: a
+    thread per (row, channel); 13 and 16: 8 batch rows per thread, the last
+    group partial for 13, a ragged channel block for 300)."""
+    L = 9
     x, w, bias, st = conv_case(batch, L, d_inner, d_conv, dtype, seed=200 + d_conv,
                                with_state=True)
     y_pre, st_pre = run_conv(x, w, bias, st, dtype)
