@@ -79,22 +79,30 @@ def test_starved_waits_report_timeout_and_context_survives(chunks):
     assert rel_l2(from_device(last), s_ref) <= TOL["bf16"]
 
 
-def test_starved_decode_reports_timeout_and_context_survives():
-    """The streaming decode kernel (d_state 16, aligned arrays): its waits run
-    out with no copy issued; the state is left untouched; a normal step
-    afterwards matches the oracle."""
+@pytest.mark.parametrize("disc", ["euler", "zoh", "trapezoid"])
+def test_starved_decode_reports_timeout_and_context_survives(disc):
+    """The streaming decode kernel (d_state 16, aligned arrays; every
+    discretisation it takes): its waits run out with no copy issued; the
+    state is left untouched; a normal step afterwards matches the oracle."""
     batch, d_inner, N = 2, 256, 16
     p = synth.decode_params(batch, d_inner, N)
     s = synth.decode_step(batch, d_inner, N, 0)
     lib = msc.load()
     dev = {k: to_device(getattr(s, k), "bf16") for k in ("u", "dt_raw", "z", "B", "C")}
     A, D, bias = (to_device(p.A, "f32"), to_device(p.D, "f32"), to_device(p.dt_bias, "f32"))
+    lam = synth.round_bf16(np.random.default_rng(5).uniform(0, 1, (batch, d_inner))
+                           .astype(np.float32))
+    lam_d = to_device(lam, "bf16")
     state = torch.from_numpy(p.state0).cuda()
     out = torch.full((batch, d_inner), float("nan"), dtype=torch.bfloat16, device="cuda")
 
     def step():
-        msc.selective_state_update(state, dev["u"], dev["dt_raw"], A, dev["B"], dev["C"],
-                                   D, dev["z"], bias, out=out)
+        if disc == "trapezoid":
+            msc.selective_state_update_trap(state, None, None, dev["u"], dev["dt_raw"], lam_d,
+                                            A, dev["B"], dev["C"], D, dev["z"], bias, out=out)
+        else:
+            msc.selective_state_update(state, dev["u"], dev["dt_raw"], A, dev["B"], dev["C"],
+                                       D, dev["z"], bias, out=out, zoh=disc == "zoh")
         torch.cuda.synchronize()
 
     msc.tuning_set("debug_starve_copies", 64)
@@ -107,7 +115,11 @@ def test_starved_decode_reports_timeout_and_context_survives():
     msc.tuning_set("debug_starve_copies", 0)
     step()
     assert lib.msc_check_device_error(0) == 0
-    ref_state, ref_out = oracle.state_update(p.state0, s.u, s.dt_raw, p.A, s.B, s.C, p.D,
-                                             s.z, p.dt_bias)
+    if disc == "trapezoid":
+        ref_state, ref_out = oracle.state_update_trap(p.state0, None, None, s.u, s.dt_raw, lam,
+                                                      p.A, s.B, s.C, p.D, s.z, p.dt_bias)
+    else:
+        ref_state, ref_out = oracle.state_update(p.state0, s.u, s.dt_raw, p.A, s.B, s.C, p.D,
+                                                 s.z, p.dt_bias, zoh=disc == "zoh")
     assert rel_l2(from_device(out), as_stored(ref_out, "bf16")) <= TOL["bf16"]
     assert rel_l2(from_device(state), ref_state) <= TOL["bf16"]
