@@ -21,7 +21,7 @@ import ctypes
 import os
 
 __all__ = [
-    "MscError", "selective_scan_fwd", "selective_scan_fwd_ws",
+    "MscError", "selective_scan", "selective_scan_fwd", "selective_scan_fwd_ws",
     "selective_scan_fwd_ckpt", "scan_checkpoint_size", "selective_scan_bwd",
     "selective_scan_trap_fwd", "selective_state_update_trap",
     "causal_conv1d_fwd", "causal_conv1d_update",
@@ -440,6 +440,63 @@ def selective_scan_bwd(u, dt, A, B, C, D=None, z=None, dt_bias=None, h0=None,
         batch, L, d_inner, d_state, code, _stream(dev))
     _check(fn, st)
     return g
+
+
+_SCAN_FN = None
+
+
+def _scan_function():
+    """The autograd Function of selective_scan (defined on first use, since
+    torch is imported lazily)."""
+    global _SCAN_FN
+    if _SCAN_FN is not None:
+        return _SCAN_FN
+    torch = _torch()
+
+    class SelectiveScanFn(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, u, dt, A, B, C, D, z, dt_bias, h0):
+            ck = None
+            try:  # the forward that also writes the backward's checkpoints
+                out, last, ck = selective_scan_fwd_ckpt(u, dt, A, B, C, D, z, dt_bias, h0=h0)
+            except MscError as e:
+                if e.status != 2:  # only unsupported shapes take the plain forward
+                    raise
+                out, last = selective_scan_fwd(u, dt, A, B, C, D, z, dt_bias, h0=h0)
+            ctx.save_for_backward(u, dt, A, B, C, D, z, dt_bias, h0, ck)
+            return out, last
+
+        @staticmethod
+        def backward(ctx, dout, dlast):
+            u, dt, A, B, C, D, z, dt_bias, h0, ck = ctx.saved_tensors
+            dout = (torch.zeros_like(u) if dout is None
+                    else dout.to(u.dtype).contiguous())
+            dlast = None if dlast is None else dlast.float().contiguous()
+            want_dh0 = h0 is not None and ctx.needs_input_grad[8]
+            try:
+                g = selective_scan_bwd(u, dt, A, B, C, D, z, dt_bias, h0=h0, dout=dout,
+                                       dlast_state=dlast, want_dh0=want_dh0, ckpt=ck)
+            except MscError as e:
+                if ck is None or e.status != 2:
+                    raise
+                g = selective_scan_bwd(u, dt, A, B, C, D, z, dt_bias, h0=h0, dout=dout,
+                                       dlast_state=dlast, want_dh0=want_dh0)
+            return (g["du"], g["ddt"], g["dA"], g["dB"].to(B.dtype), g["dC"].to(C.dtype),
+                    g["dD"], g["dz"], g["ddt_bias"], g["dh0"])
+
+    _SCAN_FN = SelectiveScanFn
+    return _SCAN_FN
+
+
+def selective_scan(u, dt, A, B, C, D=None, z=None, dt_bias=None, h0=None):
+    """Differentiable selective scan (the Euler form) -> (out, last_state).
+
+    Forward: selective_scan_fwd_ckpt where the shape allows (the state
+    entering every backward tile is kept for the backward), else
+    selective_scan_fwd.  Backward: selective_scan_bwd from those
+    checkpoints (or recomputing them).  Gradients of B and C are cast to
+    their storage dtype; the others keep the dtypes of selective_scan_bwd."""
+    return _scan_function().apply(u, dt, A, B, C, D, z, dt_bias, h0)
 
 
 def causal_conv1d_fwd(x, w, bias=None, state_in=None, out=None, state_out=None,

@@ -226,3 +226,45 @@ def test_ckpt_rows_two_lanes_per_channel(d_state):
     interval, _ = msc.scan_checkpoint_size(2, 100, 64, d_state)
     e = rel_l2(from_device(ck), oracle_ckpt_rows(x, h0, interval))
     assert e <= TOL["bf16"], f"checkpoint rows rel-L2 {e:.3e}"
+
+
+@pytest.mark.parametrize("d_inner", [64, 12])
+def test_autograd_selective_scan_matches_direct_calls(d_inner):
+    """selective_scan under torch autograd: the forward and the gradients
+    equal the direct calls bit for bit (d_inner 64: checkpoints kept by the
+    forward; 12: no TMA kernels, the plain forward and the recomputing
+    backward)."""
+    x = synth.scan_inputs(2, 70, d_inner, 16, dtype="bf16", seed=1800 + d_inner, D="normal")
+    a = scan_device_args(x)
+    h0 = to_device(np.random.default_rng(41).standard_normal((2, d_inner, 16))
+                   .astype(np.float32), "f32")
+    leaves = {k: a[k].clone().requires_grad_(True) for k in a}
+    h0l = h0.clone().requires_grad_(True)
+    rng = np.random.default_rng(42)
+    W = to_device(synth.round_bf16(rng.standard_normal(x.u.shape).astype(np.float32)), "bf16")
+    V = to_device(rng.standard_normal((2, d_inner, 16)).astype(np.float32), "f32")
+    msc.tuning_set("scan_chunks", 1)  # one time chunk: checkpoint rows = recomputed states
+    try:
+        out, last = msc.selective_scan(leaves["u"], leaves["dt"], leaves["A"], leaves["B"],
+                                       leaves["C"], leaves["D"], leaves["z"],
+                                       leaves["dt_bias"], h0=h0l)
+        loss = (out.float() * W.float()).sum() + (last * V).sum()
+        loss.backward()
+        out0, last0 = msc.selective_scan_fwd(a["u"], a["dt"], a["A"], a["B"], a["C"], a["D"],
+                                             a["z"], a["dt_bias"], h0=h0)
+    finally:
+        msc.tuning_set("scan_chunks", 0)
+    # d loss / d out, as autograd hands it over: W in fp32, rounded to out's dtype
+    g = msc.selective_scan_bwd(a["u"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                               a["dt_bias"], h0=h0, dout=W, dlast_state=V, want_dh0=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out0) and torch.equal(last, last0)
+    for k, name in (("du", "u"), ("ddt", "dt"), ("dz", "z")):
+        assert torch.equal(leaves[name].grad, g[k]), k
+    assert torch.equal(h0l.grad, g["dh0"])
+    for k, name in (("dA", "A"), ("dD", "D"), ("ddt_bias", "dt_bias")):
+        e = rel_l2(from_device(leaves[name].grad), from_device(g[k]).astype(np.float64))
+        assert e <= 1e-6, f"{k} rel-L2 {e:.3e}"
+    for k, name in (("dB", "B"), ("dC", "C")):
+        e = rel_l2(from_device(leaves[name].grad), from_device(g[k].to(torch.bfloat16)))
+        assert e <= 1e-2, f"{k} rel-L2 {e:.3e}"   # bf16 gradients of bf16 inputs
