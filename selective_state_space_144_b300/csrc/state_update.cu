@@ -181,32 +181,34 @@ state_update_row_kernel(UpdateArgs a) {
 // Set (bit 0) by a decode kernel whose bounded wait for a copy gave up.
 __device__ unsigned int g_update_error;
 
-// Decode step for N = 16 with the state streamed by the copy engine.  A CTA
-// owns one tile of kStreamCh channels of every R-th batch row (rows r, r+R,
-// ...) and walks those tiles through a ring of SS shared-memory stages: one
-// thread issues 1-D bulk copies of each tile's state rows (8 KB), u, dt, z
-// (kStreamCh elements each) and the row's B, C into a stage, completing the
-// stage's mbarrier, AHEAD tiles ahead; the CTA updates the states in place
-// in shared memory and the same thread copies the tile's state back with a
-// bulk store.  So the HBM stream is kept in flight by the
-// copy engine rather than by the threads' registers, and A, dt_bias and D
-// of the CTA's channels are read once per CTA.  Work split inside a tile:
-// thread t owns the float4 of states (t % 4) of channels t / 4, 32 + t / 4,
-// 64 + t / 4, 96 + t / 4, so every shared access of a warp is 512
-// contiguous bytes; the four partial C.h of a channel are summed with two
-// shuffles.
-constexpr int kStreamCh = 128;
+// Decode step with the state streamed by the copy engine (N = 16, 32, 64).  A CTA owns one tile of CH = 2048 / N channels (8 KB of state) of
+// every R-th batch row (rows r, r+R, ...) and walks those tiles through a
+// ring of SS shared-memory stages: one thread issues 1-D bulk copies of each
+// tile's state rows, u, dt, z (CH elements each) and the row's B, C into a
+// stage, completing the stage's mbarrier, AHEAD tiles ahead; the CTA updates
+// the states in place in shared memory and the same thread copies the
+// tile's state back with a bulk store.  So the HBM stream is kept in flight
+// by the copy engine rather than by the threads' registers, and A, dt_bias
+// and D of the CTA's channels are read once per CTA.  Work split inside a
+// tile: TPC = N / 4 threads per channel, thread t owning the float4 of
+// states (t % TPC) of channels t / TPC + k * (128 / TPC), k = 0..3, so every
+// shared access of a warp is 512 contiguous bytes; the TPC partial C.h of a
+// channel are summed with log2(TPC) shuffles.
 constexpr int kStreamThreads = 128;
 
 // SS stages; the tile AHEAD steps ahead is loaded while one is updated and
 // the store of an earlier one (SS - AHEAD stages) may still read its stage.
 // TRAP: the exponential trapezoid's lambda and previous-token u (kX each)
 // and B row follow the C row.
-template <typename T, int SS, bool TRAP = false>
+// A tile is CH = 2048 / N channels (8 KB of state); a channel's N states
+// are N/4 threads' float4s.
+template <typename T, int N_, int SS, bool TRAP = false>
 struct StreamLayout {
-    static constexpr int N = 16;
-    static constexpr int kState = kStreamCh * N * 4;                    // 8192
-    static constexpr int kX = kStreamCh * (int)sizeof(T);               // u / dt / z
+    static constexpr int N = N_;
+    static constexpr int CH = 2048 / N;                                 // channels per tile
+    static constexpr int TPC = N / 4;                                   // threads per channel
+    static constexpr int kState = CH * N * 4;                           // 8192
+    static constexpr int kX = CH * (int)sizeof(T);                      // u / dt / z
     static constexpr int kBC = N * (int)sizeof(T);                      // B / C row
     static constexpr int kBCa = ((kBC + 15) / 16) * 16;
     static constexpr int kU = kState, kDt = kU + kX, kZ = kDt + kX;
@@ -218,22 +220,25 @@ struct StreamLayout {
     static constexpr int kTotal = kBar + SS * 8;
 };
 
-template <typename T, int SS, int AHEAD, int DISC>
+template <typename T, int N_, int SS, int AHEAD, int DISC>
 __global__ void __launch_bounds__(kStreamThreads)
 state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
     static_assert(AHEAD >= 1 && AHEAD <= SS - 2, "a stage for the update and one for a store");
     constexpr int kStreamStages = SS;
     constexpr int kStreamAhead = AHEAD;
     constexpr bool ZOH = DISC == 1, TRAP = DISC == 2;
-    using Lay = StreamLayout<T, SS, TRAP>;
+    using Lay = StreamLayout<T, N_, SS, TRAP>;
     constexpr int N = Lay::N;
+    constexpr int CH = Lay::CH, TPC = Lay::TPC;
+    constexpr int CPP = kStreamThreads / TPC;  // channels per pass of the CTA's threads
+    static_assert(CH == 4 * CPP, "four passes cover a tile");
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x;
-    const int q = tid & 3;
+    const int q = tid % TPC;
     const int j = blockIdx.x % nJ;
     const int r = blockIdx.x / nJ;
-    const int64_t c0 = (int64_t)j * kStreamCh;
-    const int nch = (int)min((int64_t)kStreamCh, a.d_inner - c0);
+    const int64_t c0 = (int64_t)j * CH;
+    const int nch = (int)min((int64_t)CH, a.d_inner - c0);
     const int nt = r < a.batch ? (int)((a.batch - 1 - r) / R + 1) : 0;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + Lay::kBar;
@@ -283,7 +288,7 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
     bool valid[4];
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
-        const int cl = it * 32 + (tid >> 2);
+        const int cl = it * CPP + tid / TPC;
         valid[it] = cl < nch;
         const int64_t d = c0 + (valid[it] ? cl : 0);
         const float4 av = __ldg(reinterpret_cast<const float4*>(a.A + d * N) + q);
@@ -328,7 +333,7 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
         T* outp = static_cast<T*>(a.out) + b * a.d_inner + c0;
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
-            const int cl = it * 32 + (tid >> 2);
+            const int cl = it * CPP + tid / TPC;
             float4* hp = reinterpret_cast<float4*>(sp) + it * kStreamThreads + tid;
             float4 h = *hp;
             const float uu = lds_scalar<T>(su + cl);
@@ -359,8 +364,8 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
                 y = fmaf(Cv[k], hv[k], y);
             }
             *hp = make_float4(hv[0], hv[1], hv[2], hv[3]);
-            y += __shfl_xor_sync(0xffffffffu, y, 1);
-            y += __shfl_xor_sync(0xffffffffu, y, 2);
+#pragma unroll
+            for (int o = 1; o < TPC; o <<= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
             if (q == 0 && valid[it]) {
                 y = fmaf(Dd[it], uu, y);
                 if (a.z) y *= silu(lds_scalar<T>(sz + cl));
@@ -389,22 +394,25 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
 
 bool stream_update_supported(const UpdateArgs& a, size_t es) {
     auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-    return a.N == 16 && (a.d_inner * (int64_t)es) % 16 == 0 && al16(a.state) && al16(a.A) &&
+    // d_state 8 measured no faster than the thread-per-channel kernel (22.7
+    // against 21.8 us on 256 x 5120): its state is small next to the inputs
+    return (a.N == 16 || a.N == 32 || a.N == 64) &&
+           (a.d_inner * (int64_t)es) % 16 == 0 && al16(a.state) && al16(a.A) &&
            al16(a.u) && al16(a.dt) && al16(a.B) && al16(a.C) && (!a.z || al16(a.z)) &&
            (!a.trap || (al16(a.lam) && (!a.u_prev || al16(a.u_prev)) &&
                         (!a.B_prev || al16(a.B_prev))));
 }
 
-template <typename T, int SS, int AHEAD, int DISC>
+template <typename T, int N, int SS, int AHEAD, int DISC>
 static cudaError_t launch_stream_s(const UpdateArgs& a, int ctas_per_sm, cudaStream_t s) {
-    using Lay = StreamLayout<T, SS, DISC == 2>;
-    const int nJ = (int)((a.d_inner + kStreamCh - 1) / kStreamCh);
+    using Lay = StreamLayout<T, N, SS, DISC == 2>;
+    const int nJ = (int)((a.d_inner + Lay::CH - 1) / Lay::CH);
     const int64_t target = (int64_t)a.sms * ctas_per_sm;
     int64_t R = target / nJ;
     R = R < 1 ? 1 : (R > a.batch ? a.batch : R);
     const int64_t grid = (int64_t)nJ * R;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-    auto kern = state_update_stream_kernel<T, SS, AHEAD, DISC>;
+    auto kern = state_update_stream_kernel<T, N, SS, AHEAD, DISC>;
     if (Lay::kTotal > 48 * 1024)
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kTotal);
     kern<<<(unsigned)grid, kStreamThreads, Lay::kTotal, s>>>(a, nJ, (int)R, a.wait_limit);
@@ -415,14 +423,23 @@ static cudaError_t launch_stream_s(const UpdateArgs& a, int ctas_per_sm, cudaStr
 // memory each): measured on the 256 x 5120 x 16 step, 28.6 us with a cold
 // L2 against 45.1 us for six stages four ahead at three CTAs per SM -- many
 // small CTAs keep more tiles in flight than a few deep rings.
-template <typename T>
-static cudaError_t launch_stream(const UpdateArgs& a, cudaStream_t s) {
-    if (a.trap) return launch_stream_s<T, 3, 1, 2>(a, 8, s);
+template <typename T, int N>
+static cudaError_t launch_stream_n(const UpdateArgs& a, cudaStream_t s) {
+    if (a.trap) return launch_stream_s<T, N, 3, 1, 2>(a, 8, s);
     // zero-order hold: more arithmetic per tile, so a deeper ring (4 stages,
     // 2 ahead, 6 CTAs per SM) measured 36.5-37.0 against 37.8-38.3 us; for the
     // trapezoid (larger stages) it measured 51 against 40 us
-    if (a.zoh) return launch_stream_s<T, 4, 2, 1>(a, 6, s);
-    return launch_stream_s<T, 3, 1, 0>(a, 8, s);
+    if (a.zoh) return launch_stream_s<T, N, 4, 2, 1>(a, 6, s);
+    return launch_stream_s<T, N, 3, 1, 0>(a, 8, s);
+}
+
+template <typename T>
+static cudaError_t launch_stream(const UpdateArgs& a, cudaStream_t s) {
+    switch (a.N) {
+        case 16: return launch_stream_n<T, 16>(a, s);
+        case 32: return launch_stream_n<T, 32>(a, s);
+        default: return launch_stream_n<T, 64>(a, s);
+    }
 }
 
 template <typename T, bool VEC>

@@ -128,14 +128,17 @@ def test_decode_general_kernel_with_unaligned_A():
     assert rel_l2(from_device(state), ref_state) <= TOL["f32"]
 
 
+@pytest.mark.parametrize("N", [8, 16, 32, 64])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("batch,d_inner", [(1, 8), (3, 136), (5, 1000), (7, 264), (40, 640)])
-def test_decode_stream_kernel_shapes(dtype, batch, d_inner):
-    """d_state 16 with aligned arrays takes the copy-engine streaming kernel:
-    partial 128-channel tiles, batch rows spread over CTAs, fp32 and bf16
-    storage.  Four steps against the oracle, and the state bit for bit
-    against the thread-per-channel kernel (the same operations per state)."""
-    N, steps = 16, 4
+def test_decode_stream_kernel_shapes(N, dtype, batch, d_inner):
+    """d_state 16-64 with aligned arrays takes the copy-engine streaming
+    kernel (tiles of 2048/N channels; d_state 8 the thread-per-channel
+    kernel on both paths): partial tiles, batch rows spread over
+    CTAs, fp32 and bf16 storage.  Four steps against the oracle, and the
+    state bit for bit against the thread-per-channel or general kernel (the
+    same operations per state)."""
+    steps = 4
     p = synth.decode_params(batch, d_inner, N, seed=60 + d_inner, dtype=dtype)
     A, D, bias = to_device(p.A, "f32"), to_device(p.D, "f32"), to_device(p.dt_bias, "f32")
     states = {}
@@ -170,13 +173,14 @@ def test_decode_stream_kernel_shapes(dtype, batch, d_inner):
 
 @pytest.mark.parametrize("disc", ["zoh", "trapezoid"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("batch,d_inner", [(3, 136), (5, 1000), (40, 640)])
-def test_decode_stream_kernel_variants(disc, dtype, batch, d_inner):
+@pytest.mark.parametrize("batch,d_inner,N", [(3, 136, 16), (5, 1000, 16), (40, 640, 16),
+                                             (9, 264, 8), (6, 200, 32), (4, 72, 64)])
+def test_decode_stream_kernel_variants(disc, dtype, batch, d_inner, N):
     """The streaming decode kernel with the zero-order-hold input and with
     the exponential trapezoid (lambda, and the previous token's u and B from
     the second step on): four steps against the oracle on both decode
     kernels, and the state bit for bit between them."""
-    N, steps = 16, 4
+    steps = 4
     p = synth.decode_params(batch, d_inner, N, seed=70 + d_inner, dtype=dtype)
     A, D, bias = to_device(p.A, "f32"), to_device(p.D, "f32"), to_device(p.dt_bias, "f32")
     states = {}
