@@ -415,9 +415,10 @@ msc_status msc_scratch_release(void);
  *   "scan_min_chunk" shortest chunk the automatic plan will make (steps)
  *   "scan_path"     0 = automatic, 1 = element-load kernels only (no TMA)
  *   "scan_lanes"    lanes per channel of the TMA kernels: 0 = automatic, 2, 4
- *   "update_path"   0 = automatic (N = 16: the copy-engine streaming decode
- *                   kernel where sizes and alignment allow), 1 = the
- *                   thread-per-channel decode kernels only
+ *   "update_path"   0 = automatic (d_state 16, 32, 64: the copy-engine
+ *                   streaming decode kernel where sizes and alignment
+ *                   allow), 1 = the thread-per-channel and general decode
+ *                   kernels only
  *   "debug_starve_copies"  failure-detection test, 0 (default) = off; n > 0:
  *                   the forward scan's TMA kernels and the streaming decode
  *                   kernel issue none of their data copies and give up each
