@@ -111,15 +111,26 @@ def test_decode_workload_1000_steps():
     assert rel_l2(from_device(state)[:, sel], ref_state) <= TOL["bf16"]
 
 
-def test_backward_workload_whole_tensors():
+@pytest.mark.parametrize("name,from_ckpt", [("mamba130m_layer", False),
+                                            ("mamba130m_layer", True),
+                                            ("mamba2p8b_layer", True)])
+def test_backward_workload_whole_tensors(name, from_ckpt):
     """The backward on the 8 x 2048 x 1536 x 16 layer (the size the bench
-    times): every gradient of every input, whole."""
-    x = synth.workload_inputs("mamba130m_layer")
+    times) and on the 4 x 4096 x 5120 x 16 layer: every gradient of every
+    input, whole -- recomputing its checkpoints, or from the ones the
+    checkpointing forward wrote (the training path)."""
+    x = synth.workload_inputs(name)
     rng = np.random.default_rng(14)
     dout = synth.round_bf16(rng.standard_normal(x.u.shape).astype(np.float32))
     a = scan_device_args(x)
+    ck = None
+    if from_ckpt:
+        ck = msc.selective_scan_fwd_ckpt(a["u"], a["dt"], a["A"], a["B"], a["C"], a["D"],
+                                         a["z"], a["dt_bias"])[2]
     g = msc.selective_scan_bwd(a["u"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["z"],
-                               a["dt_bias"], dout=to_device(dout, "bf16"), want_dh0=True)
+                               a["dt_bias"], dout=to_device(dout, "bf16"), want_dh0=True,
+                               ckpt=ck)
+    del ck
     torch.cuda.synchronize()
     got = {k: (None if v is None else from_device(v)) for k, v in g.items()}
     del a, g
