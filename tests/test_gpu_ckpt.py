@@ -268,3 +268,30 @@ def test_autograd_selective_scan_matches_direct_calls(d_inner):
     for k, name in (("dB", "B"), ("dC", "C")):
         e = rel_l2(from_device(leaves[name].grad), from_device(g[k].to(torch.bfloat16)))
         assert e <= 1e-2, f"{k} rel-L2 {e:.3e}"   # bf16 gradients of bf16 inputs
+
+
+def test_ckpt_forward_with_caller_workspace():
+    """msc_selective_scan_fwd_ckpt with a caller workspace (sized by
+    msc_selective_scan_workspace_size, filled with garbage) gives the same
+    out, last_state and checkpoints as with library scratch."""
+    x = synth.scan_inputs(1, 700, 64, 16, dtype="bf16", seed=1900, D="normal")
+    a = scan_device_args(x)
+    msc.tuning_set("scan_chunks", 3)  # time chunks: the workspace holds their carries
+    try:
+        out0, last0, ck0 = msc.selective_scan_fwd_ckpt(a["u"], a["dt"], a["A"], a["B"], a["C"],
+                                                       a["D"], a["z"], a["dt_bias"])
+        n = msc.scan_workspace_size(1, 700, 64, 16, torch.bfloat16)
+        ws = torch.randint(0, 255, (max(n, 1),), dtype=torch.uint8, device="cuda")
+        out = torch.empty_like(out0)
+        last = torch.empty_like(last0)
+        ck = torch.empty_like(ck0)
+        P = lambda t: None if t is None else t.data_ptr()
+        st = msc.load().msc_selective_scan_fwd_ckpt(
+            P(a["u"]), P(a["dt"]), P(a["A"]), P(a["B"]), P(a["C"]), P(a["D"]), P(a["z"]),
+            P(a["dt_bias"]), None, P(out), P(last), P(ck), 1, 700, 64, 16, 1, P(ws), n,
+            torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+    finally:
+        msc.tuning_set("scan_chunks", 0)
+    assert st == 0
+    assert torch.equal(out, out0) and torch.equal(last, last0) and torch.equal(ck, ck0)
