@@ -583,13 +583,19 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 // state from zero, b = sum_t (prod_{l>t} dA_l) dB_t u_t.  The chunk is walked
 // backwards from its last step (Presentation article, section 3.2: segment
 // summaries merged by the associative combine) with
-//     b += P * dBu_t;   P *= dA_t        (P = prod of the later decays)
-// and the walk stops once every state of every lane of the warp has
+//     b += P * dBu_t,   P = prod_{l>t} dA_l = 2^(A log2(e) * R),
+//     R = sum_{l>t} delta_l   (one scalar per channel, grown by delta_t)
+// -- the product of the later decays is an exponential of the sum of their
+// step sizes, so it costs one exponent multiply and one ex2 per state and
+// step, like a decay, and no running product.  The zero-order hold needs
+// each step's own decay for its input gain and keeps P *= dA_t instead.
+// The walk stops once every state of every lane of the warp has
 // P < 2^-40: the remaining terms are below fp32 resolution of b and of the
 // carry a*h (with A <= 0 the decays are <= 1, so P only falls; for A > 0 or
 // NaN the walk covers the whole chunk).  Same lane layout, TMA ring and
 // prologue as scan_tma_kernel; only u, dt and B are loaded.
 constexpr float kSummaryCut = 9.094947e-13f;  // 2^-40
+constexpr float kSummaryCutLog2 = -40.0f;
 
 template <typename T, int G, int NS, int TT, int S, int DISC>
 __global__ void __launch_bounds__(32)
@@ -662,6 +668,7 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
         pend[i] = pk2(0.0f, 0.0f);
         bp[i] = pk2(0.0f, 0.0f);
     }
+    float R = 0.0f;  // Euler, trapezoid: sum of delta over the steps walked
     float2* const sDU = reinterpret_cast<float2*>(smem + Lay::kDU);
     const int lane_x = g * CPW + ch;
     u64 uu[PPL];
@@ -710,22 +717,31 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
                         Bp[i2 + 1] = bq.y;
                     }
                 }
+                [[maybe_unused]] const u64 R2 = pk2(R, R);
 #pragma unroll
                 for (int i2 = 0; i2 < NP; ++i2) {
-                    const u64 x2 = mul2(dl2, A2[i2]);
-                    const u64 dA = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
-                    if constexpr (TRAP) {
-                        // this step's B*u meets the later step's deferred weight,
-                        // and this step's own (lambda*delta*u)*B its weight P
-                        bp[i2] = fma2(pend[i2], mul2(ux2, Bp[i2]), bp[i2]);
-                        bp[i2] = fma2(Pp[i2], mul2(du2, Bp[i2]), bp[i2]);
-                        pend[i2] = mul2(Pp[i2], tr2);
-                    } else {
-                        bp[i2] = fma2(Pp[i2], injection2<ZOH>(x2, dA, dl2, du2, iA2[i2], Bp[i2]),
+                    if constexpr (ZOH) {
+                        const u64 x2 = mul2(dl2, A2[i2]);
+                        const u64 dA = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
+                        bp[i2] = fma2(Pp[i2], injection2<true>(x2, dA, dl2, du2, iA2[i2], Bp[i2]),
                                       bp[i2]);
+                        Pp[i2] = mul2(Pp[i2], dA);
+                    } else {
+                        const u64 x2 = mul2(R2, A2[i2]);
+                        const u64 P = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
+                        if constexpr (TRAP) {
+                            // this step's B*u meets the later step's deferred
+                            // weight, and this step's own (lambda*delta*u)*B its
+                            // weight P
+                            bp[i2] = fma2(pend[i2], mul2(ux2, Bp[i2]), bp[i2]);
+                            bp[i2] = fma2(P, mul2(du2, Bp[i2]), bp[i2]);
+                            pend[i2] = mul2(P, tr2);
+                        } else {
+                            bp[i2] = fma2(P, mul2(du2, Bp[i2]), bp[i2]);
+                        }
                     }
-                    Pp[i2] = mul2(Pp[i2], dA);
                 }
+                if constexpr (!ZOH) R += lo2(dl2);
             }
             // (2) the previous octet's step sizes (previous tile: wait first)
             float2* const dnx = sDU + (((c + 1) & 1) * CPW + ch) * kDUStride + g;
@@ -741,10 +757,14 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
             }
             __syncwarp();
             // (3) stop once every later-decay product is below fp32 resolution
-            float pmax = 0.0f;
+            //     (Euler, trapezoid: compared through its base-2 exponent)
+            float pmax = -INFINITY;
 #pragma unroll
-            for (int i2 = 0; i2 < NP; ++i2) pmax = fmaxf(pmax, fmaxf(lo2(Pp[i2]), hi2(Pp[i2])));
-            if (__all_sync(0xffffffffu, pmax < kSummaryCut)) {
+            for (int i2 = 0; i2 < NP; ++i2) {
+                const u64 v2 = ZOH ? Pp[i2] : mul2(pk2(R, R), A2[i2]);
+                pmax = fmaxf(pmax, fmaxf(lo2(v2), hi2(v2)));
+            }
+            if (__all_sync(0xffffffffu, pmax < (ZOH ? kSummaryCut : kSummaryCutLog2))) {
                 done = true;
                 break;
             }
@@ -772,6 +792,13 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
         trap_seed<T, NS>(a, b, d, n0, tc0, bxq);
 #pragma unroll
         for (int i = 0; i < NP; ++i) bp[i] = fma2(pend[i], bxq[i], bp[i]);
+    }
+    if constexpr (!ZOH) {  // the product of every walked step's decay
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            const u64 x2 = mul2(pk2(R, R), A2[i]);
+            Pp[i] = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
+        }
     }
     const int64_t w = ((int64_t)(b * (a.K - 1) + k) * a.d_inner + d) * N + n0;
 #pragma unroll
