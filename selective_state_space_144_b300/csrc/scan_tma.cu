@@ -111,16 +111,15 @@ __device__ __forceinline__ u64 softplus2(u64 x2) {
 }
 
 // Zero-order-hold input gain of a state pair: zoh_gain (msc_device.cuh) on
-// both halves, same operations in the same order.
-__device__ __forceinline__ u64 zoh_gain2(u64 x2, u64 dA, u64 dl2, u64 iA2) {
-    u64 p = pk2(kZohC5, kZohC5);
-    p = fma2(p, x2, pk2(kZohC4, kZohC4));
+// both halves, same operations in the same order (niA2 = -iA2).
+__device__ __forceinline__ u64 zoh_gain2(u64 x2, u64 dA, u64 dl2, u64 iA2, u64 niA2) {
+    u64 p = pk2(kZohC4, kZohC4);
     p = fma2(p, x2, pk2(kZohC3, kZohC3));
     p = fma2(p, x2, pk2(kZohC2, kZohC2));
     p = fma2(p, x2, pk2(kZohC1, kZohC1));
     p = fma2(p, x2, pk2(1.0f, 1.0f));
     const u64 small = mul2(dl2, p);
-    const u64 large = mul2(add2(dA, pk2(-1.0f, -1.0f)), iA2);
+    const u64 large = fma2(dA, iA2, niA2);
     return pk2(fabsf(lo2(x2)) < kZohSwitch ? lo2(small) : lo2(large),
                fabsf(hi2(x2)) < kZohSwitch ? hi2(small) : hi2(large));
 }
@@ -128,9 +127,10 @@ __device__ __forceinline__ u64 zoh_gain2(u64 x2, u64 dA, u64 dl2, u64 iA2) {
 // Input term of a state pair: (delta*u)*B, or with zero-order hold
 // (gain*u)*B, where `du2` carries delta*u, respectively u (see octet_prologue).
 template <bool ZOH>
-__device__ __forceinline__ u64 injection2(u64 x2, u64 dA, u64 dl2, u64 du2, u64 iA2, u64 B2) {
+__device__ __forceinline__ u64 injection2(u64 x2, u64 dA, u64 dl2, u64 du2, u64 iA2, u64 niA2,
+                                          u64 B2) {
     if constexpr (ZOH)
-        return mul2(mul2(zoh_gain2(x2, dA, dl2, iA2), du2), B2);
+        return mul2(mul2(zoh_gain2(x2, dA, dl2, iA2, niA2), du2), B2);
     else
         return mul2(du2, B2);
 }
@@ -325,7 +325,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     // per-channel constants and the starting state
     const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
     const float Dd = a.D ? __ldg(a.D + d) : 0.0f;
-    u64 A2[NP], iA2[NP], hp[NP];
+    u64 A2[NP], iA2[NP], niA2[NP], hp[NP];
     const float* h0 = (a.h0 && k == 0) ? a.h0 + ((int64_t)b * a.d_inner + d) * N + n0 : nullptr;
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
@@ -333,6 +333,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         const float a0 = __ldg(Ar), a1 = __ldg(Ar + 1);
         A2[i] = pk2(a0 * kLog2e, a1 * kLog2e);
         iA2[i] = ZOH ? pk2(1.0f / a0, 1.0f / a1) : pk2(0.0f, 0.0f);
+        niA2[i] = ZOH ? pk2(-lo2(iA2[i]), -hi2(iA2[i])) : pk2(0.0f, 0.0f);
         hp[i] = h0 ? pk2(h0[2 * i], h0[2 * i + 1]) : pk2(0.0f, 0.0f);
     }
     if (k > 0) {  // state entering chunk k (carry_prefix_kernel)
@@ -493,7 +494,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                         inj = fma2(tr2, bxp[i2], mul2(du2, Bp[i2]));
                         bxp[i2] = mul2(ux2, Bp[i2]);
                     } else {
-                        inj = injection2<ZOH>(x2, dA, dl2, du2, iA2[i2], Bp[i2]);
+                        inj = injection2<ZOH>(x2, dA, dl2, du2, iA2[i2], niA2[i2], Bp[i2]);
                     }
                     hp[i2] = fma2(dA, hp[i2], inj);
                     y2 = fma2(Cp[i2], hp[i2], y2);
@@ -656,7 +657,7 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
 
     const float bias = a.dt_bias ? __ldg(a.dt_bias + d) : 0.0f;
     const u64 bias2 = pk2(bias, bias);
-    u64 A2[NP], iA2[NP], Pp[NP], bp[NP];
+    u64 A2[NP], iA2[NP], niA2[NP], Pp[NP], bp[NP];
     u64 pend[NP];  // trapezoid: P * (1-lambda)*delta of the step after, awaiting B*u
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
@@ -664,6 +665,7 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
         const float a0 = __ldg(Ar), a1 = __ldg(Ar + 1);
         A2[i] = pk2(a0 * kLog2e, a1 * kLog2e);
         iA2[i] = ZOH ? pk2(1.0f / a0, 1.0f / a1) : pk2(0.0f, 0.0f);
+        niA2[i] = ZOH ? pk2(-lo2(iA2[i]), -hi2(iA2[i])) : pk2(0.0f, 0.0f);
         Pp[i] = pk2(1.0f, 1.0f);
         pend[i] = pk2(0.0f, 0.0f);
         bp[i] = pk2(0.0f, 0.0f);
@@ -723,7 +725,8 @@ scan_summary_kernel(const __grid_constant__ CUtensorMap tm_u,
                     if constexpr (ZOH) {
                         const u64 x2 = mul2(dl2, A2[i2]);
                         const u64 dA = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
-                        bp[i2] = fma2(Pp[i2], injection2<true>(x2, dA, dl2, du2, iA2[i2], Bp[i2]),
+                        bp[i2] = fma2(Pp[i2],
+                                      injection2<true>(x2, dA, dl2, du2, iA2[i2], niA2[i2], Bp[i2]),
                                       bp[i2]);
                         Pp[i2] = mul2(Pp[i2], dA);
                     } else {
