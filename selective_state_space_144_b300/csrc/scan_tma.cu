@@ -460,12 +460,17 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 const float4 v2 = sd[j >> 1];  // steps j & ~1 and (j & ~1) + 1
                 const float vdl = (j & 1) ? v2.z : v2.x, vdu = (j & 1) ? v2.w : v2.y;
                 const u64 dl2 = pk2(vdl, vdl), du2 = pk2(vdu, vdu);
-                [[maybe_unused]] u64 tr2 = 0, ux2 = 0;
+                [[maybe_unused]] u64 tr2 = 0, ux2 = 0, qn2 = 0;
                 if constexpr (TRAP) {
                     const float4 w2 = sd2[j >> 1];
                     const float vtr = (j & 1) ? w2.z : w2.x, vux = (j & 1) ? w2.w : w2.y;
                     tr2 = pk2(vtr, vtr);
                     ux2 = pk2(vux, vux);
+                    if (j + 1 < OCT) {  // the next step's (1-lambda)*delta times this u
+                        const float4 wn = sd2[(j + 1) >> 1];
+                        const float qn = ((j + 1) & 1 ? wn.z : wn.x) * vux;
+                        qn2 = pk2(qn, qn);
+                    }
                 }
                 u64 Bp[NP], Cp[NP];
                 if constexpr (NP == 1) {  // 2 states: one 8-byte read each
@@ -491,8 +496,14 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                     const u64 dA = pk2(ex2(lo2(x2)), ex2(hi2(x2)));
                     u64 inj;
                     if constexpr (TRAP) {
-                        inj = fma2(tr2, bxp[i2], mul2(du2, Bp[i2]));
-                        bxp[i2] = mul2(ux2, Bp[i2]);
+                        // bxp: the previous step's u*B, already weighted by this
+                        // step's (1-lambda)*delta except across octets, where
+                        // the next octet's weights are not posted yet
+                        if (j == 0)
+                            inj = fma2(tr2, bxp[i2], mul2(du2, Bp[i2]));
+                        else
+                            inj = fma2(du2, Bp[i2], bxp[i2]);
+                        bxp[i2] = j + 1 < OCT ? mul2(qn2, Bp[i2]) : mul2(ux2, Bp[i2]);
                     } else {
                         inj = injection2<ZOH>(x2, dA, dl2, du2, iA2[i2], niA2[i2], Bp[i2]);
                     }
