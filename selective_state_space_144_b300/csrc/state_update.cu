@@ -70,12 +70,13 @@ state_update_kernel(UpdateArgs a) {
             load_row4<T, false>(static_cast<const T*>(a.B_prev) + b * N, n0, N, Bq);
         }
     }
+    const float tq = tra * uq;  // the previous token's u weighted by (1-lambda)*delta
     float y = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const float x2 = delta * A2[j];
         const float dA = ex2(x2);
-        const float inj = a.trap  ? fmaf(tra, uq * Bq[j], trc * Bv[j])
+        const float inj = a.trap  ? fmaf(trc, Bv[j], tq * Bq[j])
                           : a.zoh ? zoh_gain(x2, dA, delta, iA[j]) * uu * Bv[j]
                                   : du * Bv[j];
         h[j] = fmaf(dA, h[j], inj);
@@ -147,10 +148,11 @@ state_update_row_kernel(UpdateArgs a) {
     float y = 0.0f;
     if (a.trap) {  // exponential trapezoid
         const float tra = (1.0f - lt) * delta, trc = (lt * delta) * uu;
+        const float tq = tra * uq;
 #pragma unroll
         for (int n = 0; n < N; ++n) {
             const float dA = ex2(delta * (Av[n] * kLog2e));
-            h[n] = fmaf(dA, h[n], fmaf(tra, uq * sBq[n], trc * sB[n]));
+            h[n] = fmaf(dA, h[n], fmaf(trc, sB[n], tq * sBq[n]));
             y = fmaf(sC[n], h[n], y);
         }
     } else if (a.zoh) {
@@ -341,7 +343,8 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
             const float du = delta * uu;
             float hv[4] = {h.x, h.y, h.z, h.w};
             float y = 0.0f;
-            // the input term as the scan forms it (same operations, same order)
+            // the input term as the scan forms it (same operations, same order;
+            // the trapezoid's as in the scan's steps after an octet's first)
             [[maybe_unused]] float tra = 0.0f, trc = 0.0f, uq = 0.0f;
             if constexpr (TRAP) {
                 const float lt = lds_scalar<T>(reinterpret_cast<const T*>(sp + Lay::kLam) + cl);
@@ -349,6 +352,7 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
                 trc = (lt * delta) * uu;
                 uq = prev ? lds_scalar<T>(reinterpret_cast<const T*>(sp + Lay::kUp) + cl) : 0.0f;
             }
+            [[maybe_unused]] const float tq = tra * uq;  // weighted previous u
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const float x2 = delta * A2[it][k];
@@ -357,7 +361,7 @@ state_update_stream_kernel(UpdateArgs a, int nJ, int R, uint32_t wait_limit) {
                 if constexpr (ZOH)
                     inj = zoh_gain(x2, dA, delta, iA[it][k]) * uu * Bv[k];
                 else if constexpr (TRAP)
-                    inj = fmaf(tra, uq * Bq[k], trc * Bv[k]);
+                    inj = fmaf(trc, Bv[k], tq * Bq[k]);
                 else
                     inj = du * Bv[k];
                 hv[k] = fmaf(dA, hv[k], inj);
