@@ -71,7 +71,8 @@ def parse():
                          "pass on the 130M layer; for scan_bwd_ckpt, the backward "
                          "from forward-written checkpoints) on WORKLOAD "
                          "--warmup + --steps times, print nothing else "
-                         "(for ncu; see profiles/)")
+                         "(for ncu; see profiles/); a scan workload with the "
+                         "suffix _zoh or _trapezoid runs that discretisation")
     return ap.parse_args()
 
 
@@ -1156,6 +1157,12 @@ def run_profile(args):
         msc.check_device_error()
         print(f"profile run done: {name}, {args.warmup + args.steps} calls", flush=True)
         return 0
+    # a scan workload with a suffix runs that discretisation: NAME_zoh (the
+    # zero-order-hold input) or NAME_trapezoid (lambda ~ U[0, 1])
+    disc = "euler"
+    for sfx in ("_zoh", "_trapezoid"):
+        if name.endswith(sfx):
+            name, disc = name[:-len(sfx)], sfx[1:]
     w = synth.WORKLOADS[name]
     if name.startswith("decode"):
         Bb, Dd, Nn = w["batch"], w["d_inner"], w["d_state"]
@@ -1173,6 +1180,10 @@ def run_profile(args):
         a = dict(u=dev_t(x.u, kind), dt=dev_t(x.dt_raw, kind), A=dev_t(x.A, "f32"),
                  B=dev_t(x.B, kind), C=dev_t(x.C, kind), D=dev_t(x.D, "f32"),
                  z=dev_t(x.z, kind), dt_bias=dev_t(x.dt_bias, "f32"))
+        lam = None
+        if disc == "trapezoid":  # the same lambda as the bench's trapezoid workload
+            lam = dev_t(synth.round_bf16(np.random.default_rng(13).uniform(
+                0.0, 1.0, x.u.shape).astype(np.float32)), kind)
         del x
         B_, L_, D_, N_ = w["batch"], w["L"], w["d_inner"], w["d_state"]
         out = torch.empty_like(a["u"])
@@ -1180,7 +1191,13 @@ def run_profile(args):
         n = msc.scan_workspace_size(B_, L_, D_, N_, a["u"].dtype)
         wsp = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
         for _ in range(args.warmup + args.steps):
-            msc.selective_scan_fwd_ws(**a, out=out, last_state=last, workspace=wsp)
+            if lam is not None:
+                msc.selective_scan_trap_fwd(a["u"], a["dt"], lam, a["A"], a["B"], a["C"],
+                                            a["D"], a["z"], a["dt_bias"], out=out,
+                                            last_state=last, workspace=wsp)
+            else:
+                msc.selective_scan_fwd_ws(**a, out=out, last_state=last, workspace=wsp,
+                                          zoh=disc == "zoh")
     torch.cuda.synchronize(dev)
     msc.check_device_error()
     print(f"profile run done: {name}, {args.warmup + args.steps} calls", flush=True)
